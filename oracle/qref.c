@@ -1,0 +1,217 @@
+/*
+ * qref.c -- CPU oracle for the quantized-weight matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow definition that the
+ * CUDA library is checked against.  Only the tests, the smoke check and the
+ * CPU-baseline leg of the benchmark may load it.  It shares no code, header,
+ * table or helper with the CUDA library and includes nothing from it.
+ *
+ * What it computes.  Sources: the page "CUDA 后端" (colibri-analysis 09),
+ * section 1 "设备侧库 backend_cuda.cu": the device function `weight_at`
+ * turns one stored element into its value (int4 code minus 8, int2 code minus
+ * 2, the same meaning as the CPU kernel) and `quant_matmul` multiplies the
+ * per-row scale; the page "第 8 章 · 02 CUDA/Metal/Vulkan 三后端", section 四,
+ * header of qmatmul.comp: each output is the dot product of an input row with
+ * a dequantized weight row, times that weight row's scale.  In symbols,
+ *
+ *     y[s,o] = scale[o] * sum_i deq(W[o,i]) * x[s,i]
+ *
+ *   deq(f32, row, i) = ((float *)row)[i]
+ *   deq(i8,  row, i) = row[i] read as a two's-complement byte
+ *   deq(i4,  row, i) = ((row[i/2] >> 4*(i%2)) & 15) - 8     low nibble first
+ *   deq(i2,  row, i) = ((row[i/4] >> 2*(i%4)) &  3) - 2     low bits first
+ *
+ * Readings where the pages are silent (each is listed with its reason in the
+ * design notes): nibble / bit order is low-first; a row of the host layout is
+ * ceil(I*b/8) bytes and the unused high bits of its last byte are ignored; a
+ * NULL scale vector means 1.0 (the CUDA tour applies the scale for quantized
+ * tensors, the shader header applies it always; the two agree at scale 1).
+ *
+ * Every product is formed in double and summed in double in index order; the
+ * result is rounded once to f32.  The error bound that goes with it is
+ * bound[s,o] = |scale[o]| * sum_i |deq(W[o,i]) * x[s,i]|.
+ *
+ * Parallelism: OpenMP over (s, o) only; each inner sum is sequential.
+ *
+ * Parity: pinned.  The tests pin the code tables exhaustively, the bit order
+ * by one-hot rows, the accumulation by hand-expanded worked examples and by
+ * closed forms, and the scale by power-of-two invariance.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { QREF_F32 = 0, QREF_I8 = 1, QREF_I4 = 2, QREF_I2 = 3 };
+
+/* Bytes of one row of the host layout: ceil(I * bits / 8). */
+long qref_row_bytes(int fmt, long I)
+{
+    if (I < 0) return -1;
+    switch (fmt) {
+    case QREF_F32: return 4 * I;
+    case QREF_I8:  return I;
+    case QREF_I4:  return (I + 1) / 2;
+    case QREF_I2:  return (I + 3) / 4;
+    default:       return -1;
+    }
+}
+
+/* The signed value a quantized code stands for; for f32 the stored float. */
+double qref_weight(int fmt, const uint8_t *row, long i)
+{
+    switch (fmt) {
+    case QREF_F32: {
+        float f;
+        memcpy(&f, row + 4 * i, sizeof f);
+        return (double)f;
+    }
+    case QREF_I8: {
+        int v = row[i];              /* two's complement, written out */
+        if (v >= 128) v -= 256;
+        return (double)v;
+    }
+    case QREF_I4: {
+        int code = (row[i / 2] >> (4 * (i % 2))) & 0xF;
+        return (double)(code - 8);
+    }
+    case QREF_I2: {
+        int code = (row[i / 4] >> (2 * (i % 4))) & 0x3;
+        return (double)(code - 2);
+    }
+    default:
+        return NAN;
+    }
+}
+
+/* Decodes one whole row into doubles (used by the exhaustive table tests). */
+int qref_dequant_row(int fmt, long I, const uint8_t *row, double *out)
+{
+    if (qref_row_bytes(fmt, I) < 0) return -1;
+    for (long i = 0; i < I; ++i) out[i] = qref_weight(fmt, row, i);
+    return 0;
+}
+
+static int qref_threads = 0;   /* 0: OpenMP default */
+
+void qref_set_threads(int n) { qref_threads = n; }
+
+int qref_max_threads(void)
+{
+#ifdef _OPENMP
+    return qref_threads > 0 ? qref_threads : omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * y[s*O + o]     = (float)(scale[o] * sum_i deq(W[o,i]) * x[s*I + i])
+ * ydbl[s*O + o]  = the same before the final rounding (may be NULL)
+ * bound[s*O + o] = |scale[o]| * sum_i |deq(W[o,i]) * x[s*I + i]| (may be NULL)
+ *
+ * codes: host layout, row-major [O, qref_row_bytes(fmt, I)] bytes.
+ * scales: [O] floats or NULL (= 1.0).  x: [S, I] floats, row-major.
+ * Returns 0, or -1 on a bad argument.
+ */
+int qref_matmul(int fmt, long O, long I, const uint8_t *codes, const float *scales,
+                const float *x, long S, float *y, double *ydbl, double *bound)
+{
+    long rb = qref_row_bytes(fmt, I);
+    if (rb < 0 || O < 0 || S < 0) return -1;
+    if (O == 0 || S == 0) return 0;
+    if (!codes || !x || !y) return -1;
+    long n = S * O;
+#ifdef _OPENMP
+    int nt = qref_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nt)
+#endif
+    for (long so = 0; so < n; ++so) {
+        long s = so / O, o = so % O;
+        const uint8_t *row = codes + o * rb;
+        const float *xs = x + s * I;
+        double acc = 0.0, bnd = 0.0;
+        for (long i = 0; i < I; ++i) {
+            double t = qref_weight(fmt, row, i) * (double)xs[i];
+            acc += t;
+            bnd += fabs(t);
+        }
+        double sc = scales ? (double)scales[o] : 1.0;
+        y[so] = (float)(sc * acc);
+        if (ydbl) ydbl[so] = sc * acc;
+        if (bound) bound[so] = fabs(sc) * bnd;
+    }
+    return 0;
+}
+
+/*
+ * The fused gate/up pair (qmatmul_gate_up.comp in the three-backends chapter):
+ * two matmuls of equal shape on the same input x.
+ */
+int qref_matmul_gate_up(int fmt, long O, long I,
+                        const uint8_t *codes_g, const float *scales_g,
+                        const uint8_t *codes_u, const float *scales_u,
+                        const float *x, long S,
+                        float *yg, double *bound_g, float *yu, double *bound_u)
+{
+    int rc = qref_matmul(fmt, O, I, codes_g, scales_g, x, S, yg, NULL, bound_g);
+    if (rc) return rc;
+    return qref_matmul(fmt, O, I, codes_u, scales_u, x, S, yu, NULL, bound_u);
+}
+
+/*
+ * Expert glue between gate/up and down: h = silu(g) * u with the textbook
+ * silu(z) = z / (1 + e^-z), in double.  The pages name the gated
+ * up-projection but do not print the activation, so this is the plain reading.
+ * h is returned both rounded to f32 (the input format of the next matmul) and
+ * unrounded.
+ */
+void qref_silu_mul(const float *g, const float *u, long n, float *h, double *hdbl)
+{
+    for (long k = 0; k < n; ++k) {
+        double z = (double)g[k];
+        double v = z / (1.0 + exp(-z)) * (double)u[k];
+        if (h) h[k] = (float)v;
+        if (hdbl) hdbl[k] = v;
+    }
+}
+
+/*
+ * Round an f32 to the nearest bfloat16 (8 significant bits, f32's exponent
+ * range), ties to the even significand, returned as an f32.  Written from the
+ * definition: take the two bf16 neighbours of v (truncation toward zero and
+ * one unit further away), keep the nearer one, and on a tie the one whose last
+ * kept bit is 0.  Finite inputs only.
+ */
+float qref_round_bf16(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    uint32_t lo_bits = u & 0xFFFF0000u;                 /* toward zero */
+    uint32_t hi_bits = lo_bits + 0x00010000u;           /* next bf16 away from zero */
+    float lo, hi;
+    memcpy(&lo, &lo_bits, sizeof lo);
+    memcpy(&hi, &hi_bits, sizeof hi);
+    double dlo = fabs((double)v - (double)lo);
+    double dhi = fabs((double)hi - (double)v);
+    if (dlo < dhi) return lo;
+    if (dhi < dlo) return hi;
+    return ((lo_bits >> 16) & 1u) ? hi : lo;           /* tie: even significand */
+}
+
+/*
+ * The tensor-core prefill path rounds x to bf16 before the contraction; this
+ * is qref_matmul applied to the bf16-rounded x.  It is a diagnostic: the
+ * contract compares the tensor-core path with the unrounded qref_matmul.
+ */
+int qref_matmul_bf16x(int fmt, long O, long I, const uint8_t *codes, const float *scales,
+                      const float *x, long S, float *xr_scratch, float *y, double *ydbl,
+                      double *bound)
+{
+    if (S < 0 || I < 0) return -1;
+    for (long k = 0; k < S * I; ++k) xr_scratch[k] = qref_round_bf16(x[k]);
+    return qref_matmul(fmt, O, I, codes, scales, xr_scratch, S, y, ydbl, bound);
+}
