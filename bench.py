@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized-weight matmul on GB300.
+
+Default workload (one JSON line on stdout): int4 decode GEMV on the
+attention-projection shape O=12288, I=6144, S=1.  One step = one token through
+R resident copies of that [12288, 6144] int4 tensor (R * 37.9 MB > 3x the L2,
+so every step streams its weights from HBM).  value = algorithmic bytes
+(codes + scales + x + y) of all R calls / device time.  The line also carries
+the W4A16 prefill throughput (O=12288, I=6144, S=1571, TFLOP/s), the roofline
+of the dominant kernel, an end-to-end number through the host-buffer C-ABI
+call, the clocks seen during the timed region, and the CPU oracle timed on
+the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --workload sweep        # every config, one JSON line each
+
+--impl reference times the CPU oracle (the only reference implementation of
+this method that exists here) on the same workload and metric.
+Multi-GPU: one process per GPU (torchrun); each rank runs its own replica of
+the workload (the path does not shard across GPUs here: replicas only);
+value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quant-matmul weight GB/s (% HBM peak) at S=1; W4A16 TFLOP/s at S=1571"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+L2_BYTES = 129 * 2 ** 20
+
+I4 = 2
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def algorithmic_bytes(fmt_bits, O, I, S):
+    """Codes + scales + x + y of one matmul call (row padding excluded)."""
+    return O * ((I * fmt_bits + 7) // 8) + 4 * O + 4 * S * I + 4 * S * O
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch recorded from an ncu capture for this kernel,
+    valid only while the kernel's sources hash to the recorded digest."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    for ln in lines:
+        if not ln.strip() or ln.startswith("#"):
+            continue
+        kv = dict(p.split("=", 1) for p in ln.split() if "=" in p)
+        if kv.get("key") != kernel_key:
+            continue
+        files = kv.get("sources", "").split(",")
+        try:
+            if source_digest(files) != kv.get("digest"):
+                return None
+        except OSError:
+            return None
+        return float(kv["bytes_per_launch"])
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks / throttle reasons every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for ln in open(self.path).read().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_init(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class Decode:
+    """R distinct resident [O, I] tensors, S tokens: one step = R matmul calls."""
+
+    def __init__(self, q, fmt, O, I, S, R, seed=0):
+        import torch
+        import synth
+        self.q, self.fmt, self.O, self.I, self.S, self.R = q, fmt, O, I, S, R
+        self.tensors = []
+        lo, hi = {0: (1e-3, 2e-2), 1: (1e-3, 1e-2), 2: (5e-3, 2e-2), 3: (1e-3, 2e-2)}[fmt]
+        for r in range(R):
+            codes, scales = synth.quant_tensor(fmt, O, I, seed, 1 + r, lo, hi)
+            self.tensors.append(q.tensor_upload(fmt, O, I, codes, scales))
+        x = synth.activations(S, I, seed, 9999)
+        self.x = torch.from_numpy(x).cuda()
+        self.y = torch.empty((R, S, O), dtype=torch.float32, device="cuda")
+        bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
+        self.bytes_per_call = algorithmic_bytes(bits, O, I, S)
+        self.bytes_per_step = self.bytes_per_call * R
+        self.flops_per_step = 2.0 * O * I * S * R
+        self.launches_per_step = None
+
+    def step(self, stream):
+        for r in range(self.R):
+            self.q.matmul(self.tensors[r], self.x, self.y[r], self.S, stream)
+
+    def close(self):
+        for t in self.tensors:
+            t.free()
+
+
+def time_steps(wl, steps, warmup, stream, world=1):
+    import torch
+    q = wl.q
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            wl.step(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = q.kernel_launches()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        wl.step(stream)
+    e1.record(stream)
+    n1 = q.kernel_launches()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return ms, n1 - n0
+
+
+def time_e2e(wl, steps, warmup):
+    """Same decode step through b200q_matmul_host: pinned host x in, host y out,
+    copies and a stream sync inside every call."""
+    import torch
+    q = wl.q
+    xh = torch.from_numpy(wl.x.cpu().numpy()).pin_memory()
+    yh = torch.empty((wl.R, wl.S, wl.O), dtype=torch.float32).pin_memory()
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for r in range(wl.R):
+            q.matmul_host(wl.tensors[r], xh, yh[r], wl.S, st)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for r in range(wl.R):
+            q.matmul_host(wl.tensors[r], xh, yh[r], wl.S, st)
+    t1 = time.perf_counter()
+    h2d = wl.R * wl.S * wl.I * 4
+    d2h = wl.R * wl.S * wl.O * 4
+    return (t1 - t0) * 1e3, h2d, d2h
+
+
+def cpu_baseline_decode(O, I, S, fmt=I4, seconds=3.0):
+    """The oracle as it stands on the host cores, on the full decode workload
+    repeated until `seconds` of CPU time have passed."""
+    import oracle
+    import synth
+    lo, hi = (5e-3, 2e-2)
+    codes, scales = synth.quant_tensor(fmt, O, I, 0, 1, lo, hi)
+    x = synth.activations(S, I, 0, 9999)
+    oracle.set_threads(0)
+    oracle.matmul(fmt, O, I, codes, scales, x)          # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.matmul(fmt, O, I, codes, scales, x)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
+    gbs = algorithmic_bytes(bits, O, I, S) * n / dt / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": "full O=%d I=%d S=%d int4 matmul, %d calls in %.1f s" % (O, I, S, n, dt)}
+
+
+def prefill_measure(q, steps, warmup, stream):
+    """W4A16 prefill O=12288, I=6144, S=1571 through b200q_matmul (tensor-core
+    path); returns None while that path is not available."""
+    import torch
+    import synth
+    O, I, S = 12288, 6144, 1571
+    codes, scales = synth.quant_tensor(I4, O, I, 0, 1, 5e-3, 2e-2)
+    t = q.tensor_upload(I4, O, I, codes, scales)
+    try:
+        if q.matmul_path(t, S) != q.PATH_TC:
+            return None
+        x = torch.from_numpy(synth.activations(S, I, 0, 9999)).cuda()
+        y = torch.empty((S, O), dtype=torch.float32, device="cuda")
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        try:
+            q.matmul(t, x, y, S, stream)
+        except q.B200QError:
+            return None
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                q.matmul(t, x, y, S, stream)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(steps):
+            flush.zero_()                                   # L2 flush between iterations
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            q.matmul(t, x, y, S, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        flops = 2.0 * O * I * S
+        return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": S / (ms * 1e-3)}
+    finally:
+        t.free()
+
+
+# ----------------------------------------------------------------------------- main arms
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_init(args.gpus)
+    import quantized_weight_quant_gb300 as q
+    torch.cuda.set_device(local)
+    pk = peaks()
+    O, I, S = 12288, 6144, 1
+    per_copy = algorithmic_bytes(4, O, I, S)
+    R = max(16, -(-3 * L2_BYTES // per_copy))
+    wl = Decode(q, I4, O, I, S, R)
+    stream = torch.cuda.Stream()
+    with ClockSampler(local) as clk:
+        ms, launches = time_steps(wl, args.steps, args.warmup, stream, world)
+    clocks = clk.summary()
+    ms_max = max_over_ranks(ms, world)
+    total_bytes = wl.bytes_per_step * args.steps * world
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    per_launch_ms = ms / max(1, launches)
+    achieved = per_copy / (per_launch_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("decode_i4_12288x6144_s1")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes, f32 x/y",
+        "data": "synthetic (seeded: int4 codes uniform 0..15, scales U[5e-3,2e-2], x ~ N(0,1))",
+        "config": {"workload": "int4 decode GEMV O=12288 I=6144 S=1, one step = one token through "
+                               "%d resident copies" % R,
+                   "O": O, "I": I, "S": S, "copies": R, "global_batch": S * world,
+                   "l2": "inputs larger than L2: %d distinct weight copies, %.0f MB per step > 3x L2"
+                         % (R, wl.bytes_per_step / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_hbm_peak": round(100.0 * value / world / pk["hbm_gbs"], 2),
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                     "per_launch_us": round(per_launch_ms * 1e3, 3),
+                     "algorithmic_bytes_per_launch": per_copy},
+        "clocks": clocks,
+    }
+    # W4A16 prefill TFLOP/s (second half of the metric)
+    if not args.no_prefill:
+        pf = prefill_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
+        if pf is None:
+            line["prefill_w4a16"] = {"unavailable": "tensor-core path not built"}
+        else:
+            peak_tc = pk["bf16_tflops"]
+            line["prefill_w4a16"] = {
+                "workload": "W4A16 prefill O=12288 I=6144 S=1571 (x f32 -> bf16 in the call)",
+                "value": round(pf["tflops"], 2), "unit": "TFLOP/s", "ms": round(pf["ms"], 4),
+                "tokens_per_s": round(pf["tokens_per_s"], 1),
+                "roofline": {"bound": "tensor", "achieved": round(pf["tflops"], 2), "peak": peak_tc,
+                             "unit": "TFLOP/s", "frac": round(pf["tflops"] / peak_tc, 4),
+                             "traffic": recorded_traffic("prefill_i4_12288x6144_s1571"),
+                             "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}}
+    # end to end through the host-buffer C-ABI call
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 2)
+    e2e_ms_max = max_over_ranks(e2e_ms, world)
+    line["e2e"] = {"value": round(wl.bytes_per_step * e2e_steps * world / (e2e_ms_max * 1e-3) / 1e9, 2),
+                   "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "call": "b200q_matmul_host (pinned host x in, host y out, synchronous per call)"}
+    wl.close()
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(O, I, S)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle on the same workload and metric, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    O, I, S = 12288, 6144, 1
+    codes, scales = synth.quant_tensor(I4, O, I, 0, 1, 5e-3, 2e-2)
+    x = synth.activations(S, I, 0, 9999)
+    oracle.set_threads(0)
+    for _ in range(args.warmup):
+        oracle.matmul(I4, O, I, codes, scales, x)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul(I4, O, I, codes, scales, x)
+    dt = time.perf_counter() - t0
+    per_step = algorithmic_bytes(4, O, I, S)
+    value = per_step * args.steps / dt / 1e9
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes, f64 accumulation", "data": "synthetic",
+        "config": {"workload": "int4 decode GEMV O=12288 I=6144 S=1 (one step = one call of the CPU oracle "
+                               "on the whole tensor)", "O": O, "I": I, "S": S},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "full O=12288 I=6144 S=1 int4 matmul per step"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * b200q.h -- C ABI of the GB300 quantized-weight matmul library.
+ *
+ * The library holds quantized weight tensors resident in GPU memory and runs
+ *
+ *     y[s,o] = scale[o] * sum_i deq(W[o,i]) * x[s,i]
+ *
+ * against S activation rows.  Sources for the operation: the page "CUDA 后端"
+ * (colibri-analysis 09), section 1, "设备侧库 backend_cuda.cu" (the resident
+ * tensor, `weight_at`, `quant_matmul` and the five extern "C" functions of the
+ * backend), and the page "第 8 章 · 02 CUDA/Metal/Vulkan 三后端", section 四
+ * (the qmatmul.comp and qmatmul_gate_up.comp shader headers).
+ *
+ * Formats and their codes (fmt numbering 0/1/2 as on the Vulkan tensor in the
+ * three-backends chapter, section 三; int2 = 3 extends it):
+ *   B200Q_F32  stored f32 weights, deq = the float
+ *   B200Q_I8   one byte per weight, deq = two's-complement value (-128..127)
+ *   B200Q_I4   two codes per byte, low nibble first, deq = code - 8
+ *   B200Q_I2   four codes per byte, low bits first, deq = code - 2
+ * Host layout of codes: row-major [O, rb] bytes with rb = ceil(I*bits/8)
+ * (4*I for f32); the unused high bits of a row's last byte are ignored.
+ *
+ * Numerics.  Every path computes from exact dequantized integers (or the
+ * stored floats) and accumulates in f32.  Two paths:
+ *   f32 path        (S < b200q_tc_min_s(), every S for f32 and int2 tensors):
+ *                   |y - y_exact| <= 1e-5 * |scale[o]| * sum_i |deq * x|
+ *   tensor-core path (int8 / int4 tensors at S >= b200q_tc_min_s()): x is
+ *                   rounded to bf16 (nearest, ties to even) inside the call,
+ *                   products and sums are f32 on the tensor cores:
+ *                   |y - y_exact| <= 4e-3 * |scale[o]| * sum_i |deq * x|
+ * NaN and Inf inputs are outside the contract.
+ *
+ * Devices.  A tensor lives on the device that was current when it was
+ * uploaded; every call on it must be made with that device current.
+ *
+ * Errors.  Calls return B200Q_OK (0) or a negative status; the text of the
+ * last error of the calling thread is b200q_last_error().  No call falls back
+ * to the CPU.  Kernel faults that happen after an asynchronous call returned
+ * surface at the caller's next synchronization, as usual in CUDA.
+ */
+#ifndef B200Q_H
+#define B200Q_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct b200q_tensor b200q_tensor;   /* opaque, immutable after upload */
+
+enum { B200Q_F32 = 0, B200Q_I8 = 1, B200Q_I4 = 2, B200Q_I2 = 3 };
+
+enum {
+    B200Q_OK = 0,
+    B200Q_EINVAL = -1,     /* bad argument: format, shape, pointer, alignment, device */
+    B200Q_ENOMEM = -2,     /* device allocation failed */
+    B200Q_ECUDA = -3,      /* a CUDA call or kernel launch failed */
+    B200Q_ETIMEOUT = -4    /* a bounded device-side wait gave up (kernel returned early) */
+};
+
+/* Path selection for b200q_matmul_ex. */
+enum { B200Q_PATH_AUTO = 0, B200Q_PATH_F32 = 1, B200Q_PATH_TC = 2 };
+
+/*
+ * Upload one weight tensor to the current device and keep it resident.
+ * Counterpart of coli_cuda_tensor_upload ("CUDA 后端", section 1, public C ABI
+ * table: uploads weights and scales once).
+ *
+ *   fmt     B200Q_F32 / I8 / I4 / I2
+ *   O, I    output rows and input columns, both > 0
+ *   codes   HOST pointer to the host layout above ([O, rb] bytes; f32: O*I
+ *           floats).  Read during the call only; the caller keeps ownership.
+ *   scales  HOST pointer to O floats, required for quantized formats; for f32
+ *           it may be NULL, meaning 1.0 for every row.
+ *
+ * Copies synchronously and returns once the tensor is resident.  The library
+ * owns the device memory until b200q_tensor_free.  Returns NULL (and sets the
+ * last error) on a bad argument or when device memory runs out; with the
+ * environment variable B200Q_FAULT_INJECT=alloc it fails with out-of-memory
+ * before touching the GPU (for testing callers' error paths).
+ */
+b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, const float *scales);
+
+/*
+ * Free a tensor (counterpart of coli_cuda_tensor_free).  NULL is a no-op.
+ * The caller must make sure no queued kernel still reads the tensor.
+ */
+void b200q_tensor_free(b200q_tensor *t);
+
+/*
+ * y = matmul(t, x) on `stream` (counterpart of coli_cuda_matmul, "CUDA 后端"
+ * section 1; the formula is the qmatmul.comp header, three-backends chapter
+ * section 四).
+ *
+ *   x       DEVICE pointer, [S, I] f32 row-major, contiguous, 16-byte aligned
+ *   y       DEVICE pointer, [S, O] f32 row-major, 16-byte aligned; fully
+ *           overwritten; must not overlap x
+ *   S       number of activation rows, >= 0 (0 is a no-op)
+ *   stream  a cudaStream_t passed as void*; NULL is the legacy default stream
+ *
+ * Asynchronous: returns after the kernels are queued.  The caller owns x and y
+ * and must keep them alive until the stream reaches this work.  Path: the f32
+ * path for S < b200q_tc_min_s() or for f32 / int2 tensors, else the
+ * tensor-core path.  Returns B200Q_OK, B200Q_EINVAL or B200Q_ECUDA.
+ */
+int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *stream);
+
+/*
+ * As b200q_matmul with an explicit path: B200Q_PATH_AUTO (same as
+ * b200q_matmul), B200Q_PATH_F32 (the f32-accurate path at any S, any format)
+ * or B200Q_PATH_TC (the bf16 tensor-core path at any S >= 1; int8 and int4
+ * tensors only, B200Q_EINVAL otherwise).
+ */
+int b200q_matmul_ex(const b200q_tensor *t, const float *x, float *y, int S, int path,
+                    void *stream);
+
+/*
+ * The path b200q_matmul takes for this tensor at this S: B200Q_PATH_F32 or
+ * B200Q_PATH_TC, or a negative status for a bad argument.
+ */
+int b200q_matmul_path(const b200q_tensor *t, int S);
+
+/*
+ * Threshold S from which int8 / int4 tensors take the tensor-core path:
+ * 16 by default (the colibri CUDA docs, "The GPU-resident pipeline" section:
+ * the Tensor-Core W4A16 dispatch pays from 16 rows up), or the value of the
+ * environment variable B200Q_TC_MIN_S (>= 1) read at the first call.
+ */
+int b200q_tc_min_s(void);
+
+/*
+ * Fused gate/up pair: yg = matmul(tg, x) and yu = matmul(tu, x) in one pass
+ * that reads x once (qmatmul_gate_up.comp, three-backends chapter, section 四
+ * list of shaders).  tg and tu must have the same fmt, O, I and device.  The
+ * pointer rules of b200q_matmul hold for x, yg, yu; yg and yu must not
+ * overlap each other or x.  Same numerics and path rule as b200q_matmul.
+ */
+int b200q_matmul_gate_up(const b200q_tensor *tg, const b200q_tensor *tu, const float *x,
+                         float *yg, float *yu, int S, void *stream);
+
+/*
+ * Expert glue: h[k] = silu(g[k]) * u[k], silu(z) = z / (1 + e^-z), for
+ * k < n, f32, on `stream`.  g, u, h are DEVICE pointers to n floats, 16-byte
+ * aligned; h may equal g or u (in place) but must not partially overlap them.
+ * The activation itself is not printed on the pages; this is the textbook
+ * SiLU of a gated MoE expert.
+ */
+int b200q_silu_mul(const float *g, const float *u, float *h, long n, void *stream);
+
+/*
+ * Host-buffer call in the style of the reference backend ("CUDA 后端",
+ * section 1: each matmul copies its input to the GPU, runs the kernel and
+ * copies the result back, blocking): copies x_host ([S, I] f32) to a
+ * library-owned device staging buffer on `stream`, runs b200q_matmul, copies
+ * y back to y_host ([S, O] f32) and synchronizes `stream` before returning.
+ * Pinned host memory gives the fastest copies; pageable memory works.  The
+ * staging buffer belongs to the device and grows as needed (it is allocated
+ * with cudaMalloc); calls on one device from several threads are serialized.
+ */
+int b200q_matmul_host(const b200q_tensor *t, const float *x_host, float *y_host, int S,
+                      void *stream);
+
+/*
+ * Describe a tensor.  Any out pointer may be NULL.  device_bytes is the size of
+ * the resident copy (codes with row padding plus scales).
+ */
+int b200q_tensor_info(const b200q_tensor *t, int *fmt, int *O, int *I, int *device,
+                      long long *device_bytes);
+
+/*
+ * Number of kernels this process has launched through the library so far (all
+ * devices, all threads).  Lets a caller count the launches inside a timed
+ * region.
+ */
+long long b200q_kernel_launches(void);
+
+/* Text of the calling thread's last error ("" if none). */
+const char *b200q_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B200Q_H */

@@ -1,0 +1,211 @@
+"""Python binding of the b200q C ABI (``include/b200q.h``).
+
+Argument marshalling only: every step of the matmul runs in the CUDA library
+``libb200q.so`` built from ``csrc/``.  There is no CPU fallback; importing the
+package without the built library raises.
+
+Device arrays are passed as torch CUDA tensors (their ``data_ptr()``) or as
+raw integer device pointers.  ``stream`` is None (torch's current stream on
+the current device), a ``torch.cuda.Stream``, or a raw ``cudaStream_t`` int.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+F32, I8, I4, I2 = 0, 1, 2, 3
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4
+PATH_AUTO, PATH_F32, PATH_TC = 0, 1, 2
+FORMATS = {"f32": F32, "i8": I8, "i4": I4, "i2": I2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libb200q.so")
+
+
+class B200QError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("b200q status %d: %s" % (status, message))
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libb200q.so is not built: run `python -c \"import __graft_entry__ as g; g.build()\"` "
+                          "or `python quantized_weight_quant_gb300/build.py`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, ci, cl, cll, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_longlong, ctypes.c_float
+    L.b200q_tensor_upload.argtypes = [ci, ci, ci, vp, vp]
+    L.b200q_tensor_upload.restype = vp
+    L.b200q_tensor_free.argtypes = [vp]
+    L.b200q_tensor_free.restype = None
+    L.b200q_matmul.argtypes = [vp, vp, vp, ci, vp]
+    L.b200q_matmul.restype = ci
+    L.b200q_matmul_ex.argtypes = [vp, vp, vp, ci, ci, vp]
+    L.b200q_matmul_ex.restype = ci
+    L.b200q_matmul_path.argtypes = [vp, ci]
+    L.b200q_matmul_path.restype = ci
+    L.b200q_tc_min_s.argtypes = []
+    L.b200q_tc_min_s.restype = ci
+    L.b200q_matmul_gate_up.argtypes = [vp, vp, vp, vp, vp, ci, vp]
+    L.b200q_matmul_gate_up.restype = ci
+    L.b200q_silu_mul.argtypes = [vp, vp, vp, cl, vp]
+    L.b200q_silu_mul.restype = ci
+    L.b200q_matmul_host.argtypes = [vp, vp, vp, ci, vp]
+    L.b200q_matmul_host.restype = ci
+    L.b200q_tensor_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci),
+                                    ctypes.POINTER(ci), ctypes.POINTER(cll)]
+    L.b200q_tensor_info.restype = ci
+    L.b200q_kernel_launches.argtypes = []
+    L.b200q_kernel_launches.restype = cll
+    L.b200q_last_error.argtypes = []
+    L.b200q_last_error.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.b200q_last_error().decode()
+
+
+def kernel_launches() -> int:
+    """Kernels launched through the library so far in this process."""
+    return int(lib.b200q_kernel_launches())
+
+
+def tc_min_s() -> int:
+    return int(lib.b200q_tc_min_s())
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise B200QError(rc, last_error())
+    return rc
+
+
+def _dptr(a) -> int:
+    """Device pointer of a torch CUDA tensor (checked contiguous f32) or an int."""
+    if a is None:
+        return 0
+    if isinstance(a, int):
+        return a
+    import torch
+    if not isinstance(a, torch.Tensor):
+        raise TypeError("expected a torch CUDA tensor or an int device pointer")
+    if not a.is_cuda:
+        raise ValueError("expected a CUDA tensor, got a %s tensor" % a.device)
+    if a.dtype != torch.float32 or not a.is_contiguous():
+        raise ValueError("expected a contiguous float32 tensor")
+    return a.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class QTensor:
+    """A weight tensor resident on the GPU (owns its b200q_tensor handle)."""
+
+    def __init__(self, handle: int, fmt: int, O: int, I: int):
+        self.handle, self.fmt, self.O, self.I = handle, fmt, O, I
+
+    def free(self):
+        if self.handle:
+            lib.b200q_tensor_free(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+        return False
+
+    def info(self):
+        return tensor_info(self)
+
+
+def _h(t) -> int:
+    return t.handle if isinstance(t, QTensor) else t
+
+
+def tensor_upload(fmt: int, O: int, I: int, codes, scales) -> QTensor:
+    """Upload host codes ([O, row_bytes] uint8, or f32 [O, I] for fmt F32) and
+    host scales (f32 [O], or None for F32) to the current device."""
+    codes = np.ascontiguousarray(codes)
+    if codes.dtype != np.uint8:
+        codes = codes.view(np.uint8)
+    if scales is not None:
+        scales = np.ascontiguousarray(scales, dtype=np.float32)
+        if scales.size != O:
+            raise ValueError("scales must hold O floats")
+    bits = {F32: 32, I8: 8, I4: 4, I2: 2}.get(fmt)
+    if bits is not None and codes.size != O * ((I * bits + 7) // 8):
+        raise ValueError("codes hold %d bytes, expected O * row_bytes = %d"
+                         % (codes.size, O * ((I * bits + 7) // 8)))
+    h = lib.b200q_tensor_upload(fmt, O, I, codes.ctypes.data,
+                                None if scales is None else scales.ctypes.data)
+    if not h:
+        msg = last_error()
+        raise B200QError(ENOMEM if "memory" in msg else EINVAL, msg)
+    return QTensor(h, fmt, O, I)
+
+
+def tensor_free(t) -> None:
+    if isinstance(t, QTensor):
+        t.free()
+    else:
+        lib.b200q_tensor_free(t)
+
+
+def tensor_info(t):
+    f, o, i, d = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    nb = ctypes.c_longlong()
+    _check(lib.b200q_tensor_info(_h(t), ctypes.byref(f), ctypes.byref(o), ctypes.byref(i),
+                                 ctypes.byref(d), ctypes.byref(nb)))
+    return {"fmt": f.value, "O": o.value, "I": i.value, "device": d.value,
+            "device_bytes": nb.value}
+
+
+def matmul(t, x, y, S: int, stream=None) -> None:
+    _check(lib.b200q_matmul(_h(t), _dptr(x), _dptr(y), S, _stream(stream)))
+
+
+def matmul_ex(t, x, y, S: int, path: int, stream=None) -> None:
+    _check(lib.b200q_matmul_ex(_h(t), _dptr(x), _dptr(y), S, path, _stream(stream)))
+
+
+def matmul_path(t, S: int) -> int:
+    return _check(lib.b200q_matmul_path(_h(t), S))
+
+
+def matmul_gate_up(tg, tu, x, yg, yu, S: int, stream=None) -> None:
+    _check(lib.b200q_matmul_gate_up(_h(tg), _h(tu), _dptr(x), _dptr(yg), _dptr(yu), S,
+                                    _stream(stream)))
+
+
+def silu_mul(g, u, h, n: int, stream=None) -> None:
+    _check(lib.b200q_silu_mul(_dptr(g), _dptr(u), _dptr(h), n, _stream(stream)))
+
+
+def matmul_host(t, x_host, y_host, S: int, stream=None) -> None:
+    """x_host / y_host: host f32 buffers (numpy arrays or pinned torch CPU tensors)."""
+    def hptr(a):
+        if isinstance(a, np.ndarray):
+            if a.dtype != np.float32 or not a.flags.c_contiguous:
+                raise ValueError("expected a contiguous float32 array")
+            return a.ctypes.data
+        if isinstance(a, int):
+            return a
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError("expected a contiguous host tensor")
+        return a.data_ptr()
+    _check(lib.b200q_matmul_host(_h(t), hptr(x_host), hptr(y_host), S, _stream(stream)))

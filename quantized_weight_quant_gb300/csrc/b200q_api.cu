@@ -1,0 +1,355 @@
+// Host side of the b200q C ABI: argument checks, tensor upload / free, path
+// selection, the host-staged call and error reporting.  Every computation is
+// done by the kernels; nothing here runs on the CPU besides bookkeeping.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "qwq_internal.h"
+
+namespace qwq {
+
+// Kernels of the other translation units.
+cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
+                          cudaStream_t st, bool *handled);
+cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu,
+                              int S, cudaStream_t st, bool *handled);
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(e == cudaErrorMemoryAllocation ? B200Q_ENOMEM : B200Q_ECUDA, "%s: %s (%s)", what,
+                cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const char *pa = (const char *)a, *pb = (const char *)b;
+    return pa < pb + nb && pb < pa + na;
+}
+
+long long host_row_bytes(int fmt, long long I) { return (I * fmt_bits(fmt) + 7) / 8; }
+
+int check_tensor(const b200q_tensor *h, const char *who) {
+    if (!h) return fail(B200Q_EINVAL, "%s: tensor is NULL", who);
+    const Tensor *t = reinterpret_cast<const Tensor *>(h);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    if (dev != t->device)
+        return fail(B200Q_EINVAL, "%s: tensor lives on device %d but device %d is current", who, t->device,
+                    dev);
+    return B200Q_OK;
+}
+
+int check_io(const Tensor &t, const float *x, const float *y, int S, const char *who) {
+    if (!x || !y) return fail(B200Q_EINVAL, "%s: x and y must be device pointers, got NULL", who);
+    if (!aligned16(x) || !aligned16(y)) return fail(B200Q_EINVAL, "%s: x and y must be 16-byte aligned", who);
+    if (overlap(x, (size_t)S * t.I * 4, y, (size_t)S * t.O * 4))
+        return fail(B200Q_EINVAL, "%s: x and y overlap", who);
+    return B200Q_OK;
+}
+
+std::atomic<long long> g_launches{0};
+
+int g_tc_min_s = 0;
+std::once_flag g_tc_once;
+
+struct Staging {
+    std::mutex m;
+    void *buf = nullptr;
+    size_t cap = 0;
+};
+Staging g_staging[64];
+
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int tc_min_s() {
+    std::call_once(g_tc_once, [] {
+        int v = 16;
+        if (const char *s = std::getenv("B200Q_TC_MIN_S")) {
+            int p = std::atoi(s);
+            if (p >= 1) v = p;
+        }
+        g_tc_min_s = v;
+    });
+    return g_tc_min_s;
+}
+
+int select_path(const Tensor &t, int S, int path) {
+    if (path == B200Q_PATH_AUTO)
+        return ((t.fmt == B200Q_I4 || t.fmt == B200Q_I8) && S >= tc_min_s()) ? B200Q_PATH_TC : B200Q_PATH_F32;
+    return path;
+}
+
+int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S, int path,
+               cudaStream_t st, const char *who) {
+    if (S == 0) return B200Q_OK;
+    path = select_path(t, S, path);
+    cudaError_t e = cudaSuccess;
+    bool handled = false;
+    if (path == B200Q_PATH_TC) {
+        if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
+            return fail(B200Q_EINVAL, "%s: the tensor-core path takes int8 and int4 tensors only", who);
+        e = launch_prefill_tc(t, tu, x, y, yu, S, st, &handled);
+        if (e == cudaSuccess && !handled)
+            return fail(B200Q_ECUDA, "%s: no tensor-core kernel for this shape", who);
+    } else {
+        e = launch_decode(t, tu, x, y, yu, S, st, &handled);
+        if (e == cudaSuccess && !handled) e = launch_qmv_simt(t, tu, x, y, yu, S, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return B200Q_OK;
+}
+
+}  // namespace qwq
+
+using namespace qwq;
+
+extern "C" {
+
+const char *b200q_last_error(void) { return g_err.c_str(); }
+
+long long b200q_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int b200q_tc_min_s(void) { return tc_min_s(); }
+
+b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, const float *scales) {
+    g_err.clear();
+    if (fmt_bits(fmt) == 0) {
+        fail(B200Q_EINVAL, "b200q_tensor_upload: unknown format %d", fmt);
+        return nullptr;
+    }
+    if (O <= 0 || I <= 0) {
+        fail(B200Q_EINVAL, "b200q_tensor_upload: O and I must be > 0 (got O=%d, I=%d)", O, I);
+        return nullptr;
+    }
+    if (!codes) {
+        fail(B200Q_EINVAL, "b200q_tensor_upload: codes is NULL");
+        return nullptr;
+    }
+    if (!scales && fmt != B200Q_F32) {
+        fail(B200Q_EINVAL, "b200q_tensor_upload: scales are required for quantized formats");
+        return nullptr;
+    }
+    if (const char *fi = std::getenv("B200Q_FAULT_INJECT")) {
+        if (std::strcmp(fi, "alloc") == 0) {
+            fail(B200Q_ENOMEM, "b200q_tensor_upload: out of device memory (injected by B200Q_FAULT_INJECT)");
+            return nullptr;
+        }
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "b200q_tensor_upload: cudaGetDevice");
+        return nullptr;
+    }
+    Tensor *t = new (std::nothrow) Tensor();
+    if (!t) {
+        fail(B200Q_ENOMEM, "b200q_tensor_upload: out of host memory");
+        return nullptr;
+    }
+    const long long rb = host_row_bytes(fmt, I);
+    t->fmt = fmt;
+    t->O = O;
+    t->I = I;
+    t->device = dev;
+    t->o_pad = (O + kRowTile - 1) / kRowTile * kRowTile;
+    t->ld = (rb + kRowAlign - 1) / kRowAlign * kRowAlign;
+    t->k_pad = t->ld * 8 / fmt_bits(fmt);
+    const size_t code_bytes = (size_t)t->o_pad * t->ld;
+    t->bytes = code_bytes + (size_t)t->o_pad * sizeof(float);
+    void *mem = nullptr;
+    e = cudaMalloc(&mem, t->bytes);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "b200q_tensor_upload: cudaMalloc");
+        cudaGetLastError();
+        delete t;
+        return nullptr;
+    }
+    t->codes = (uint8_t *)mem;
+    t->scales = (float *)((uint8_t *)mem + code_bytes);
+
+    cudaStream_t st = nullptr;
+    e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaMemsetAsync(t->codes, zero_byte(fmt), code_bytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(t->scales, 0, (size_t)t->o_pad * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(t->codes, (size_t)t->ld, codes, (size_t)rb, (size_t)rb, (size_t)O,
+                              cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = launch_fix_row_tails(*t, rb, st);
+    if (e == cudaSuccess) {
+        if (scales) {
+            e = cudaMemcpyAsync(t->scales, scales, (size_t)O * sizeof(float), cudaMemcpyHostToDevice, st);
+        } else {
+            // f32 without scales: 1.0 for every real row (0x3f800000 as four bytes is not a
+            // memset pattern, so copy from a host vector)
+            float *ones = (float *)std::malloc((size_t)O * sizeof(float));
+            if (!ones) {
+                e = cudaErrorMemoryAllocation;
+            } else {
+                for (int i = 0; i < O; ++i) ones[i] = 1.0f;
+                e = cudaMemcpyAsync(t->scales, ones, (size_t)O * sizeof(float), cudaMemcpyHostToDevice, st);
+                if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+                std::free(ones);
+            }
+        }
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (st) cudaStreamDestroy(st);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "b200q_tensor_upload: copy");
+        cudaGetLastError();
+        cudaFree(mem);
+        delete t;
+        return nullptr;
+    }
+    return reinterpret_cast<b200q_tensor *>(t);
+}
+
+void b200q_tensor_free(b200q_tensor *h) {
+    if (!h) return;
+    Tensor *t = reinterpret_cast<Tensor *>(h);
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != t->device) cudaSetDevice(t->device);
+    cudaFree(t->codes);
+    if (cur != t->device && cur >= 0) cudaSetDevice(cur);
+    delete t;
+}
+
+int b200q_tensor_info(const b200q_tensor *h, int *fmt, int *O, int *I, int *device, long long *device_bytes) {
+    if (!h) return fail(B200Q_EINVAL, "b200q_tensor_info: tensor is NULL");
+    const Tensor *t = reinterpret_cast<const Tensor *>(h);
+    if (fmt) *fmt = t->fmt;
+    if (O) *O = t->O;
+    if (I) *I = t->I;
+    if (device) *device = t->device;
+    if (device_bytes) *device_bytes = (long long)t->bytes;
+    return B200Q_OK;
+}
+
+int b200q_matmul_path(const b200q_tensor *h, int S) {
+    if (!h) return fail(B200Q_EINVAL, "b200q_matmul_path: tensor is NULL");
+    if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_path: S must be >= 0");
+    return select_path(*reinterpret_cast<const Tensor *>(h), S, B200Q_PATH_AUTO);
+}
+
+int b200q_matmul_ex(const b200q_tensor *h, const float *x, float *y, int S, int path, void *stream) {
+    int rc = check_tensor(h, "b200q_matmul");
+    if (rc) return rc;
+    const Tensor &t = *reinterpret_cast<const Tensor *>(h);
+    if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul: S must be >= 0 (got %d)", S);
+    if (path != B200Q_PATH_AUTO && path != B200Q_PATH_F32 && path != B200Q_PATH_TC)
+        return fail(B200Q_EINVAL, "b200q_matmul: unknown path %d", path);
+    if (S == 0) return B200Q_OK;
+    rc = check_io(t, x, y, S, "b200q_matmul");
+    if (rc) return rc;
+    return run_matmul(t, nullptr, x, y, nullptr, S, path, (cudaStream_t)stream, "b200q_matmul");
+}
+
+int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *stream) {
+    return b200q_matmul_ex(t, x, y, S, B200Q_PATH_AUTO, stream);
+}
+
+int b200q_matmul_gate_up(const b200q_tensor *hg, const b200q_tensor *hu, const float *x, float *yg, float *yu,
+                         int S, void *stream) {
+    int rc = check_tensor(hg, "b200q_matmul_gate_up");
+    if (rc) return rc;
+    rc = check_tensor(hu, "b200q_matmul_gate_up");
+    if (rc) return rc;
+    const Tensor &tg = *reinterpret_cast<const Tensor *>(hg);
+    const Tensor &tu = *reinterpret_cast<const Tensor *>(hu);
+    if (tg.fmt != tu.fmt || tg.O != tu.O || tg.I != tu.I)
+        return fail(B200Q_EINVAL, "b200q_matmul_gate_up: gate and up differ in format or shape");
+    if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_gate_up: S must be >= 0 (got %d)", S);
+    if (S == 0) return B200Q_OK;
+    rc = check_io(tg, x, yg, S, "b200q_matmul_gate_up");
+    if (rc) return rc;
+    rc = check_io(tu, x, yu, S, "b200q_matmul_gate_up");
+    if (rc) return rc;
+    if (overlap(yg, (size_t)S * tg.O * 4, yu, (size_t)S * tu.O * 4))
+        return fail(B200Q_EINVAL, "b200q_matmul_gate_up: yg and yu overlap");
+    return run_matmul(tg, &tu, x, yg, yu, S, B200Q_PATH_AUTO, (cudaStream_t)stream, "b200q_matmul_gate_up");
+}
+
+int b200q_silu_mul(const float *g, const float *u, float *h, long n, void *stream) {
+    if (n < 0) return fail(B200Q_EINVAL, "b200q_silu_mul: n must be >= 0");
+    if (n == 0) return B200Q_OK;
+    if (!g || !u || !h) return fail(B200Q_EINVAL, "b200q_silu_mul: NULL pointer");
+    if (!aligned16(g) || !aligned16(u) || !aligned16(h))
+        return fail(B200Q_EINVAL, "b200q_silu_mul: pointers must be 16-byte aligned");
+    const size_t nb = (size_t)n * 4;
+    if ((h != g && overlap(h, nb, g, nb)) || (h != u && overlap(h, nb, u, nb)))
+        return fail(B200Q_EINVAL, "b200q_silu_mul: h partially overlaps g or u");
+    cudaError_t e = launch_silu_mul(g, u, h, n, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_silu_mul");
+    return B200Q_OK;
+}
+
+int b200q_matmul_host(const b200q_tensor *h, const float *x_host, float *y_host, int S, void *stream) {
+    int rc = check_tensor(h, "b200q_matmul_host");
+    if (rc) return rc;
+    const Tensor &t = *reinterpret_cast<const Tensor *>(h);
+    if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_host: S must be >= 0 (got %d)", S);
+    if (S == 0) return B200Q_OK;
+    if (!x_host || !y_host) return fail(B200Q_EINVAL, "b200q_matmul_host: NULL host pointer");
+    if (t.device < 0 || t.device >= 64) return fail(B200Q_EINVAL, "b200q_matmul_host: device index too large");
+    const size_t xb = (size_t)S * t.I * 4, yb = (size_t)S * t.O * 4;
+    const size_t xb_al = (xb + 255) / 256 * 256;
+    cudaStream_t st = (cudaStream_t)stream;
+    Staging &sg = g_staging[t.device];
+    std::lock_guard<std::mutex> lock(sg.m);
+    cudaError_t e = cudaSuccess;
+    if (sg.cap < xb_al + yb) {
+        if (sg.buf) {
+            e = cudaStreamSynchronize(st);
+            if (e == cudaSuccess) e = cudaFree(sg.buf);
+            sg.buf = nullptr;
+            sg.cap = 0;
+            if (e != cudaSuccess) return cuda_fail(e, "b200q_matmul_host: free staging");
+        }
+        e = cudaMalloc(&sg.buf, xb_al + yb);
+        if (e != cudaSuccess) {
+            sg.buf = nullptr;
+            cudaGetLastError();
+            return cuda_fail(e, "b200q_matmul_host: staging allocation");
+        }
+        sg.cap = xb_al + yb;
+    }
+    float *xd = (float *)sg.buf;
+    float *yd = (float *)((char *)sg.buf + xb_al);
+    e = cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_matmul_host: copy x to device");
+    rc = run_matmul(t, nullptr, xd, yd, nullptr, S, B200Q_PATH_AUTO, st, "b200q_matmul_host");
+    if (rc) return rc;
+    e = cudaMemcpyAsync(y_host, yd, yb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_matmul_host: copy y to host");
+    return B200Q_OK;
+}
+
+}  // extern "C"

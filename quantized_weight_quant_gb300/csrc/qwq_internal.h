@@ -1,0 +1,59 @@
+// Internal declarations of the b200q library (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/b200q.h"
+
+namespace qwq {
+
+// Device copy of one weight tensor.
+//
+// codes: [o_pad, ld] bytes, row-major.  A row holds the host row's bytes
+//        followed by padding up to ld (a multiple of kRowAlign).  Padding
+//        bytes, the unused high bits of a row's last byte, and the rows
+//        o >= O all hold the format's zero-point code, so they decode to 0.
+// scales: [o_pad] f32; rows o >= O have scale 0.
+struct Tensor {
+    int fmt;
+    int O, I;
+    int device;
+    int o_pad;        // O rounded up to kRowTile
+    long long ld;     // device row stride in bytes
+    long long k_pad;  // elements per padded row = ld * 8 / bits
+    uint8_t *codes;
+    float *scales;
+    size_t bytes;     // one allocation: codes then scales
+};
+
+constexpr int kRowAlign = 128;  // bytes; rows start on 128-byte boundaries
+constexpr int kRowTile = 128;   // O is padded to a multiple of this
+
+inline int fmt_bits(int fmt) {
+    return fmt == B200Q_F32 ? 32 : fmt == B200Q_I8 ? 8 : fmt == B200Q_I4 ? 4 : fmt == B200Q_I2 ? 2 : 0;
+}
+
+// Zero-point code replicated over a byte: decodes to 0 in every position.
+inline uint8_t zero_byte(int fmt) {
+    return fmt == B200Q_I4 ? 0x88 : fmt == B200Q_I2 ? 0xAA : 0x00;
+}
+
+// Counts kernel launches made through the library (b200q_kernel_launches).
+void count_launch(int n = 1);
+
+// ---- kernels (launchers return cudaGetLastError() after the launch) ----
+
+// Tail fix after the upload copy: forces the unused high bits of every row's
+// last host byte to the zero-point pattern.
+cudaError_t launch_fix_row_tails(const Tensor &t, long long rb, cudaStream_t st);
+
+// f32-accurate SIMT path, any format, any S.  With tu != nullptr the launch
+// also computes yu = matmul(tu, x) (gate/up pair, same shape as t).
+cudaError_t launch_qmv_simt(const Tensor &t, const Tensor *tu, const float *x, float *y,
+                            float *yu, int S, cudaStream_t st);
+
+cudaError_t launch_silu_mul(const float *g, const float *u, float *h, long n, cudaStream_t st);
+
+}  // namespace qwq

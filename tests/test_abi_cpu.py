@@ -1,0 +1,96 @@
+"""The C-ABI library loads and exports every declared symbol; host-side error
+paths that need no GPU (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "b200q.h")
+
+
+@pytest.fixture(scope="module")
+def built_lib():
+    from quantized_weight_quant_gb300 import build as B
+    return B.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(b200q_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_core_calls():
+    names = declared_functions()
+    for n in ("b200q_tensor_upload", "b200q_matmul", "b200q_matmul_gate_up", "b200q_tensor_free",
+              "b200q_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(built_lib):
+    L = ctypes.CDLL(built_lib)
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_names_match_the_abi(built_lib):
+    import quantized_weight_quant_gb300 as q
+    for n in declared_functions():
+        assert hasattr(q, n[len("b200q_"):]), n
+
+
+def test_upload_argument_errors(built_lib):
+    import quantized_weight_quant_gb300 as q
+    L = q.lib
+    codes = np.zeros(64, np.uint8)
+    sc = np.ones(4, np.float32)
+    assert not L.b200q_tensor_upload(9, 4, 16, codes.ctypes.data, sc.ctypes.data)
+    assert "format" in q.last_error()
+    assert not L.b200q_tensor_upload(q.I8, 0, 16, codes.ctypes.data, sc.ctypes.data)
+    assert "O and I" in q.last_error()
+    assert not L.b200q_tensor_upload(q.I8, 4, -1, codes.ctypes.data, sc.ctypes.data)
+    assert not L.b200q_tensor_upload(q.I8, 4, 16, None, sc.ctypes.data)
+    assert "NULL" in q.last_error()
+    assert not L.b200q_tensor_upload(q.I4, 4, 16, codes.ctypes.data, None)
+    assert "scales" in q.last_error()
+
+
+def test_fault_injection_alloc(built_lib, monkeypatch):
+    import quantized_weight_quant_gb300 as q
+    monkeypatch.setenv("B200Q_FAULT_INJECT", "alloc")
+    codes = np.zeros(64, np.uint8)
+    sc = np.ones(4, np.float32)
+    with pytest.raises(q.B200QError) as ei:
+        q.tensor_upload(q.I8, 4, 16, codes, sc)
+    assert ei.value.status == q.ENOMEM
+    assert "injected" in q.last_error()
+
+
+def test_null_tensor_calls(built_lib):
+    import quantized_weight_quant_gb300 as q
+    L = q.lib
+    assert L.b200q_matmul(None, None, None, 1, None) == q.EINVAL
+    assert L.b200q_matmul_gate_up(None, None, None, None, None, 1, None) == q.EINVAL
+    assert L.b200q_matmul_path(None, 1) == q.EINVAL
+    assert L.b200q_matmul_host(None, None, None, 1, None) == q.EINVAL
+    assert L.b200q_tensor_info(None, None, None, None, None, None) == q.EINVAL
+    L.b200q_tensor_free(None)            # no-op
+
+
+def test_silu_mul_argument_errors(built_lib):
+    import quantized_weight_quant_gb300 as q
+    L = q.lib
+    assert L.b200q_silu_mul(None, None, None, 0, None) == q.OK      # n == 0 is a no-op
+    assert L.b200q_silu_mul(None, None, None, -1, None) == q.EINVAL
+    assert L.b200q_silu_mul(None, None, None, 4, None) == q.EINVAL
+    assert L.b200q_silu_mul(16, 32, 49, 4, None) == q.EINVAL         # misaligned h
+    assert L.b200q_silu_mul(16, 64, 32, 8, None) == q.EINVAL         # h partially overlaps g
+
+
+def test_tc_threshold_default(built_lib):
+    import quantized_weight_quant_gb300 as q
+    if "B200Q_TC_MIN_S" not in os.environ:
+        assert q.tc_min_s() == 16
