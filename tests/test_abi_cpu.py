@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "b200q.h")
 
 @pytest.fixture(scope="module")
 def built_lib():
-    from quantized_weight_quant_gb300 import build as B
-    return B.build()
+    import __graft_entry__
+    return __graft_entry__._build_module().build()
 
 
 def declared_functions():
