@@ -38,7 +38,7 @@ def test_int8_256x512_s1(q):
 
 @pytest.mark.parametrize("fmt", list(FMTS.values()), ids=list(FMTS))
 @pytest.mark.parametrize("O,I", [(1, 1), (7, 3), (129, 31), (33, 33), (7, 1023), (130, 257), (64, 1000)])
-@pytest.mark.parametrize("S", [1, 2, 5, 8])
+@pytest.mark.parametrize("S", [1, 2, 5, 8, 11, 15])
 def test_ragged_shapes(q, fmt, O, I, S):
     _check(q, fmt, O, I, S, seed=O * 1000 + I)
 
