@@ -402,6 +402,85 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Every decode config as one JSON line each (device time, weight rotation
+    larger than L2), then the MoE layer and the prefill."""
+    import torch
+    import quantized_weight_quant_gb300 as q
+    torch.cuda.set_device(0)
+    pk = peaks()
+    stream = torch.cuda.Stream()
+    cases = [("int8 256x512", 1, 256, 512, 1)]
+    cases += [("int4 12288x6144", I4, 12288, 6144, s) for s in (1, 4)]
+    cases += [("%s 8192x8192" % n, f, 8192, 8192, s) for n, f in (("f32", 0), ("int8", 1), ("int4", 2), ("int2", 3))
+              for s in (1, 2, 8)]
+    for name, fmt, O, I, S in cases:
+        bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
+        per = algorithmic_bytes(bits, O, I, S)
+        R = max(2, min(64, -(-3 * L2_BYTES // per)))
+        wl = Decode(q, fmt, O, I, S, R)
+        ms, launches = time_steps(wl, args.steps, args.warmup, stream)
+        gbs = wl.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": "%s S=%d" % (name, S), "GB/s": round(gbs, 1),
+                          "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                          "us_per_call": round(ms * 1e3 / (args.steps * R), 3),
+                          "launches_per_call": launches / (args.steps * R), "copies": R}), flush=True)
+        wl.close()
+    moe = moe_measure(q, args.steps, args.warmup, stream)
+    print(json.dumps(moe), flush=True)
+    pf = prefill_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
+    print(json.dumps({"workload": "prefill W4A16 12288x6144 S=1571", "result": pf}), flush=True)
+
+
+def moe_measure(q, steps, warmup, stream):
+    """MoE expert layer at S=1: 256 resident experts (int4 gate/up [2048,6144],
+    down [6144,2048]); each step routes one token to 8 distinct experts
+    (pre-drawn seeded ids) and runs fused gate/up -> silu*up -> down for each."""
+    import torch
+    import synth
+    D, F, E, K = 6144, 2048, 256, 8
+    gates, ups, downs = [], [], []
+    for e in range(E):
+        cg, sg = synth.quant_tensor(I4, F, D, 0, 10 * e + 1, 5e-3, 2e-2)
+        cu, su = synth.quant_tensor(I4, F, D, 0, 10 * e + 2, 5e-3, 2e-2)
+        cd, sd = synth.quant_tensor(I4, D, F, 0, 10 * e + 3, 5e-3, 2e-2)
+        gates.append(q.tensor_upload(I4, F, D, cg, sg))
+        ups.append(q.tensor_upload(I4, F, D, cu, su))
+        downs.append(q.tensor_upload(I4, D, F, cd, sd))
+    ids = synth.expert_draws(E, K, steps + warmup, 0, 77)
+    x = torch.from_numpy(synth.activations(1, D, 0, 78)).cuda()
+    yg = torch.empty((K, F), device="cuda")
+    yu = torch.empty((K, F), device="cuda")
+    h = torch.empty((K, F), device="cuda")
+    y = torch.empty((K, D), device="cuda")
+
+    def step(r):
+        for k in range(K):
+            e = int(ids[r, k])
+            q.matmul_gate_up(gates[e], ups[e], x, yg[k], yu[k], 1, stream)
+            q.silu_mul(yg[k], yu[k], h[k], F, stream)
+            q.matmul(downs[e], h[k], y[k], 1, stream)
+
+    for r in range(warmup):
+        step(r)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for r in range(steps):
+        step(warmup + r)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    layer_bytes = K * (2 * algorithmic_bytes(4, F, D, 1) - 4 * D + algorithmic_bytes(4, D, F, 1) + 4 * 2 * F)
+    for lst in (gates, ups, downs):
+        for t in lst:
+            t.free()
+    return {"workload": "MoE expert layer S=1, 8 of 256 experts, plain launches", "us_per_layer": round(ms * 1e3, 2),
+            "layer_tokens_per_s": round(1e3 / ms, 1), "GB/s": round(layer_bytes / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(layer_bytes / (ms * 1e-3) / 1e9 / peaks()["hbm_gbs"], 4)}
+
+
 def run_reference(args):
     """The CPU oracle on the same workload and metric, on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -444,11 +523,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="default", choices=["default", "sweep"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "sweep":
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -167,6 +167,14 @@ int b200q_tensor_info(const b200q_tensor *t, int *fmt, int *O, int *I, int *devi
                       long long *device_bytes);
 
 /*
+ * Synchronizes the current device and reports whether any kernel of the
+ * library gave up on a bounded device-side wait since the last call
+ * (B200Q_ETIMEOUT; such a kernel leaves its outputs incomplete), or a CUDA
+ * error (B200Q_ECUDA).  Clears the record.  B200Q_OK otherwise.
+ */
+int b200q_device_status(void);
+
+/*
  * Number of kernels this process has launched through the library so far (all
  * devices, all threads).  Lets a caller count the launches inside a timed
  * region.

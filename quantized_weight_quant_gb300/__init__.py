@@ -57,6 +57,8 @@ def _load():
     L.b200q_tensor_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci),
                                     ctypes.POINTER(ci), ctypes.POINTER(cll)]
     L.b200q_tensor_info.restype = ci
+    L.b200q_device_status.argtypes = []
+    L.b200q_device_status.restype = ci
     L.b200q_kernel_launches.argtypes = []
     L.b200q_kernel_launches.restype = cll
     L.b200q_last_error.argtypes = []
@@ -74,6 +76,11 @@ def last_error() -> str:
 def kernel_launches() -> int:
     """Kernels launched through the library so far in this process."""
     return int(lib.b200q_kernel_launches())
+
+
+def device_status() -> int:
+    """Synchronize the device; raise if a kernel gave up on a bounded wait."""
+    return _check(lib.b200q_device_status())
 
 
 def tc_min_s() -> int:

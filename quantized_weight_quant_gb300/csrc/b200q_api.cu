@@ -21,6 +21,8 @@ cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, flo
                           cudaStream_t st, bool *handled);
 cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu,
                               int S, cudaStream_t st, bool *handled);
+cudaError_t decode_take_error(unsigned int *code);
+cudaError_t prefill_take_error(unsigned int *code);
 
 namespace {
 
@@ -133,6 +135,17 @@ extern "C" {
 const char *b200q_last_error(void) { return g_err.c_str(); }
 
 long long b200q_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int b200q_device_status(void) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_device_status");
+    unsigned int a = 0, b = 0;
+    e = decode_take_error(&a);
+    if (e == cudaSuccess) e = prefill_take_error(&b);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_device_status");
+    if (a || b) return fail(B200Q_ETIMEOUT, "b200q_device_status: a kernel gave up on a bounded wait");
+    return B200Q_OK;
+}
 
 int b200q_tc_min_s(void) { return tc_min_s(); }
 

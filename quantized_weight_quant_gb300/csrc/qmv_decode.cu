@@ -5,8 +5,8 @@
 //
 // Why tensor cores here.  Decode streams every weight once (HBM-bound), but
 // on the SIMT pipe each int4 weight costs an unpack, a convert and an FMA per
-// token: about 3-4 issue slots per weight, more than an SM can issue at HBM
-// rate.  So the FMAs go to mma.sync and the SIMT pipe only unpacks:
+// token: 3-4 issue slots per weight, more than an SM can issue at HBM rate.
+// So the FMAs go to mma.sync and the SIMT pipe only unpacks:
 //
 //   * codes -> exact fp16 in registers.  A code c is ORed into the mantissa
 //     of 1024.0 (fp16 0x6400, whose mantissa LSB is 1), giving 1024 + c
@@ -19,27 +19,34 @@
 //     lo = fp16(v - hi).  hi + lo carries 22 significant bits; the remainder
 //     is below 2^-21 |x| or 2^-38 max|x_s|, far inside the 1e-5 tolerance.
 //   * every product of an exact fp16 integer and an fp16 term is exact in
-//     f32; the tensor core sums them in f32.  The MMA accumulator is folded
-//     into an f32 register sum after every k-block (at most 16 MMA steps per
-//     chain), the K-slices of the 16 warps are summed in shared memory in a
-//     fixed order, and y = 2^-e_s * (hi + lo sums) * scale[o].
+//     f32; the tensor core sums them in f32.  Four independent accumulators
+//     take alternate MMAs and are folded into an f32 register sum after every
+//     k-block, so no accumulation chain is longer than a few MMAs;
+//     y = 2^-e_s * (hi + lo sums) * scale[o].
 //
 // MMA shape m16n8k16 (row.col, f16 in, f32 accumulate), weights as the B
 // operand: n = 8 weight rows (a "row group"), m = 16 rows of x terms
 // (m = s is token s's hi term, m = 8 + s its lo term, so S <= 8 per launch),
 // k = 16 weights of a row.  The contraction index is reordered consistently
-// on both operands: lane (g, q) of the warp loads the 16-byte chunk q of
-// each 4-chunk k-block of weight row g, and MMA j of the chunk takes its
-// code pairs 2j and 2j+1; the x terms are staged in shared memory in exactly
-// that order, 16 bytes per lane per MMA, so each A fragment is one
-// conflict-free 16-byte shared load.
+// on both operands: lane (g, q) reads the 16-byte chunk q of each 4-chunk
+// k-block of weight row g, and MMA j of the chunk takes its code pairs 2j and
+// 2j+1; the x terms are staged in shared memory in exactly that order, 16
+// bytes per lane per MMA, so each A fragment is one conflict-free 16-byte
+// shared load.
 //
-// Work split.  Persistent CTAs of 16 warps, one per SM: each CTA owns a
-// contiguous run of row groups (at most 12); its warps split the K blocks
-// (warp wk owns a contiguous K-slice) and walk the CTA's row groups four at
-// a time, so one A fragment feeds four MMAs.  The weight loads of the next
-// step are issued before the current step's MMAs, and the first loads go
-// out before x is staged, so the x prologue hides under the first HBM trip.
+// Data movement.  Every warp owns whole row groups (no cross-warp sums) and
+// streams them through its own ring of DEPTH shared-memory stages; a stage
+// holds one segment (up to 1 KB) of each of the row group's 8 rows, fetched
+// by 8 bulk async copies (cp.async.bulk, completion on an mbarrier) that
+// lane 0 issues DEPTH-1 stages ahead.  With ~12 warps x 2 stages in flight an
+// SM keeps ~100 KB of weights in flight, enough to cover HBM latency at full
+// bandwidth without spending registers on it.  Rows are stored with a
+// 16-byte pad so the 8 rows of a fragment load fall in different banks.  The
+// first copies are issued before x is staged, so the x prologue hides under
+// the first HBM trip.  Persistent CTAs, one per SM, own contiguous runs of
+// row groups.  Every mbarrier wait is bounded in time; a wait that gives up
+// records B200Q_ETIMEOUT in a device word (b200q_device_status), drains its
+// own copies in flight and returns.
 #include <cuda_fp16.h>
 
 #include "qwq_internal.h"
@@ -47,13 +54,13 @@
 namespace qwq {
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
-constexpr int kT = 4;          // row groups per pass (share one A fragment)
-constexpr int kMaxS = 8;       // tokens per launch (hi terms in m 0..7, lo in 8..15)
-constexpr int kMaxRgPerCta = 12;
-constexpr int kMaxPasses = (kMaxRgPerCta + kT - 1) / kT;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr int kMaxWarps = 16;
+constexpr int kMaxS = 8;           // tokens per launch (hi terms in m 0..7, lo in 8..15)
+constexpr int kSegMax = 1024;      // bytes per row per stage
+constexpr size_t kSmemMax = 220 * 1024;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
+
+__device__ unsigned int g_decode_err = 0;
 
 template <int FMT>
 struct F;  // E: elements per 16-byte chunk; J: MMAs per chunk
@@ -151,103 +158,149 @@ __device__ __forceinline__ void elem_pos<B200Q_I2>(int e, int &pair, int &half) 
     half = r >> 3;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+// ---- mbarrier / bulk-copy helpers (PTX ISA: mbarrier, cp.async.bulk)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (it == 0) t0 = global_ns();
+        if ((it & 255) == 255 && global_ns() - t0 > limit_ns) return false;
+    }
 }
 
 struct DecParams {
     const uint8_t *codes[2];
     const float *scales[2];
     float *y[2];
-    const float *x;      // [S, I] f32 (already offset to this launch's first token)
+    const float *x;      // [S, I] f32 (offset to this launch's first token)
     int x_ld;            // row stride of x in elements (I)
     int y_ld;            // row stride of y in elements (O)
     int O, I;
     long long ld;        // device row stride in bytes
     int k_pad;           // elements per padded row
-    int nkb;             // k-blocks per row (k_pad / (4 E))
-    int wk;              // warps along K (WK), wr = kWarps / WK warp rows
     int S;               // tokens in this launch, 1..kMaxS
     int rg_per_set;      // ceil(O / 8)
     int n_rg;            // total row groups (sets * rg_per_set)
+    int seg;             // bytes per row per stage (multiple of 128, <= kSegMax)
+    int depth;           // stages per warp
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const DecParams p) {
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const DecParams p) {
     using Fm = F<FMT>;
     constexpr int E = Fm::E, J = Fm::J;
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = blockDim.x >> 5;
     const int g = lane >> 2, q = lane & 3;
     const int S = p.S;
-    const int WK = p.wk, WR = kWarps / p.wk;
-    const int wk = warp % WK, wr = warp / WK;
-    const bool active = wr < WR;
+    const int depth = p.depth;
+    const int rp = p.seg + 16;                       // smem row pitch
+    const int stage_bytes = 8 * rp;
+    const int nseg = (int)((p.ld + p.seg - 1) / p.seg);
 
-    // this CTA's row groups [rg0, rg1)
+    // shared memory: x terms | rings | mbarriers | exps | max scratch
+    uint8_t *a_s = smem;                                              // 4 * S * k_pad
+    uint8_t *ring = smem + (size_t)4 * S * p.k_pad;                   // nw * depth * stage_bytes
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stage_bytes);
+    int *exps = reinterpret_cast<int *>(bars + nw * depth);
+    float *red = reinterpret_cast<float *>(exps + kMaxS);            // [S][nw]
+
+    // this CTA's row groups [rg0, rg1); warp w takes rg0 + w, rg0 + w + nw, ...
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
-    const int n_pass = (rg1 - rg0 + kT - 1) / kT;
+    const int my_rgs = rg1 - rg0 > warp ? (rg1 - rg0 - warp + nw - 1) / nw : 0;
+    const int n_units = my_rgs * nseg;
 
-    // this warp's k-blocks [kb0, kb1)
-    const int kb0 = wk * p.nkb / WK, kb1 = (wk + 1) * p.nkb / WK;
-    const int n_kb = kb1 - kb0;
+    uint8_t *my_ring = ring + (size_t)warp * depth * stage_bytes;
+    const uint32_t my_bars = smem_u32(bars + warp * depth);
+    uint64_t policy = 0;
 
-    // shared memory: A terms | partial sums | per-token exponents + max scratch
-    uint8_t *a_s = smem;                                             // 4 * S * k_pad bytes
-    float *part = reinterpret_cast<float *>(smem + (size_t)4 * S * p.k_pad);  // [pass][WK][kT][S][8]
-    float *red = part + (size_t)kMaxPasses * WK * kT * S * 8;        // [S][kWarps]
-    int *exps = reinterpret_cast<int *>(red + kMaxS * kWarps);       // [S]
-
-    // iteration it = pass * n_kb + kb (this warp's passes are wr, wr + WR, ...)
-    const int my_passes = active ? (n_pass > wr ? (n_pass - wr + WR - 1) / WR : 0) : 0;
-    const int n_it = my_passes * n_kb;
-
-    auto load_it = [&](int it, uint4 (&buf)[kT]) {
-        const int pass = wr + (it / n_kb) * WR;
-        const int kb = kb0 + it % n_kb;
-        const int rgb = rg0 + pass * kT;
+    auto issue = [&](int u) {  // lane 0 only
+        const int i = u / nseg, sg = u - i * nseg;
+        const int rg = rg0 + warp + i * nw;
+        const int set = rg >= p.rg_per_set;
+        const uint8_t *base = (set ? p.codes[1] : p.codes[0]) +
+                              (long long)((rg - set * p.rg_per_set) * 8) * p.ld + (long long)sg * p.seg;
+        const long long left = p.ld - (long long)sg * p.seg;
+        const uint32_t bytes = (uint32_t)(left < p.seg ? left : p.seg);
+        const int b = u % depth;
+        const uint32_t bar = my_bars + 8 * b;
+        const uint32_t dst = smem_u32(my_ring + (size_t)b * stage_bytes);
+        mbar_expect_tx(bar, 8 * bytes);
 #pragma unroll
-        for (int t = 0; t < kT; ++t) {
-            const int rg = rgb + t;
-            if (rg < rg1) {
-                const int set = rg >= p.rg_per_set;
-                const int row = (rg - set * p.rg_per_set) * 8 + g;
-                const uint8_t *base = set ? p.codes[1] : p.codes[0];
-                buf[t] = ld_stream(base + (long long)row * p.ld + (long long)(kb * 4 + q) * 16);
-            } else {
-                buf[t] = make_uint4(0, 0, 0, 0);
-            }
-        }
+        for (int r = 0; r < 8; ++r) bulk_g2s(dst + r * rp, base + (long long)r * p.ld, bytes, bar, policy);
     };
 
-    uint4 cur[kT], nxt[kT];
-    if (n_it > 0) load_it(0, cur);
+    if (lane == 0) {
+        for (int b = 0; b < depth; ++b) mbar_init(my_bars + 8 * b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        policy = evict_first_policy();
+        for (int u = 0; u < depth - 1 && u < n_units; ++u) issue(u);
+    }
+    __syncwarp();
 
     // ---- stage x: per-token power-of-two scale, hi/lo fp16 split, MMA order
     for (int s = 0; s < S; ++s) {
         float m = 0.f;
-        for (int k = tid; k < p.I; k += kThreads) m = fmaxf(m, fabsf(__ldg(p.x + (long long)s * p.x_ld + k)));
+        for (int k = tid; k < p.I; k += blockDim.x) m = fmaxf(m, fabsf(__ldg(p.x + (long long)s * p.x_ld + k)));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) red[s * kWarps + warp] = m;
+        if (lane == 0) red[s * nw + warp] = m;
     }
     __syncthreads();
     if (tid < S) {
         float m = 0.f;
-        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, red[tid * kWarps + w]);
+        for (int w = 0; w < nw; ++w) m = fmaxf(m, red[tid * nw + w]);
         exps[tid] = m > 0.f ? 14 - ilogbf(m) : 0;
     }
     __syncthreads();
     {
         const int total = S * p.k_pad;
         __half *a_h = reinterpret_cast<__half *>(a_s);
-        for (int idx = tid; idx < total; idx += kThreads) {
+        for (int idx = tid; idx < total; idx += blockDim.x) {
             const int s = idx / p.k_pad, k = idx - s * p.k_pad;
             const float v = k < p.I ? ldexpf(__ldg(p.x + (long long)s * p.x_ld + k), exps[s]) : 0.f;
             const __half hi = __float2half_rn(v);
@@ -258,83 +311,73 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mma_kernel(const DecParams p)
             const int j = pair >> 1, slot = pair & 1;
             // 16-byte group (kb, j, s, q): words {hi p0, lo p0, hi p1, lo p1}
             const size_t grp = (((size_t)(c >> 2) * J + j) * S + s) * 4 + (c & 3);
-            const size_t hidx = grp * 8 + slot * 4 + half;     // in halves
+            const size_t hidx = grp * 8 + slot * 4 + half;  // in halves
             a_h[hidx] = hi;
             a_h[hidx + 2] = lo;
         }
     }
     __syncthreads();
 
-    // ---- main loop
-    float acc[kT][4];
-    float cfr[kT][4];
-#pragma unroll
-    for (int t = 0; t < kT; ++t)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-
+    // ---- main loop over this warp's (row group, segment) units
     const uint4 *a_v = reinterpret_cast<const uint4 *>(a_s);
-    for (int it = 0; it < n_it; ++it) {
-        if (it + 1 < n_it) load_it(it + 1, nxt);
-        const int pass_local = it / n_kb;
-        const int kb = kb0 + it % n_kb;
+    const bool has_tok = g < S;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int kb_per_seg = p.seg / 64;
+    int u = 0;
+    bool ok = true;
+    for (; u < n_units; ++u) {
+        if (lane == 0 && u + depth - 1 < n_units) issue(u + depth - 1);
+        const int b = u % depth;
+        if (!mbar_wait(my_bars + 8 * b, (uint32_t)((u / depth) & 1), kWaitNs)) {
+            ok = false;
+            break;
+        }
+        const int i = u / nseg, sg = u - i * nseg;
+        const long long left = p.ld - (long long)sg * p.seg;
+        const int n_kb = (int)((left < p.seg ? left : p.seg) / 64);
+        const uint8_t *rowp = my_ring + (size_t)b * stage_bytes + g * rp + q * 16;
+        const int kb_base = sg * kb_per_seg;
+        for (int kb = 0; kb < n_kb; ++kb) {
+            const uint4 codes = *reinterpret_cast<const uint4 *>(rowp + kb * 64);
+            float c4[4][4];
 #pragma unroll
-        for (int t = 0; t < kT; ++t)
+            for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) cfr[t][i] = 0.f;
+                for (int r = 0; r < 4; ++r) c4[a][r] = 0.f;
+            const uint4 *ak = a_v + ((size_t)(kb_base + kb) * J * S + g) * 4 + q;
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            uint4 a = make_uint4(0, 0, 0, 0);
-            if (g < S) a = a_v[(((size_t)kb * J + j) * S + g) * 4 + q];
-#pragma unroll
-            for (int t = 0; t < kT; ++t) {
+            for (int j = 0; j < J; ++j) {
+                uint4 a = make_uint4(0, 0, 0, 0);
+                if (has_tok) a = ak[(size_t)j * S * 4];
                 uint32_t b0, b1;
-                b_regs<FMT>(cur[t], j, b0, b1);
-                mma_16816(cfr[t], a, b0, b1);
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < kT; ++t)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[t][i] += cfr[t][i];
-
-        if (it % n_kb == n_kb - 1) {
-            // end of a pass: publish this warp's K-slice partials (hi + lo)
-            if (g < S) {
-                const int pass = wr + pass_local * WR;
-#pragma unroll
-                for (int t = 0; t < kT; ++t) {
-                    float2 v = make_float2(acc[t][0] + acc[t][2], acc[t][1] + acc[t][3]);
-                    float *dst = part + ((((size_t)pass * WK + wk) * kT + t) * S + g) * 8 + 2 * q;
-                    *reinterpret_cast<float2 *>(dst) = v;
-                }
+                b_regs<FMT>(codes, j, b0, b1);
+                mma_16816(c4[j & 3], a, b0, b1);
             }
 #pragma unroll
-            for (int t = 0; t < kT; ++t)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[r] += (c4[0][r] + c4[1][r]) + (c4[2][r] + c4[3][r]);
         }
-#pragma unroll
-        for (int t = 0; t < kT; ++t) cur[t] = nxt[t];
+        __syncwarp();  // every lane is done with stage b before lane 0 refills it
+        if (sg == nseg - 1) {
+            // row group done: rows 2q, 2q+1 of token g = hi + lo terms
+            if (has_tok) {
+                const int rg = rg0 + warp + i * nw;
+                const int set = rg >= p.rg_per_set;
+                const int o = (rg - set * p.rg_per_set) * 8 + 2 * q;
+                float *yb = (set ? p.y[1] : p.y[0]) + (long long)g * p.y_ld;
+                const float *sb = set ? p.scales[1] : p.scales[0];
+                const int e = exps[g];
+                if (o < p.O) yb[o] = ldexpf(acc[0] + acc[2], -e) * sb[o];
+                if (o + 1 < p.O) yb[o + 1] = ldexpf(acc[1] + acc[3], -e) * sb[o + 1];
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        }
     }
-    __syncthreads();
-
-    // ---- combine K-slices in a fixed order, unscale, apply the row scale
-    const int rows = (rg1 - rg0) * 8;
-    for (int idx = tid; idx < rows * S; idx += kThreads) {
-        const int s = idx / rows, r = idx - s * rows;
-        const int rgl = r >> 3, rr = r & 7;
-        const int pass = rgl / kT, t = rgl % kT;
-        float sum = 0.f;
-        for (int w = 0; w < WK; ++w) sum += part[((((size_t)pass * WK + w) * kT + t) * S + s) * 8 + rr];
-        const int rg = rg0 + rgl;
-        const int set = rg >= p.rg_per_set;
-        const int o = (rg - set * p.rg_per_set) * 8 + rr;
-        if (o < p.O) {
-            float *yb = set ? p.y[1] : p.y[0];
-            const float *sb = set ? p.scales[1] : p.scales[0];
-            yb[(long long)s * p.y_ld + o] = ldexpf(sum, -exps[s]) * sb[o];
-        }
+    if (!ok) {
+        // give up: record the timeout, then let this warp's copies in flight
+        // land before the CTA's shared memory goes away
+        if (lane == 0) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
+        const int last = (u + depth - 1 < n_units ? u + depth - 1 : n_units - 1);
+        for (int v = u; v <= last; ++v) mbar_wait(my_bars + 8 * (v % depth), (uint32_t)((v / depth) & 1), kWaitNs / 4);
     }
 }
 
@@ -343,15 +386,11 @@ int g_sms = 0;
 template <int FMT>
 cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
                        cudaStream_t st) {
-    constexpr int E = F<FMT>::E;
     if (!g_sms) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    const int k_pad = (int)t.k_pad;
-    const int nkb = k_pad / (4 * E);
-    const int WK = nkb < kWarps ? nkb : kWarps;
     DecParams p{};
     p.codes[0] = t.codes;
     p.scales[0] = t.scales;
@@ -362,39 +401,47 @@ cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float 
     p.O = t.O;
     p.I = t.I;
     p.ld = t.ld;
-    p.k_pad = k_pad;
-    p.nkb = nkb;
-    p.wk = WK;
+    p.k_pad = (int)t.k_pad;
     p.rg_per_set = (t.O + 7) / 8;
     p.n_rg = p.rg_per_set * (tu ? 2 : 1);
-    int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
-    const int need = (p.n_rg + kMaxRgPerCta - 1) / kMaxRgPerCta;
-    if (grid < need) grid = need;
+    p.seg = (int)(t.ld < kSegMax ? t.ld : kSegMax);
 
-    // tokens per launch: the staged x and the partials must fit
-    const size_t per_tok = (size_t)4 * k_pad + (size_t)kMaxPasses * WK * kT * 8 * 4;
-    int s_chunk = (int)((kSmemBudget - (size_t)kMaxS * kWarps * 4 - kMaxS * 4) / per_tok);
-    if (s_chunk > kMaxS) s_chunk = kMaxS;
-    if (s_chunk < 1) return cudaErrorInvalidValue;  // caller takes the general path
-
+    // tokens per launch: at most 4 keeps the A-fragment shared-memory traffic
+    // under the SM's bandwidth; fewer when x terms would crowd out the rings
+    const int s_chunk_max = 4;
+    const size_t stage = (size_t)8 * (p.seg + 16);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(qmv_mma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBudget);
+        cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemMax);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    for (int s0 = 0; s0 < S; s0 += s_chunk) {
-        const int sc = S - s0 < s_chunk ? S - s0 : s_chunk;
+    for (int s0 = 0; s0 < S;) {
+        int sc = S - s0 < s_chunk_max ? S - s0 : s_chunk_max;
+        // choose warps / depth for the remaining shared memory
+        size_t fixed = (size_t)4 * sc * p.k_pad + kMaxS * 4 + (size_t)kMaxS * kMaxWarps * 4;
+        while (sc > 1 && fixed + (size_t)4 * 2 * (stage + 8) > kSmemMax) {
+            --sc;
+            fixed = (size_t)4 * sc * p.k_pad + kMaxS * 4 + (size_t)kMaxS * kMaxWarps * 4;
+        }
+        if (fixed + (size_t)4 * 2 * (stage + 8) > kSmemMax) return cudaErrorInvalidValue;
+        int depth = 3, nw = kMaxWarps;
+        while (nw > 4 && fixed + (size_t)nw * depth * (stage + 8) > kSmemMax) --nw;
+        if (fixed + (size_t)nw * depth * (stage + 8) > kSmemMax) depth = 2;
+        while (nw > 4 && fixed + (size_t)nw * depth * (stage + 8) > kSmemMax) --nw;
+        p.depth = depth;
         p.S = sc;
         p.x = x + (long long)s0 * t.I;
         p.y[0] = y + (long long)s0 * t.O;
         p.y[1] = tu ? yu + (long long)s0 * t.O : p.y[0];
-        const size_t smem = (size_t)sc * per_tok + (size_t)kMaxS * kWarps * 4 + kMaxS * 4;
-        qmv_mma_kernel<FMT><<<grid, kThreads, smem, st>>>(p);
+        int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
+        const size_t smem = fixed + (size_t)nw * depth * (stage + 8);
+        qmv_decode_kernel<FMT><<<grid, nw * 32, smem, st>>>(p);
         count_launch();
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        s0 += sc;
     }
     return cudaSuccess;
 }
@@ -407,7 +454,6 @@ cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, flo
                           cudaStream_t st, bool *handled) {
     *handled = false;
     if (S < 1 || S > 15) return cudaSuccess;
-    if (t.k_pad > 40960) return cudaSuccess;  // x terms of one token must fit in shared memory
     cudaError_t e = cudaSuccess;
     switch (t.fmt) {
     case B200Q_I8: e = launch_fmt<B200Q_I8>(t, tu, x, y, yu, S, st); break;
@@ -415,8 +461,16 @@ cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, flo
     case B200Q_I2: e = launch_fmt<B200Q_I2>(t, tu, x, y, yu, S, st); break;
     default: return cudaSuccess;
     }
-    if (e == cudaErrorInvalidValue) return cudaSuccess;
+    if (e == cudaErrorInvalidValue) return cudaSuccess;  // x too large for shared memory
     *handled = (e == cudaSuccess);
+    return e;
+}
+
+// Reads and clears the decode kernel's device error word.
+cudaError_t decode_take_error(unsigned int *code) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_decode_err, sizeof(unsigned int));
+    if (e == cudaSuccess && *code) e = cudaMemcpyToSymbol(g_decode_err, &zero, sizeof(unsigned int));
     return e;
 }
 
