@@ -56,7 +56,7 @@ namespace {
 
 constexpr int kMaxWarps = 16;
 constexpr int kMaxS = 8;           // tokens per launch (hi terms in m 0..7, lo in 8..15)
-constexpr int kSegMax = 1024;      // bytes per row per stage
+constexpr int kSegMax = 512;       // bytes per row per stage
 constexpr size_t kSmemMax = 220 * 1024;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
 
@@ -224,7 +224,52 @@ struct DecParams {
     int n_rg;            // total row groups (sets * rg_per_set)
     int seg;             // bytes per row per stage (multiple of 128, <= kSegMax)
     int depth;           // stages per warp
+    int max_units;       // bound on (row group, segment) units per CTA (partials buffer)
 };
+
+// Calls fn(k, v) for every k in [0, k_end) of x row s (v = 0 for k >= I),
+// with up to 8 independent 16-byte loads in flight per thread.
+template <typename Fn>
+__device__ __forceinline__ void for_x_row(const DecParams &p, int s, int k_end, Fn fn) {
+    const float *xr = p.x + (long long)s * p.x_ld;
+    const int nthr = blockDim.x;
+    if ((p.x_ld & 3) == 0) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+        const int n4 = k_end >> 2;               // k_end is a multiple of 4
+        for (int base = 0; base < n4; base += 8 * nthr) {
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k4 = base + i * nthr + threadIdx.x;
+                v[i] = (k4 < n4 && 4 * k4 < p.I) ? x4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k4 = base + i * nthr + threadIdx.x;
+                if (k4 < n4) {
+                    fn(4 * k4, v[i].x);
+                    fn(4 * k4 + 1, v[i].y);
+                    fn(4 * k4 + 2, v[i].z);
+                    fn(4 * k4 + 3, v[i].w);
+                }
+            }
+        }
+    } else {
+        for (int base = 0; base < k_end; base += 8 * nthr) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = base + i * nthr + threadIdx.x;
+                v[i] = k < p.I ? xr[k] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = base + i * nthr + threadIdx.x;
+                if (k < k_end) fn(k, v[i]);
+            }
+        }
+    }
+}
 
 template <int FMT>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const DecParams p) {
@@ -241,32 +286,35 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     const int stage_bytes = 8 * rp;
     const int nseg = (int)((p.ld + p.seg - 1) / p.seg);
 
-    // shared memory: x terms | rings | mbarriers | exps | max scratch
+    // shared memory: x terms | rings | mbarriers | partials | exps | max scratch
     uint8_t *a_s = smem;                                              // 4 * S * k_pad
     uint8_t *ring = smem + (size_t)4 * S * p.k_pad;                   // nw * depth * stage_bytes
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stage_bytes);
-    int *exps = reinterpret_cast<int *>(bars + nw * depth);
+    float *part = reinterpret_cast<float *>(bars + nw * depth);      // [unit][S][8]
+    int *exps = reinterpret_cast<int *>(part + (size_t)p.max_units * S * 8);
     float *red = reinterpret_cast<float *>(exps + kMaxS);            // [S][nw]
 
-    // this CTA's row groups [rg0, rg1); warp w takes rg0 + w, rg0 + w + nw, ...
+    // this CTA's row groups [rg0, rg1) and its units (row group, segment);
+    // warp w takes units w, w + nw, ...
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
-    const int my_rgs = rg1 - rg0 > warp ? (rg1 - rg0 - warp + nw - 1) / nw : 0;
-    const int n_units = my_rgs * nseg;
+    const int cta_units = (rg1 - rg0) * nseg;
+    const int n_units = cta_units > warp ? (cta_units - warp + nw - 1) / nw : 0;
 
     uint8_t *my_ring = ring + (size_t)warp * depth * stage_bytes;
     const uint32_t my_bars = smem_u32(bars + warp * depth);
     uint64_t policy = 0;
 
-    auto issue = [&](int u) {  // lane 0 only
-        const int i = u / nseg, sg = u - i * nseg;
-        const int rg = rg0 + warp + i * nw;
+    auto issue = [&](int i) {  // lane 0 only: this warp's i-th unit
+        const int u = warp + i * nw;
+        const int rgl = u / nseg, sg = u - rgl * nseg;
+        const int rg = rg0 + rgl;
         const int set = rg >= p.rg_per_set;
         const uint8_t *base = (set ? p.codes[1] : p.codes[0]) +
                               (long long)((rg - set * p.rg_per_set) * 8) * p.ld + (long long)sg * p.seg;
         const long long left = p.ld - (long long)sg * p.seg;
         const uint32_t bytes = (uint32_t)(left < p.seg ? left : p.seg);
-        const int b = u % depth;
+        const int b = i % depth;
         const uint32_t bar = my_bars + 8 * b;
         const uint32_t dst = smem_u32(my_ring + (size_t)b * stage_bytes);
         mbar_expect_tx(bar, 8 * bytes);
@@ -278,14 +326,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
         for (int b = 0; b < depth; ++b) mbar_init(my_bars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         policy = evict_first_policy();
-        for (int u = 0; u < depth - 1 && u < n_units; ++u) issue(u);
+        for (int i = 0; i < depth - 1 && i < n_units; ++i) issue(i);
     }
     __syncwarp();
 
     // ---- stage x: per-token power-of-two scale, hi/lo fp16 split, MMA order
     for (int s = 0; s < S; ++s) {
         float m = 0.f;
-        for (int k = tid; k < p.I; k += blockDim.x) m = fmaxf(m, fabsf(__ldg(p.x + (long long)s * p.x_ld + k)));
+        for_x_row(p, s, (p.I + 3) & ~3, [&](int, float v) { m = fmaxf(m, fabsf(v)); });
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (lane == 0) red[s * nw + warp] = m;
@@ -298,22 +346,23 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     }
     __syncthreads();
     {
-        const int total = S * p.k_pad;
         __half *a_h = reinterpret_cast<__half *>(a_s);
-        for (int idx = tid; idx < total; idx += blockDim.x) {
-            const int s = idx / p.k_pad, k = idx - s * p.k_pad;
-            const float v = k < p.I ? ldexpf(__ldg(p.x + (long long)s * p.x_ld + k), exps[s]) : 0.f;
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
-            const int c = k / E, e = k - c * E;
-            int pair, half;
-            elem_pos<FMT>(e, pair, half);
-            const int j = pair >> 1, slot = pair & 1;
-            // 16-byte group (kb, j, s, q): words {hi p0, lo p0, hi p1, lo p1}
-            const size_t grp = (((size_t)(c >> 2) * J + j) * S + s) * 4 + (c & 3);
-            const size_t hidx = grp * 8 + slot * 4 + half;  // in halves
-            a_h[hidx] = hi;
-            a_h[hidx + 2] = lo;
+        for (int s = 0; s < S; ++s) {
+            const int ex = exps[s];
+            for_x_row(p, s, p.k_pad, [&](int k, float xv) {
+                const float v = ldexpf(xv, ex);
+                const __half hi = __float2half_rn(v);
+                const __half lo = __float2half_rn(v - __half2float(hi));
+                const int c = k / E, e = k - c * E;
+                int pair, half;
+                elem_pos<FMT>(e, pair, half);
+                const int j = pair >> 1, slot = pair & 1;
+                // 16-byte group (kb, j, s, q): words {hi p0, lo p0, hi p1, lo p1}
+                const size_t grp = (((size_t)(c >> 2) * J + j) * S + s) * 4 + (c & 3);
+                const size_t hidx = grp * 8 + slot * 4 + half;  // in halves
+                a_h[hidx] = hi;
+                a_h[hidx + 2] = lo;
+            });
         }
     }
     __syncthreads();
@@ -321,63 +370,71 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     // ---- main loop over this warp's (row group, segment) units
     const uint4 *a_v = reinterpret_cast<const uint4 *>(a_s);
     const bool has_tok = g < S;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int kb_per_seg = p.seg / 64;
-    int u = 0;
+    int i = 0;
     bool ok = true;
-    for (; u < n_units; ++u) {
-        if (lane == 0 && u + depth - 1 < n_units) issue(u + depth - 1);
-        const int b = u % depth;
-        if (!mbar_wait(my_bars + 8 * b, (uint32_t)((u / depth) & 1), kWaitNs)) {
+    for (; i < n_units; ++i) {
+        if (lane == 0 && i + depth - 1 < n_units) issue(i + depth - 1);
+        const int b = i % depth;
+        if (!mbar_wait(my_bars + 8 * b, (uint32_t)((i / depth) & 1), kWaitNs)) {
             ok = false;
             break;
         }
-        const int i = u / nseg, sg = u - i * nseg;
+        const int u = warp + i * nw;
+        const int sg = u % nseg;
         const long long left = p.ld - (long long)sg * p.seg;
         const int n_kb = (int)((left < p.seg ? left : p.seg) / 64);
         const uint8_t *rowp = my_ring + (size_t)b * stage_bytes + g * rp + q * 16;
-        const int kb_base = sg * kb_per_seg;
+        const uint4 *ak = a_v + ((size_t)sg * kb_per_seg * J * S + g) * 4 + q;
+        float c4[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) c4[a][r] = 0.f;
         for (int kb = 0; kb < n_kb; ++kb) {
             const uint4 codes = *reinterpret_cast<const uint4 *>(rowp + kb * 64);
-            float c4[4][4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) c4[a][r] = 0.f;
-            const uint4 *ak = a_v + ((size_t)(kb_base + kb) * J * S + g) * 4 + q;
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 uint4 a = make_uint4(0, 0, 0, 0);
-                if (has_tok) a = ak[(size_t)j * S * 4];
+                if (has_tok) a = ak[((size_t)kb * J + j) * S * 4];
                 uint32_t b0, b1;
                 b_regs<FMT>(codes, j, b0, b1);
                 mma_16816(c4[j & 3], a, b0, b1);
             }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[r] += (c4[0][r] + c4[1][r]) + (c4[2][r] + c4[3][r]);
         }
         __syncwarp();  // every lane is done with stage b before lane 0 refills it
-        if (sg == nseg - 1) {
-            // row group done: rows 2q, 2q+1 of token g = hi + lo terms
-            if (has_tok) {
-                const int rg = rg0 + warp + i * nw;
-                const int set = rg >= p.rg_per_set;
-                const int o = (rg - set * p.rg_per_set) * 8 + 2 * q;
-                float *yb = (set ? p.y[1] : p.y[0]) + (long long)g * p.y_ld;
-                const float *sb = set ? p.scales[1] : p.scales[0];
-                const int e = exps[g];
-                if (o < p.O) yb[o] = ldexpf(acc[0] + acc[2], -e) * sb[o];
-                if (o + 1 < p.O) yb[o + 1] = ldexpf(acc[1] + acc[3], -e) * sb[o + 1];
-            }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        if (has_tok) {
+            // rows 2q, 2q+1 of token g: hi terms (m = g) + lo terms (m = g + 8)
+            float2 v;
+            v.x = (c4[0][0] + c4[1][0]) + (c4[2][0] + c4[3][0]) + (c4[0][2] + c4[1][2]) + (c4[2][2] + c4[3][2]);
+            v.y = (c4[0][1] + c4[1][1]) + (c4[2][1] + c4[3][1]) + (c4[0][3] + c4[1][3]) + (c4[2][3] + c4[3][3]);
+            *reinterpret_cast<float2 *>(part + ((size_t)u * S + g) * 8 + 2 * q) = v;
         }
     }
     if (!ok) {
         // give up: record the timeout, then let this warp's copies in flight
         // land before the CTA's shared memory goes away
         if (lane == 0) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
-        const int last = (u + depth - 1 < n_units ? u + depth - 1 : n_units - 1);
-        for (int v = u; v <= last; ++v) mbar_wait(my_bars + 8 * (v % depth), (uint32_t)((v / depth) & 1), kWaitNs / 4);
+        const int last = (i + depth - 1 < n_units ? i + depth - 1 : n_units - 1);
+        for (int v = i; v <= last; ++v) mbar_wait(my_bars + 8 * (v % depth), (uint32_t)((v / depth) & 1), kWaitNs / 4);
+    }
+    __syncthreads();
+
+    // ---- combine the segments of each row group in a fixed order
+    const int rows = (rg1 - rg0) * 8;
+    for (int idx = tid; idx < rows * S; idx += blockDim.x) {
+        const int s = idx / rows, r = idx - s * rows;
+        const int rgl = r >> 3, rr = r & 7;
+        float sum = 0.f;
+        for (int sg = 0; sg < nseg; ++sg) sum += part[((size_t)(rgl * nseg + sg) * S + s) * 8 + rr];
+        const int rg = rg0 + rgl;
+        const int set = rg >= p.rg_per_set;
+        const int o = (rg - set * p.rg_per_set) * 8 + rr;
+        if (o < p.O) {
+            float *yb = set ? p.y[1] : p.y[0];
+            const float *sb = set ? p.scales[1] : p.scales[0];
+            yb[(long long)s * p.y_ld + o] = ldexpf(sum, -exps[s]) * sb[o];
+        }
     }
 }
 
@@ -405,11 +462,18 @@ cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float 
     p.rg_per_set = (t.O + 7) / 8;
     p.n_rg = p.rg_per_set * (tu ? 2 : 1);
     p.seg = (int)(t.ld < kSegMax ? t.ld : kSegMax);
+    const int nseg = (int)((t.ld + p.seg - 1) / p.seg);
+
+    // one CTA per SM unless the partial-sum buffer would grow too large
+    int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
+    const int max_rg_cta = 64;
+    const int need = (p.n_rg + max_rg_cta - 1) / max_rg_cta;
+    if (grid < need) grid = need;
+    p.max_units = ((p.n_rg + grid - 1) / grid) * nseg;
 
     // tokens per launch: at most 4 keeps the A-fragment shared-memory traffic
     // under the SM's bandwidth; fewer when x terms would crowd out the rings
-    const int s_chunk_max = 4;
-    const size_t stage = (size_t)8 * (p.seg + 16);
+    const size_t stage = (size_t)8 * (p.seg + 16) + 8;   // ring stage + its mbarrier
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -417,26 +481,25 @@ cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    auto fixed_for = [&](int sc) {
+        return (size_t)4 * sc * p.k_pad + (size_t)p.max_units * sc * 8 * 4 + kMaxS * 4 +
+               (size_t)kMaxS * kMaxWarps * 4;
+    };
     for (int s0 = 0; s0 < S;) {
-        int sc = S - s0 < s_chunk_max ? S - s0 : s_chunk_max;
-        // choose warps / depth for the remaining shared memory
-        size_t fixed = (size_t)4 * sc * p.k_pad + kMaxS * 4 + (size_t)kMaxS * kMaxWarps * 4;
-        while (sc > 1 && fixed + (size_t)4 * 2 * (stage + 8) > kSmemMax) {
-            --sc;
-            fixed = (size_t)4 * sc * p.k_pad + kMaxS * 4 + (size_t)kMaxS * kMaxWarps * 4;
-        }
-        if (fixed + (size_t)4 * 2 * (stage + 8) > kSmemMax) return cudaErrorInvalidValue;
+        int sc = S - s0 < 4 ? S - s0 : 4;
+        while (sc > 1 && fixed_for(sc) + (size_t)4 * 2 * stage > kSmemMax) --sc;
+        const size_t fixed = fixed_for(sc);
+        if (fixed + (size_t)4 * 2 * stage > kSmemMax) return cudaErrorInvalidValue;
         int depth = 3, nw = kMaxWarps;
-        while (nw > 4 && fixed + (size_t)nw * depth * (stage + 8) > kSmemMax) --nw;
-        if (fixed + (size_t)nw * depth * (stage + 8) > kSmemMax) depth = 2;
-        while (nw > 4 && fixed + (size_t)nw * depth * (stage + 8) > kSmemMax) --nw;
+        while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
+        if (fixed + (size_t)nw * depth * stage > kSmemMax) depth = 2;
+        while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
         p.depth = depth;
         p.S = sc;
         p.x = x + (long long)s0 * t.I;
         p.y[0] = y + (long long)s0 * t.O;
         p.y[1] = tu ? yu + (long long)s0 * t.O : p.y[0];
-        int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
-        const size_t smem = fixed + (size_t)nw * depth * (stage + 8);
+        const size_t smem = fixed + (size_t)nw * depth * stage;
         qmv_decode_kernel<FMT><<<grid, nw * 32, smem, st>>>(p);
         count_launch();
         cudaError_t e = cudaGetLastError();
