@@ -1,17 +1,533 @@
-// Tensor-core prefill path (placeholder until the tcgen05 kernel lands).
+// Tensor-core prefill path: W4A16 / W8A16 GEMM on tcgen05 (sm_103a).
+//
+// y[s,o] = scale[o] * sum_k deq(W[o,k]) * bf16(x[s,k])
+//
+// The colibri CUDA docs ("The GPU-resident pipeline" section) describe a
+// Tensor-Core int4 x 16-bit dispatch for batched rows that pays from 16 rows;
+// this is that contraction built for the 5th-generation tensor cores.
+//
+// 1. A pre-pass converts x (f32 [S, I]) to bf16 (round to nearest even) into a
+//    stream-ordered workspace [S, k_pad], zero past I.  For int4 the eight
+//    elements of every 8-group are stored in the order 0,4,1,5,2,6,3,7, the
+//    order in which the dequantizer below produces them (the contraction
+//    index may be permuted freely as long as both operands agree).
+// 2. The GEMM, D[o, s] = sum_k A[o, k] B[s, k], M = weight rows (A = the
+//    dequantized weights, K-major), N = tokens (B = x, K-major), K = I.
+//    Persistent CTAs walk 128 x 176 output tiles (176 = 11 * 16 splits 1571
+//    tokens into 9 tiles with 0.8% padding).  Warp roles:
+//      warp 0     TMA producer: per 64-wide k-block, one 2-D load of the
+//                 128-row code tile and one of the 176 x 64 bf16 x tile
+//                 (128-byte swizzle), completion on an mbarrier;
+//      warps 2-5  dequantizers, one thread per weight row: codes -> exact
+//                 bf16 (int4: OR the nibble into the mantissa of 128.0 and
+//                 subtract 136; int8: exact via f32), written in the
+//                 128-byte-swizzled K-major layout the MMA reads;
+//      warp 1     MMA issuer (one thread): 4 x tcgen05.mma (kind::f16,
+//                 bf16 in, f32 accumulate, 128 x 176 x 16) per k-block into
+//                 one of two TMEM accumulators; tcgen05.commit releases the
+//                 stage and, after the last k-block, hands the tile to ...
+//      warps 6-9  epilogue: tcgen05.ld of its 32 TMEM lanes, times scale[o],
+//                 coalesced f32 stores of y (32 consecutive o per store).
+//    Integer codes are exact in bf16 and products are exact in f32, so the
+//    only approximation is x's rounding to bf16 plus f32 accumulation.
+// Every mbarrier wait is bounded; a wait that gives up records
+// B200Q_ETIMEOUT (b200q_device_status) and the CTA winds down, draining its
+// copies and freeing its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "qwq_internal.h"
 
 namespace qwq {
+namespace {
 
-cudaError_t launch_prefill_tc(const Tensor &, const Tensor *, const float *, float *, float *, int,
-                              cudaStream_t, bool *handled) {
-    *handled = false;
+constexpr int BM = 128, BN = 176, BK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 320;        // 10 warps
+constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
+constexpr int kAccStride = 256;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ unsigned int g_prefill_err = 0;
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (it == 0) t0 = global_ns();
+        if ((it & 255) == 255 && global_ns() - t0 > kWaitNs) {
+            atomicExch(&g_prefill_err, (unsigned)(-B200Q_ETIMEOUT));
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);      // start address
+    d |= (uint64_t)1 << 16;                        // leading-dimension byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride-dimension byte offset
+    d |= (uint64_t)1 << 46;                        // descriptor version
+    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One int4 code word (8 nibbles, k = 8m..8m+7) -> 8 exact bf16 in the order
+// 0,4,1,5,2,6,3,7: 0x4300 | c is 128 + c in bf16, minus 136 is c - 8.
+__device__ __forceinline__ uint4 deq_i4_word(uint32_t w) {
+    uint4 o;
+    o.x = bsub2(lop3_and_or(w, 0x000F000Fu, 0x43004300u), 0x43084308u);
+    o.y = bsub2(lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u), 0x43084308u);
+    o.z = bsub2(lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u), 0x43084308u);
+    o.w = bsub2(lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u), 0x43084308u);
+    return o;
+}
+
+// One int8 code word (4 bytes) -> 4 exact bf16 in natural order, through f32:
+// the byte with its sign bit flipped is u = code + 128; 0x4B000000 | u is
+// 2^23 + u, minus (2^23 + 128) is the code.
+__device__ __forceinline__ uint2 deq_i8_word(uint32_t w) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
+    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
+    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
+    return make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
+}
+
+struct GemmParams {
+    const float *scales;
+    float *y;
+    int O, S;
+    int m_tiles, n_tiles, nk;
+    int code_bytes;      // bytes of one code tile row per k-block (32 int4, 64 int8)
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
+                    const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled operand tiles
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    constexpr int A_BYTES = BM * BK * 2;               // 16384
+    constexpr int B_BYTES = BN * BK * 2;               // 22528
+    constexpr int C_BYTES = BM * (FMT == B200Q_I4 ? 32 : 64);
+    uint8_t *a_s = smem;                                 // [kStages][A_BYTES]
+    uint8_t *b_s = a_s + kStages * A_BYTES;              // [kStages][B_BYTES]
+    uint8_t *c_s = b_s + kStages * B_BYTES;              // [kStages][C_BYTES]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(c_s + kStages * C_BYTES);
+    uint64_t *tma_full = bars, *a_full = bars + kStages, *empty = bars + 2 * kStages;
+    uint64_t *acc_full = bars + 3 * kStages, *acc_empty = acc_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles_total = p.m_tiles * p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&tma_full[s]), 1);
+            mbar_init(smem_u32(&a_full[s]), 4);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 4);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+                const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BN;
+                for (int kb = 0; kb < p.nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = smem_u32(&tma_full[stage]);
+                    mbar_expect_tx(bar, (uint32_t)(C_BYTES + B_BYTES));
+                    tma_load_2d(smem_u32(c_s + stage * C_BYTES), &map_codes, kb * p.code_bytes, m0, bar);
+                    tma_load_2d(smem_u32(b_s + stage * B_BYTES), &map_x, kb * BK, n0, bar);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // the copies of the last kStages loads must land before the CTA
+            // may leave (earlier ones were consumed before their stage was
+            // refilled); a phase that already completed returns at once
+            for (long long i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
+                mbar_wait(smem_u32(&tma_full[i % kStages]), (uint32_t)((i / kStages) & 1));
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int t = 0;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x, ++t) {
+                const int ab = t & 1;
+                if (!mbar_wait(smem_u32(&acc_empty[ab]), ((t >> 1) & 1) ^ 1)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + ab * kAccStride;
+                for (int kb = 0; kb < p.nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&a_full[stage]), phase)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(a_s + stage * A_BYTES);
+                    const uint32_t b_addr = smem_u32(b_s + stage * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k),
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&empty[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) mma_commit(smem_u32(&acc_full[ab]));
+            }
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ---------------- dequantizers: thread r owns row r of every A tile
+        const int r = (warp - 2) * 32 + lane;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < p.nk; ++kb) {
+                if (!mbar_wait(smem_u32(&tma_full[stage]), phase)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *crow = c_s + stage * C_BYTES + r * (C_BYTES / BM);
+                uint8_t *arow = a_s + stage * A_BYTES + r * 128;
+                const int sw = r & 7;
+                if (FMT == B200Q_I4) {
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(crow);
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + 16);
+                    const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = deq_i4_word(wv[c]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * h);
+                        const uint2 lo = deq_i8_word(cw.x), hi = deq_i8_word(cw.y);
+                        const uint2 lo2 = deq_i8_word(cw.z), hi2 = deq_i8_word(cw.w);
+                        *reinterpret_cast<uint4 *>(arow + (((2 * h) ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                        *reinterpret_cast<uint4 *>(arow + (((2 * h + 1) ^ sw) << 4)) =
+                            make_uint4(lo2.x, lo2.y, hi2.x, hi2.y);
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&a_full[stage]));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: TMEM lanes 32 * (warp % 4) ..
+        const int quarter = warp & 3;
+        int t = 0;
+        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++t) {
+            const int ab = t & 1;
+            if (!mbar_wait(smem_u32(&acc_full[ab]), (t >> 1) & 1)) break;
+            tc_fence_after();
+            const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BN;
+            const int o = m0 + quarter * 32 + lane;
+            const float sc = o < p.O ? p.scales[o] : 0.f;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kAccStride;
+#pragma unroll 1
+            for (int c = 0; c < BN / 16; ++c) {
+                float v[16];
+                tmem_ld16(taddr + c * 16, v);
+                const int s0 = n0 + c * 16;
+                if (o < p.O) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (s0 + j < p.S) p.y[(long long)(s0 + j) * p.O + o] = v[j] * sc;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+}
+
+// x f32 [S, I] -> bf16 [S, k_pad] (RNE, zero past I); int4 tensors get each
+// 8-group in the order 0,4,1,5,2,6,3,7.
+__global__ void x_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ xb, int S, int I,
+                                 int k_pad, int permute8) {
+    const long long total = (long long)S * k_pad / 8;
+    for (long long g8 = (long long)blockIdx.x * blockDim.x + threadIdx.x; g8 < total;
+         g8 += (long long)gridDim.x * blockDim.x) {
+        const long long s = g8 / (k_pad / 8);
+        const int k0 = (int)(g8 - s * (k_pad / 8)) * 8;
+        const float *xr = x + s * I;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (k0 + i < I) ? xr[k0 + i] : 0.f;
+        uint4 o;
+        if (permute8) {
+            o.x = pack_bf16(v[0], v[4]);
+            o.y = pack_bf16(v[1], v[5]);
+            o.z = pack_bf16(v[2], v[6]);
+            o.w = pack_bf16(v[3], v[7]);
+        } else {
+            o.x = pack_bf16(v[0], v[1]);
+            o.y = pack_bf16(v[2], v[3]);
+            o.z = pack_bf16(v[4], v[5]);
+            o.w = pack_bf16(v[6], v[7]);
+        }
+        reinterpret_cast<uint4 *>(xb + s * k_pad)[k0 / 8] = o;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaMemPool_t g_pool[64] = {};
+std::mutex g_pool_mu;
+int g_sms = 0;
+
+cudaError_t get_pool(int dev, cudaMemPool_t *out) {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaError_t e = cudaMemPoolCreate(&g_pool[dev], &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = ~0ull;   // keep freed workspace cached in the pool
+        cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    *out = g_pool[dev];
     return cudaSuccess;
 }
 
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT>
+cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, cudaStream_t st) {
+    constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
+    CUtensorMap map_codes, map_x;
+    if (!encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
+                   (uint64_t)t.ld, code_bytes, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (!encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)xb, (uint64_t)t.k_pad, (uint64_t)S,
+                   (uint64_t)t.k_pad * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.scales = t.scales;
+    p.y = y;
+    p.O = t.O;
+    p.S = S;
+    p.m_tiles = t.o_pad / BM;
+    p.n_tiles = (S + BN - 1) / BN;
+    p.nk = (int)(t.k_pad / BK);
+    p.code_bytes = code_bytes;
+    constexpr int C_BYTES = BM * code_bytes;
+    const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BN * BK * 2 + C_BYTES) + (3 * kStages + 4) * 8 + 16;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = tiles < g_sms ? tiles : g_sms;
+    qgemm_tc_kernel<FMT><<<grid, kThreads, smem, st>>>(map_codes, map_x, p);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
+                              cudaStream_t st, bool *handled) {
+    *handled = false;
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return cudaSuccess;
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaMemPool_t pool;
+    cudaError_t e = get_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    const size_t ws_bytes = (size_t)S * t.k_pad * 2;
+    void *ws = nullptr;
+    e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, st);
+    if (e != cudaSuccess) return e;
+    const long long groups = (long long)S * t.k_pad / 8;
+    long long blocks = (groups + 255) / 256;
+    if (blocks > (long long)g_sms * 16) blocks = (long long)g_sms * 16;
+    x_to_bf16_kernel<<<(int)blocks, 256, 0, st>>>(x, (__nv_bfloat16 *)ws, S, t.I, (int)t.k_pad,
+                                                   t.fmt == B200Q_I4 ? 1 : 0);
+    count_launch();
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = t.fmt == B200Q_I4 ? run_gemm<B200Q_I4>(t, (__nv_bfloat16 *)ws, y, S, st)
+                              : run_gemm<B200Q_I8>(t, (__nv_bfloat16 *)ws, y, S, st);
+    if (e == cudaSuccess && tu)
+        e = t.fmt == B200Q_I4 ? run_gemm<B200Q_I4>(*tu, (__nv_bfloat16 *)ws, yu, S, st)
+                              : run_gemm<B200Q_I8>(*tu, (__nv_bfloat16 *)ws, yu, S, st);
+    cudaError_t ef = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = ef;
+    *handled = (e == cudaSuccess);
+    return e;
+}
+
 cudaError_t prefill_take_error(unsigned int *code) {
-    *code = 0;
-    return cudaSuccess;
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_prefill_err, sizeof(unsigned int));
+    if (e == cudaSuccess && *code) e = cudaMemcpyToSymbol(g_prefill_err, &zero, sizeof(unsigned int));
+    return e;
 }
 
 }  // namespace qwq
