@@ -432,6 +432,31 @@ def run_sweep(args):
     print(json.dumps({"workload": "prefill W4A16 12288x6144 S=1571", "result": pf}), flush=True)
 
 
+def run_single(args):
+    """One configuration (for profiling runs): --workload decode|prefill with
+    --fmt/--O/--I/--S/--copies; one JSON line."""
+    import torch
+    import quantized_weight_quant_gb300 as q
+    torch.cuda.set_device(0)
+    pk = peaks()
+    stream = torch.cuda.Stream()
+    fmt = {"f32": 0, "i8": 1, "i4": 2, "i2": 3}[args.fmt]
+    bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
+    per = algorithmic_bytes(bits, args.O, args.I, args.S)
+    R = args.copies or max(2, min(64, -(-3 * L2_BYTES // per)))
+    wl = Decode(q, fmt, args.O, args.I, args.S, R)
+    ms, launches = time_steps(wl, args.steps, args.warmup, stream)
+    sec = ms * 1e-3
+    print(json.dumps({"workload": "%s %s O=%d I=%d S=%d" % (args.workload, args.fmt, args.O, args.I, args.S),
+                      "path": q.matmul_path(wl.tensors[0], args.S),
+                      "GB/s": round(wl.bytes_per_step * args.steps / sec / 1e9, 1),
+                      "frac_hbm": round(wl.bytes_per_step * args.steps / sec / 1e9 / pk["hbm_gbs"], 4),
+                      "TFLOP/s": round(wl.flops_per_step * args.steps / sec / 1e12, 2),
+                      "us_per_call": round(ms * 1e3 / (args.steps * R), 3), "copies": R,
+                      "launches": launches}), flush=True)
+    wl.close()
+
+
 def moe_measure(q, steps, warmup, stream):
     """MoE expert layer at S=1: 256 resident experts (int4 gate/up [2048,6144],
     down [6144,2048]); each step routes one token to 8 distinct experts
@@ -523,7 +548,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="default", choices=["default", "sweep"])
+    ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill"])
+    ap.add_argument("--fmt", default="i4", choices=["f32", "i8", "i4", "i2"])
+    ap.add_argument("--O", type=int, default=12288)
+    ap.add_argument("--I", type=int, default=6144)
+    ap.add_argument("--S", type=int, default=1)
+    ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: enough for 3x L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -531,6 +561,8 @@ def main():
         run_reference(args)
     elif args.workload == "sweep":
         run_sweep(args)
+    elif args.workload in ("decode", "prefill"):
+        run_single(args)
     else:
         run_ours(args)
 
