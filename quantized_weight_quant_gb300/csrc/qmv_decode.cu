@@ -1,168 +1,132 @@
-// Decode kernel for int8 / int4 / int2 weights at small S (the f32-accurate
-// path): y[s,o] = scale[o] * sum_i deq(W[o,i]) * x[s,i]   ("CUDA 后端",
-// section 1, weight_at / quant_matmul; three-backends chapter, section 四,
-// qmatmul.comp header: x staged once and reused for every output row).
+// Decode kernel, the f32-accurate path at small S for every format:
+//     y[s,o] = scale[o] * sum_i deq(W[o,i]) * x[s,i]
+// ("CUDA 后端", section 1: weight_at / quant_matmul; three-backends chapter,
+// section 四: the qmatmul.comp header, x staged once and reused for every
+// output row).
 //
-// Why tensor cores here.  Decode streams every weight once (HBM-bound), but
-// on the SIMT pipe each int4 weight costs an unpack, a convert and an FMA per
-// token: 3-4 issue slots per weight, more than an SM can issue at HBM rate.
-// So the FMAs go to mma.sync and the SIMT pipe only unpacks:
+// Decode reads every weight once, so the kernel must retire weights at HBM
+// rate: ~90 G int4 weights/s per SM on GB300.  Two facts set the design.
+//   * mma.sync (the pre-Blackwell tensor-core path) runs at a small fraction
+//     of the tcgen05 rate here and at S = 1 would waste 7/8 of every
+//     fragment, so the products stay on the FP32 pipe.
+//   * A conventional unpack (shift, mask, convert, subtract) costs 3-4 issue
+//     slots per weight before the FMA.  Instead each code is ANDed in place
+//     out of its 32-bit word: with the exponent field zero the result *is* an
+//     f32 (a subnormal) whose value is code * 2^b * 2^-149, b = the code's bit
+//     offset in the word, exactly.  x is staged in shared memory pre-scaled by
+//     the matching power of two, so one FFMA forms code * x * 2^T exactly
+//     (2^T a per-token power of two that keeps every value in range).  The
+//     zero-point is folded out at the end: sum (c - z) x = sum c x - z sum x.
+//     int4: nibbles 0-4 of a word are masked in place, nibbles 5-7 after one
+//     shift by 12; int8 (two's complement): the sign bits are flipped once per
+//     word (c + 128), bytes 0-1 in place, bytes 2-3 after one shift; int2:
+//     fields 0-10 in place, 11-15 after one shift; f32 weights FFMA directly.
+//     That is one AND and one FFMA per weight, plus a shift per word.
 //
-//   * codes -> exact fp16 in registers.  A code c is ORed into the mantissa
-//     of 1024.0 (fp16 0x6400, whose mantissa LSB is 1), giving 1024 + c
-//     exactly; one packed subtraction of 1024 + zero-point leaves deq(c)
-//     exactly (|deq| <= 128 fits fp16's 11-bit significand).  Two codes per
-//     instruction pair: lop3 (int4: nibbles i and i+4 of a word; int2: fields
-//     t and t+8) or prmt (int8: adjacent bytes, after flipping the sign bit).
-//   * x -> two fp16 terms.  Per token s, x is scaled by 2^e_s (exact) so that
-//     max|x_s| lands in [2^14, 2^15), then split as hi = fp16(v),
-//     lo = fp16(v - hi).  hi + lo carries 22 significant bits; the remainder
-//     is below 2^-21 |x| or 2^-38 max|x_s|, far inside the 1e-5 tolerance.
-//   * every product of an exact fp16 integer and an fp16 term is exact in
-//     f32; the tensor core sums them in f32.  Four independent accumulators
-//     take alternate MMAs and are folded into an f32 register sum after every
-//     k-block, so no accumulation chain is longer than a few MMAs;
-//     y = 2^-e_s * (hi + lo sums) * scale[o].
+// Data movement: every warp streams units of 8 weight rows x 512 bytes
+// through its own ring of shared-memory stages, filled by bulk async copies
+// (cp.async.bulk, mbarrier completion) that lane 0 issues DEPTH-1 units
+// ahead; ~15 warps x 2 stages keep ~120 KB per SM in flight.  In a unit,
+// lane l takes 16-byte chunk l of all 8 rows, so the x values it loads from
+// shared memory serve 8 rows.  Lane sums are combined with a butterfly
+// reduce-scatter, each unit's 8 x NS partial sums go to shared memory, and
+// after the CTA's last unit the segments of every row are added in a fixed
+// order.  Units (row group, segment) are dealt round-robin to the warps of
+// persistent CTAs that own contiguous runs of row groups.  Every mbarrier
+// wait is bounded; a wait that gives up records B200Q_ETIMEOUT in a device
+// word (b200q_device_status), drains its own copies and returns.
 //
-// MMA shape m16n8k16 (row.col, f16 in, f32 accumulate), weights as the B
-// operand: n = 8 weight rows (a "row group"), m = 16 rows of x terms
-// (m = s is token s's hi term, m = 8 + s its lo term, so S <= 8 per launch),
-// k = 16 weights of a row.  The contraction index is reordered consistently
-// on both operands: lane (g, q) reads the 16-byte chunk q of each 4-chunk
-// k-block of weight row g, and MMA j of the chunk takes its code pairs 2j and
-// 2j+1; the x terms are staged in shared memory in exactly that order, 16
-// bytes per lane per MMA, so each A fragment is one conflict-free 16-byte
-// shared load.
-//
-// Data movement.  Every warp owns whole row groups (no cross-warp sums) and
-// streams them through its own ring of DEPTH shared-memory stages; a stage
-// holds one segment (up to 1 KB) of each of the row group's 8 rows, fetched
-// by 8 bulk async copies (cp.async.bulk, completion on an mbarrier) that
-// lane 0 issues DEPTH-1 stages ahead.  With ~12 warps x 2 stages in flight an
-// SM keeps ~100 KB of weights in flight, enough to cover HBM latency at full
-// bandwidth without spending registers on it.  Rows are stored with a
-// 16-byte pad so the 8 rows of a fragment load fall in different banks.  The
-// first copies are issued before x is staged, so the x prologue hides under
-// the first HBM trip.  Persistent CTAs, one per SM, own contiguous runs of
-// row groups.  Every mbarrier wait is bounded in time; a wait that gives up
-// records B200Q_ETIMEOUT in a device word (b200q_device_status), drains its
-// own copies in flight and returns.
-#include <cuda_fp16.h>
-
+// Accuracy: f32 FFMA chains of at most 32 terms per lane and unit, then
+// fixed-order f32 additions; with the zero-point folded out the result stays
+// within 1e-5 of sum |scale * deq * x| on the workloads' distributions.
 #include "qwq_internal.h"
 
 namespace qwq {
 namespace {
 
-constexpr int kMaxWarps = 16;
-constexpr int kMaxS = 8;           // tokens per launch (hi terms in m 0..7, lo in 8..15)
-constexpr int kSegMax = 512;       // bytes per row per stage
+constexpr int kMaxWarps = 15;
+constexpr int kSeg = 512;            // bytes per row per stage: 32 lanes x 16 B
 constexpr size_t kSmemMax = 220 * 1024;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
 
 __device__ unsigned int g_decode_err = 0;
 
 template <int FMT>
-struct F;  // E: elements per 16-byte chunk; J: MMAs per chunk
+struct F;
+// E: elements per 16-byte chunk; ZP: zero point of the extracted code
+template <>
+struct F<B200Q_F32> {
+    static constexpr int E = 4;
+    static constexpr float ZP = 0.f;
+};
 template <>
 struct F<B200Q_I8> {
-    static constexpr int E = 16, J = 4;
+    static constexpr int E = 16;
+    static constexpr float ZP = 128.f;
 };
 template <>
 struct F<B200Q_I4> {
-    static constexpr int E = 32, J = 8;
+    static constexpr int E = 32;
+    static constexpr float ZP = 8.f;
 };
 template <>
 struct F<B200Q_I2> {
-    static constexpr int E = 64, J = 16;
+    static constexpr int E = 64;
+    static constexpr float ZP = 2.f;
 };
 
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint4 &a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t word(const uint4 &c, int m) {
-    return m == 0 ? c.x : m == 1 ? c.y : m == 2 ? c.z : c.w;
-}
-
-// The two fp16x2 B registers of MMA j from one 16-byte chunk of codes:
-// code pairs 2j and 2j+1 in the production order of the format.
+// Bit offset b of element e (0 <= e < 32 / bits) inside its extracted word:
+// the value of the masked code is code * 2^b * 2^-149.
 template <int FMT>
-__device__ __forceinline__ void b_regs(const uint4 &c, int j, uint32_t &b0, uint32_t &b1);
-
+__device__ __forceinline__ int bit_offset(int e);
 template <>
-__device__ __forceinline__ void b_regs<B200Q_I4>(const uint4 &c, int j, uint32_t &b0, uint32_t &b1) {
-    // pair p = 4m + h holds nibbles h and h + 4 of word m
-    const uint32_t w = word(c, j >> 1);
-    const int h = 2 * (j & 1);
-    b0 = hsub2(lop3_and_or(w >> (4 * h), 0x000F000Fu, 0x64006400u), 0x64086408u);
-    b1 = hsub2(lop3_and_or(w >> (4 * h + 4), 0x000F000Fu, 0x64006400u), 0x64086408u);
-}
-
+__device__ __forceinline__ int bit_offset<B200Q_F32>(int) { return 0; }
 template <>
-__device__ __forceinline__ void b_regs<B200Q_I8>(const uint4 &c, int j, uint32_t &b0, uint32_t &b1) {
-    // pair p = 2m + h holds bytes 2h and 2h + 1 of word m; flipping the sign
-    // bit turns the two's-complement code into code + 128 in 0..255
-    const uint32_t w = word(c, j) ^ 0x80808080u;
-    b0 = hsub2(__byte_perm(w, 0x64646464u, 0x4140), 0x64806480u);
-    b1 = hsub2(__byte_perm(w, 0x64646464u, 0x4342), 0x64806480u);
-}
-
+__device__ __forceinline__ int bit_offset<B200Q_I8>(int e) { return 8 * (e & 1); }               // 2,3: >> 16
 template <>
-__device__ __forceinline__ void b_regs<B200Q_I2>(const uint4 &c, int j, uint32_t &b0, uint32_t &b1) {
-    // pair p = 8m + t holds 2-bit fields t and t + 8 of word m
-    const uint32_t w = word(c, j >> 2);
-    const int t = 2 * (j & 3);
-    b0 = hsub2(lop3_and_or(w >> (2 * t), 0x00030003u, 0x64006400u), 0x64026402u);
-    b1 = hsub2(lop3_and_or(w >> (2 * t + 2), 0x00030003u, 0x64006400u), 0x64026402u);
-}
-
-// Inverse of the pair order: element e of a chunk -> (pair, half).
-template <int FMT>
-__device__ __forceinline__ void elem_pos(int e, int &pair, int &half);
-
+__device__ __forceinline__ int bit_offset<B200Q_I4>(int e) { return e < 5 ? 4 * e : 4 * (e - 3); }  // 5-7: >> 12
 template <>
-__device__ __forceinline__ void elem_pos<B200Q_I4>(int e, int &pair, int &half) {
-    const int r = e & 7;
-    pair = 4 * (e >> 3) + (r & 3);
-    half = r >> 2;
-}
+__device__ __forceinline__ int bit_offset<B200Q_I2>(int e) { return e < 11 ? 2 * e : 2 * (e - 11); }  // >> 22
 
-template <>
-__device__ __forceinline__ void elem_pos<B200Q_I8>(int e, int &pair, int &half) {
-    const int r = e & 3;
-    pair = 2 * (e >> 2) + (r >> 1);
-    half = r & 1;
-}
-
-template <>
-__device__ __forceinline__ void elem_pos<B200Q_I2>(int e, int &pair, int &half) {
-    const int r = e & 15;
-    pair = 8 * (e >> 4) + (r & 7);
-    half = r >> 3;
+// FFMA the codes of one 32-bit word of a quantized row against the staged x.
+template <int FMT, int NS, int EW>
+__device__ __forceinline__ void word_fma(uint32_t w, const float (&xv)[NS * EW], float (&acc)[NS]) {
+    if (FMT == B200Q_I8) {
+        const uint32_t u = w ^ 0x80808080u;
+        const uint32_t v = u >> 16;
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
+            acc[t] = fmaf(__uint_as_float(u & 0xFFu), xv[t * EW + 0], acc[t]);
+            acc[t] = fmaf(__uint_as_float(u & 0xFF00u), xv[t * EW + 1], acc[t]);
+            acc[t] = fmaf(__uint_as_float(v & 0xFFu), xv[t * EW + 2], acc[t]);
+            acc[t] = fmaf(__uint_as_float(v & 0xFF00u), xv[t * EW + 3], acc[t]);
+        }
+    } else if (FMT == B200Q_I4) {
+        const uint32_t v = w >> 12;
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
+#pragma unroll
+            for (int e = 0; e < 5; ++e) acc[t] = fmaf(__uint_as_float(w & (0xFu << (4 * e))), xv[t * EW + e], acc[t]);
+#pragma unroll
+            for (int e = 5; e < 8; ++e)
+                acc[t] = fmaf(__uint_as_float(v & (0xFu << (4 * (e - 3)))), xv[t * EW + e], acc[t]);
+        }
+    } else if (FMT == B200Q_I2) {
+        const uint32_t v = w >> 22;
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
+#pragma unroll
+            for (int e = 0; e < 11; ++e) acc[t] = fmaf(__uint_as_float(w & (0x3u << (2 * e))), xv[t * EW + e], acc[t]);
+#pragma unroll
+            for (int e = 11; e < 16; ++e)
+                acc[t] = fmaf(__uint_as_float(v & (0x3u << (2 * (e - 11)))), xv[t * EW + e], acc[t]);
+        }
+    }
 }
 
 // ---- mbarrier / bulk-copy helpers (PTX ISA: mbarrier, cp.async.bulk)
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -193,7 +157,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -209,6 +172,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// Butterfly reduce-scatter of N values (N a power of two <= 32) over the 32
+// lanes: afterwards every lane holds the full sum of value index
+// lane >> (5 - log2 N) (lanes that differ only in the low bits hold the same).
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+    int n = N;
+    int off = 16;
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        if (n > 1) {
+            const int h = n / 2;
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                if (i < h) {
+                    const float send = upper ? v[i] : v[i + h];
+                    const float keep = upper ? v[i + h] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            n = h;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+        off >>= 1;
+    }
+    return v[0];
+}
+
 struct DecParams {
     const uint8_t *codes[2];
     const float *scales[2];
@@ -219,83 +211,36 @@ struct DecParams {
     int O, I;
     long long ld;        // device row stride in bytes
     int k_pad;           // elements per padded row
-    int S;               // tokens in this launch, 1..kMaxS
     int rg_per_set;      // ceil(O / 8)
     int n_rg;            // total row groups (sets * rg_per_set)
-    int seg;             // bytes per row per stage (multiple of 128, <= kSegMax)
     int depth;           // stages per warp
-    int max_units;       // bound on (row group, segment) units per CTA (partials buffer)
+    int max_units;       // bound on (row group, segment) units per CTA
 };
 
-// Calls fn(k, v) for every k in [0, k_end) of x row s (v = 0 for k >= I),
-// with up to 8 independent 16-byte loads in flight per thread.
-template <typename Fn>
-__device__ __forceinline__ void for_x_row(const DecParams &p, int s, int k_end, Fn fn) {
-    const float *xr = p.x + (long long)s * p.x_ld;
-    const int nthr = blockDim.x;
-    if ((p.x_ld & 3) == 0) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
-        const int n4 = k_end >> 2;               // k_end is a multiple of 4
-        for (int base = 0; base < n4; base += 8 * nthr) {
-            float4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k4 = base + i * nthr + threadIdx.x;
-                v[i] = (k4 < n4 && 4 * k4 < p.I) ? x4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k4 = base + i * nthr + threadIdx.x;
-                if (k4 < n4) {
-                    fn(4 * k4, v[i].x);
-                    fn(4 * k4 + 1, v[i].y);
-                    fn(4 * k4 + 2, v[i].z);
-                    fn(4 * k4 + 3, v[i].w);
-                }
-            }
-        }
-    } else {
-        for (int base = 0; base < k_end; base += 8 * nthr) {
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = base + i * nthr + threadIdx.x;
-                v[i] = k < p.I ? xr[k] : 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = base + i * nthr + threadIdx.x;
-                if (k < k_end) fn(k, v[i]);
-            }
-        }
-    }
-}
-
-template <int FMT>
+template <int FMT, int NS>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const DecParams p) {
-    using Fm = F<FMT>;
-    constexpr int E = Fm::E, J = Fm::J;
+    constexpr int E = F<FMT>::E;
+    constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
+    constexpr int EW = 32 / bits;                    // elements per 32-bit word
+    constexpr int NV = 8 * NS;                       // partial sums per lane and unit
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = blockDim.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    const int S = p.S;
     const int depth = p.depth;
-    const int rp = p.seg + 16;                       // smem row pitch
-    const int stage_bytes = 8 * rp;
-    const int nseg = (int)((p.ld + p.seg - 1) / p.seg);
+    constexpr int rp = kSeg + 16;                    // smem row pitch (bank spread)
+    constexpr int stage_bytes = 8 * rp;
+    const int nseg = (int)((p.ld + kSeg - 1) / kSeg);
 
-    // shared memory: x terms | rings | mbarriers | partials | exps | max scratch
-    uint8_t *a_s = smem;                                              // 4 * S * k_pad
-    uint8_t *ring = smem + (size_t)4 * S * p.k_pad;                   // nw * depth * stage_bytes
+    // shared memory: x' [NS][k_pad] | rings | mbarriers | partials | per-token terms
+    float *xs = reinterpret_cast<float *>(smem);
+    uint8_t *ring = smem + (size_t)4 * NS * p.k_pad;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stage_bytes);
-    float *part = reinterpret_cast<float *>(bars + nw * depth);      // [unit][S][8]
-    int *exps = reinterpret_cast<int *>(part + (size_t)p.max_units * S * 8);
-    float *red = reinterpret_cast<float *>(exps + kMaxS);            // [S][nw]
+    float *part = reinterpret_cast<float *>(bars + nw * depth);        // [unit][NS][8]
+    float *tok_sum = part + (size_t)p.max_units * NS * 8;             // [NS] sum of x * 2^T
+    int *tok_exp = reinterpret_cast<int *>(tok_sum + NS);              // [NS] T
+    float *red = reinterpret_cast<float *>(tok_exp + NS);              // [NS][kMaxWarps]
 
-    // this CTA's row groups [rg0, rg1) and its units (row group, segment);
-    // warp w takes units w, w + nw, ...
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
     const int cta_units = (rg1 - rg0) * nseg;
@@ -311,9 +256,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
         const int rg = rg0 + rgl;
         const int set = rg >= p.rg_per_set;
         const uint8_t *base = (set ? p.codes[1] : p.codes[0]) +
-                              (long long)((rg - set * p.rg_per_set) * 8) * p.ld + (long long)sg * p.seg;
-        const long long left = p.ld - (long long)sg * p.seg;
-        const uint32_t bytes = (uint32_t)(left < p.seg ? left : p.seg);
+                              (long long)((rg - set * p.rg_per_set) * 8) * p.ld + (long long)sg * kSeg;
+        const long long left = p.ld - (long long)sg * kSeg;
+        const uint32_t bytes = (uint32_t)(left < kSeg ? left : kSeg);
         const int b = i % depth;
         const uint32_t bar = my_bars + 8 * b;
         const uint32_t dst = smem_u32(my_ring + (size_t)b * stage_bytes);
@@ -330,47 +275,81 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     }
     __syncwarp();
 
-    // ---- stage x: per-token power-of-two scale, hi/lo fp16 split, MMA order
-    for (int s = 0; s < S; ++s) {
-        float m = 0.f;
-        for_x_row(p, s, (p.I + 3) & ~3, [&](int, float v) { m = fmaxf(m, fabsf(v)); });
+    // ---- stage x: x'[t][k] = x[t][k] * 2^(T_t + 149 - b(k)); tok_sum = sum_k x * 2^T_t
+    const int nthr = blockDim.x;
+    if (FMT != B200Q_F32) {
+        for (int t = 0; t < NS; ++t) {
+            const float *xr = p.x + (long long)t * p.x_ld;
+            float m = 0.f;
+            if ((p.x_ld & 3) == 0) {
+                const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+                const int n4 = p.I / 4;
+                for (int base = 0; base < n4; base += 4 * nthr) {
+                    float4 v[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) red[s * nw + warp] = m;
+                    for (int i = 0; i < 4; ++i) {
+                        const int k4 = base + i * nthr + tid;
+                        v[i] = k4 < n4 ? x4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+                }
+            } else {
+                for (int base = 0; base < p.I; base += 4 * nthr) {
+                    float v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int k = base + i * nthr + tid;
+                        v[i] = k < p.I ? xr[k] : 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(v[i]));
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) red[t * kMaxWarps + warp] = m;
+        }
+        __syncthreads();
+        if (tid < NS) {
+            float m = 0.f;
+            for (int w = 0; w < nw; ++w) m = fmaxf(m, red[tid * kMaxWarps + w]);
+            // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
+            tok_exp[tid] = m > 0.f ? -23 - ilogbf(m) : 0;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    if (tid < S) {
-        float m = 0.f;
-        for (int w = 0; w < nw; ++w) m = fmaxf(m, red[tid * nw + w]);
-        exps[tid] = m > 0.f ? 14 - ilogbf(m) : 0;
-    }
-    __syncthreads();
-    {
-        __half *a_h = reinterpret_cast<__half *>(a_s);
-        for (int s = 0; s < S; ++s) {
-            const int ex = exps[s];
-            for_x_row(p, s, p.k_pad, [&](int k, float xv) {
-                const float v = ldexpf(xv, ex);
-                const __half hi = __float2half_rn(v);
-                const __half lo = __float2half_rn(v - __half2float(hi));
-                const int c = k / E, e = k - c * E;
-                int pair, half;
-                elem_pos<FMT>(e, pair, half);
-                const int j = pair >> 1, slot = pair & 1;
-                // 16-byte group (kb, j, s, q): words {hi p0, lo p0, hi p1, lo p1}
-                const size_t grp = (((size_t)(c >> 2) * J + j) * S + s) * 4 + (c & 3);
-                const size_t hidx = grp * 8 + slot * 4 + half;  // in halves
-                a_h[hidx] = hi;
-                a_h[hidx + 2] = lo;
-            });
+    for (int t = 0; t < NS; ++t) {
+        const float *xr = p.x + (long long)t * p.x_ld;
+        const int T = FMT == B200Q_F32 ? 0 : tok_exp[t];
+        float psum = 0.f;
+        for (int k = tid; k < p.k_pad; k += nthr) {
+            const float v = k < p.I ? xr[k] : 0.f;
+            if (FMT == B200Q_F32) {
+                xs[t * p.k_pad + k] = v;
+            } else {
+                xs[t * p.k_pad + k] = ldexpf(v, T + 149 - bit_offset<FMT>(k % EW));
+                psum += ldexpf(v, T);
+            }
+        }
+        if (FMT != B200Q_F32) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+            if (lane == 0) red[t * kMaxWarps + warp] = psum;
         }
     }
     __syncthreads();
+    if (tid < NS) {
+        float ssum = 0.f;
+        if (FMT != B200Q_F32)
+            for (int w = 0; w < nw; ++w) ssum += red[tid * kMaxWarps + w];
+        tok_sum[tid] = ssum;
+        if (FMT == B200Q_F32) tok_exp[tid] = 0;
+    }
+    // (tok_sum / tok_exp are read only after the final __syncthreads)
 
-    // ---- main loop over this warp's (row group, segment) units
-    const uint4 *a_v = reinterpret_cast<const uint4 *>(a_s);
-    const bool has_tok = g < S;
-    const int kb_per_seg = p.seg / 64;
+    // ---- main loop: unit = (row group, 512-byte segment); lane = 16-byte chunk
     int i = 0;
     bool ok = true;
     for (; i < n_units; ++i) {
@@ -382,63 +361,120 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
         }
         const int u = warp + i * nw;
         const int sg = u % nseg;
-        const long long left = p.ld - (long long)sg * p.seg;
-        const int n_kb = (int)((left < p.seg ? left : p.seg) / 64);
-        const uint8_t *rowp = my_ring + (size_t)b * stage_bytes + g * rp + q * 16;
-        const uint4 *ak = a_v + ((size_t)sg * kb_per_seg * J * S + g) * 4 + q;
-        float c4[4][4];
+        const long long left = p.ld - (long long)sg * kSeg;
+        const int chunks = (int)((left < kSeg ? left : kSeg) / 16);
+        float acc[NV];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < NV; ++a) acc[a] = 0.f;
+        if (lane < chunks) {
+            const uint8_t *st = my_ring + (size_t)b * stage_bytes + lane * 16;
+            const int k0 = (sg * (kSeg / 16) + lane) * E;
+            uint4 cw[8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) c4[a][r] = 0.f;
-        for (int kb = 0; kb < n_kb; ++kb) {
-            const uint4 codes = *reinterpret_cast<const uint4 *>(rowp + kb * 64);
+            for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rp);
+            if (FMT == B200Q_F32) {
+                float4 xf[NS];
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                uint4 a = make_uint4(0, 0, 0, 0);
-                if (has_tok) a = ak[((size_t)kb * J + j) * S * 4];
-                uint32_t b0, b1;
-                b_regs<FMT>(codes, j, b0, b1);
-                mma_16816(c4[j & 3], a, b0, b1);
+                for (int t = 0; t < NS; ++t) xf[t] = *reinterpret_cast<const float4 *>(xs + (size_t)t * p.k_pad + k0);
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+#pragma unroll
+                    for (int t = 0; t < NS; ++t) {
+                        float a = acc[t * 8 + r];
+                        a = fmaf(__uint_as_float(cw[r].x), xf[t].x, a);
+                        a = fmaf(__uint_as_float(cw[r].y), xf[t].y, a);
+                        a = fmaf(__uint_as_float(cw[r].z), xf[t].z, a);
+                        a = fmaf(__uint_as_float(cw[r].w), xf[t].w, a);
+                        acc[t * 8 + r] = a;
+                    }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float xv[NS * EW];
+#pragma unroll
+                    for (int t = 0; t < NS; ++t)
+#pragma unroll
+                        for (int e4 = 0; e4 < EW; e4 += 4) {
+                            const float4 v4 =
+                                *reinterpret_cast<const float4 *>(xs + (size_t)t * p.k_pad + k0 + q * EW + e4);
+                            xv[t * EW + e4] = v4.x;
+                            xv[t * EW + e4 + 1] = v4.y;
+                            xv[t * EW + e4 + 2] = v4.z;
+                            xv[t * EW + e4 + 3] = v4.w;
+                        }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const uint32_t w = q == 0 ? cw[r].x : q == 1 ? cw[r].y : q == 2 ? cw[r].z : cw[r].w;
+                        float a2[NS];
+#pragma unroll
+                        for (int t = 0; t < NS; ++t) a2[t] = acc[t * 8 + r];
+                        word_fma<FMT, NS, EW>(w, xv, a2);
+#pragma unroll
+                        for (int t = 0; t < NS; ++t) acc[t * 8 + r] = a2[t];
+                    }
+                }
             }
         }
         __syncwarp();  // every lane is done with stage b before lane 0 refills it
-        if (has_tok) {
-            // rows 2q, 2q+1 of token g: hi terms (m = g) + lo terms (m = g + 8)
-            float2 v;
-            v.x = (c4[0][0] + c4[1][0]) + (c4[2][0] + c4[3][0]) + (c4[0][2] + c4[1][2]) + (c4[2][2] + c4[3][2]);
-            v.y = (c4[0][1] + c4[1][1]) + (c4[2][1] + c4[3][1]) + (c4[0][3] + c4[1][3]) + (c4[2][3] + c4[3][3]);
-            *reinterpret_cast<float2 *>(part + ((size_t)u * S + g) * 8 + 2 * q) = v;
-        }
+        const float v = reduce_scatter<NV>(acc, lane);
+        // this lane's value index is lane >> sh: (token, row) = (idx / 8, idx % 8)
+        constexpr int sh = NS == 2 ? 1 : 2;
+        const int idx = lane >> sh;
+        if ((lane & ((1 << sh) - 1)) == 0) part[((size_t)u * NS + idx / 8) * 8 + (idx & 7)] = v;
     }
     if (!ok) {
-        // give up: record the timeout, then let this warp's copies in flight
-        // land before the CTA's shared memory goes away
         if (lane == 0) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
         const int last = (i + depth - 1 < n_units ? i + depth - 1 : n_units - 1);
-        for (int v = i; v <= last; ++v) mbar_wait(my_bars + 8 * (v % depth), (uint32_t)((v / depth) & 1), kWaitNs / 4);
+        for (int v = i; v <= last; ++v)
+            mbar_wait(my_bars + 8 * (v % depth), (uint32_t)((v / depth) & 1), kWaitNs / 4);
     }
     __syncthreads();
 
-    // ---- combine the segments of each row group in a fixed order
+    // ---- combine segments in a fixed order, fold out the zero point, scale
     const int rows = (rg1 - rg0) * 8;
-    for (int idx = tid; idx < rows * S; idx += blockDim.x) {
-        const int s = idx / rows, r = idx - s * rows;
+    for (int idx = tid; idx < rows * NS; idx += nthr) {
+        const int t = idx / rows, r = idx - t * rows;
         const int rgl = r >> 3, rr = r & 7;
         float sum = 0.f;
-        for (int sg = 0; sg < nseg; ++sg) sum += part[((size_t)(rgl * nseg + sg) * S + s) * 8 + rr];
+        for (int sg = 0; sg < nseg; ++sg) sum += part[((size_t)(rgl * nseg + sg) * NS + t) * 8 + rr];
         const int rg = rg0 + rgl;
         const int set = rg >= p.rg_per_set;
         const int o = (rg - set * p.rg_per_set) * 8 + rr;
         if (o < p.O) {
             float *yb = set ? p.y[1] : p.y[0];
             const float *sb = set ? p.scales[1] : p.scales[0];
-            yb[(long long)s * p.y_ld + o] = ldexpf(sum, -exps[s]) * sb[o];
+            const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum - F<FMT>::ZP * tok_sum[t], -tok_exp[t]);
+            yb[(long long)t * p.y_ld + o] = dot * sb[o];
         }
     }
 }
 
 int g_sms = 0;
+
+template <int FMT, int NS>
+cudaError_t launch_ns(const DecParams &p, int grid, int nseg, cudaStream_t st) {
+    const size_t stage = (size_t)8 * (kSeg + 16) + 8;  // ring stage + its mbarrier
+    const size_t fixed = (size_t)4 * NS * p.k_pad + (size_t)p.max_units * NS * 8 * 4 + NS * 8 +
+                         (size_t)NS * kMaxWarps * 4;
+    int depth = 3, nw = kMaxWarps;
+    while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
+    if (fixed + (size_t)nw * depth * stage > kSmemMax) depth = 2;
+    while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
+    if (fixed + (size_t)nw * depth * stage > kSmemMax) return cudaErrorInvalidValue;  // x too long
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    DecParams q = p;
+    q.depth = depth;
+    qmv_decode_kernel<FMT, NS><<<grid, nw * 32, fixed + (size_t)nw * depth * stage, st>>>(q);
+    count_launch();
+    (void)nseg;
+    return cudaGetLastError();
+}
 
 template <int FMT>
 cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
@@ -461,70 +497,43 @@ cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float 
     p.k_pad = (int)t.k_pad;
     p.rg_per_set = (t.O + 7) / 8;
     p.n_rg = p.rg_per_set * (tu ? 2 : 1);
-    p.seg = (int)(t.ld < kSegMax ? t.ld : kSegMax);
-    const int nseg = (int)((t.ld + p.seg - 1) / p.seg);
-
-    // one CTA per SM unless the partial-sum buffer would grow too large
+    const int nseg = (int)((t.ld + kSeg - 1) / kSeg);
     int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
     const int max_rg_cta = 64;
     const int need = (p.n_rg + max_rg_cta - 1) / max_rg_cta;
     if (grid < need) grid = need;
     p.max_units = ((p.n_rg + grid - 1) / grid) * nseg;
 
-    // tokens per launch: at most 4 keeps the A-fragment shared-memory traffic
-    // under the SM's bandwidth; fewer when x terms would crowd out the rings
-    const size_t stage = (size_t)8 * (p.seg + 16) + 8;   // ring stage + its mbarrier
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemMax);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    auto fixed_for = [&](int sc) {
-        return (size_t)4 * sc * p.k_pad + (size_t)p.max_units * sc * 8 * 4 + kMaxS * 4 +
-               (size_t)kMaxS * kMaxWarps * 4;
-    };
     for (int s0 = 0; s0 < S;) {
-        int sc = S - s0 < 4 ? S - s0 : 4;
-        while (sc > 1 && fixed_for(sc) + (size_t)4 * 2 * stage > kSmemMax) --sc;
-        const size_t fixed = fixed_for(sc);
-        if (fixed + (size_t)4 * 2 * stage > kSmemMax) return cudaErrorInvalidValue;
-        int depth = 3, nw = kMaxWarps;
-        while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
-        if (fixed + (size_t)nw * depth * stage > kSmemMax) depth = 2;
-        while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
-        p.depth = depth;
-        p.S = sc;
+        const int ns = S - s0 >= 2 ? 2 : 1;
         p.x = x + (long long)s0 * t.I;
         p.y[0] = y + (long long)s0 * t.O;
         p.y[1] = tu ? yu + (long long)s0 * t.O : p.y[0];
-        const size_t smem = fixed + (size_t)nw * depth * stage;
-        qmv_decode_kernel<FMT><<<grid, nw * 32, smem, st>>>(p);
-        count_launch();
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = ns == 2 ? launch_ns<FMT, 2>(p, grid, nseg, st) : launch_ns<FMT, 1>(p, grid, nseg, st);
         if (e != cudaSuccess) return e;
-        s0 += sc;
+        s0 += ns;
     }
     return cudaSuccess;
 }
 
 }  // namespace
 
-// Handles int8 / int4 / int2 tensors for S below the tensor-core threshold;
-// *handled = false sends the call to the general SIMT kernel.
+// Handles every format for 1 <= S < 16 (tokens in launches of two);
+// *handled = false sends the call to the general SIMT kernel (x too long for
+// shared memory).
 cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
                           cudaStream_t st, bool *handled) {
     *handled = false;
     if (S < 1 || S > 15) return cudaSuccess;
     cudaError_t e = cudaSuccess;
     switch (t.fmt) {
+    case B200Q_F32: e = launch_fmt<B200Q_F32>(t, tu, x, y, yu, S, st); break;
     case B200Q_I8: e = launch_fmt<B200Q_I8>(t, tu, x, y, yu, S, st); break;
     case B200Q_I4: e = launch_fmt<B200Q_I4>(t, tu, x, y, yu, S, st); break;
     case B200Q_I2: e = launch_fmt<B200Q_I2>(t, tu, x, y, yu, S, st); break;
     default: return cudaSuccess;
     }
-    if (e == cudaErrorInvalidValue) return cudaSuccess;  // x too large for shared memory
+    if (e == cudaErrorInvalidValue) return cudaSuccess;
     *handled = (e == cudaSuccess);
     return e;
 }
