@@ -16,7 +16,10 @@
 //     offset in the word, exactly.  x is staged in shared memory pre-scaled by
 //     the matching power of two, so one FFMA forms code * x * 2^T exactly
 //     (2^T a per-token power of two that keeps every value in range).  The
-//     zero-point is folded out at the end: sum (c - z) x = sum c x - z sum x.
+//     zero-point comes out per lane and unit: the lane also runs a row of
+//     zero-point codes through the identical FFMA chain (its multipliers are
+//     compile-time constants) and subtracts it, so a run of zero-point codes
+//     cancels to exactly 0: sum (c - z) x = sum c x - sum z x.
 //     int4: nibbles 0-4 of a word are masked in place, nibbles 5-7 after one
 //     shift by 12; int8 (two's complement): the sign bits are flipped once per
 //     word (c + 128), bytes 0-1 in place, bytes 2-3 after one shift; int2:
@@ -53,26 +56,27 @@ __device__ unsigned int g_decode_err = 0;
 
 template <int FMT>
 struct F;
-// E: elements per 16-byte chunk; ZP: zero point of the extracted code
+// E: elements per 16-byte chunk; ZW: a code word whose every code is the
+// zero point (int8: the byte 0, i.e. 128 after the sign flip)
 template <>
 struct F<B200Q_F32> {
     static constexpr int E = 4;
-    static constexpr float ZP = 0.f;
+    static constexpr uint32_t ZW = 0u;
 };
 template <>
 struct F<B200Q_I8> {
     static constexpr int E = 16;
-    static constexpr float ZP = 128.f;
+    static constexpr uint32_t ZW = 0x00000000u;
 };
 template <>
 struct F<B200Q_I4> {
     static constexpr int E = 32;
-    static constexpr float ZP = 8.f;
+    static constexpr uint32_t ZW = 0x88888888u;
 };
 template <>
 struct F<B200Q_I2> {
     static constexpr int E = 64;
-    static constexpr float ZP = 2.f;
+    static constexpr uint32_t ZW = 0xAAAAAAAAu;
 };
 
 // Bit offset b of element e (0 <= e < 32 / bits) inside its extracted word:
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     }
     __syncwarp();
 
-    // ---- stage x: x'[t][k] = x[t][k] * 2^(T_t + 149 - b(k)); tok_sum = sum_k x * 2^T_t
+    // ---- stage x: x'[t][k] = x[t][k] * 2^(T_t + 149 - b(k))
     const int nthr = blockDim.x;
     if (FMT != B200Q_F32) {
         for (int t = 0; t < NS; ++t) {
@@ -323,31 +327,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     for (int t = 0; t < NS; ++t) {
         const float *xr = p.x + (long long)t * p.x_ld;
         const int T = FMT == B200Q_F32 ? 0 : tok_exp[t];
-        float psum = 0.f;
         for (int k = tid; k < p.k_pad; k += nthr) {
             const float v = k < p.I ? xr[k] : 0.f;
             if (FMT == B200Q_F32) {
                 xs[t * p.k_pad + k] = v;
             } else {
                 xs[t * p.k_pad + k] = ldexpf(v, T + 149 - bit_offset<FMT>(k % EW));
-                psum += ldexpf(v, T);
             }
-        }
-        if (FMT != B200Q_F32) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
-            if (lane == 0) red[t * kMaxWarps + warp] = psum;
         }
     }
     __syncthreads();
-    if (tid < NS) {
-        float ssum = 0.f;
-        if (FMT != B200Q_F32)
-            for (int w = 0; w < nw; ++w) ssum += red[tid * kMaxWarps + w];
-        tok_sum[tid] = ssum;
-        if (FMT == B200Q_F32) tok_exp[tid] = 0;
-    }
-    // (tok_sum / tok_exp are read only after the final __syncthreads)
+    if (FMT == B200Q_F32 && tid < NS) tok_exp[tid] = 0;   // read only after the final __syncthreads
 
     // ---- main loop: unit = (row group, 512-byte segment); lane = 16-byte chunk
     int i = 0;
@@ -363,9 +353,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
         const int sg = u % nseg;
         const long long left = p.ld - (long long)sg * kSeg;
         const int chunks = (int)((left < kSeg ? left : kSeg) / 16);
-        float acc[NV];
+        float acc[NV], accz[NS];
 #pragma unroll
         for (int a = 0; a < NV; ++a) acc[a] = 0.f;
+#pragma unroll
+        for (int t = 0; t < NS; ++t) accz[t] = 0.f;
         if (lane < chunks) {
             const uint8_t *st = my_ring + (size_t)b * stage_bytes + lane * 16;
             const int k0 = (sg * (kSeg / 16) + lane) * E;
@@ -412,8 +404,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
 #pragma unroll
                         for (int t = 0; t < NS; ++t) acc[t * 8 + r] = a2[t];
                     }
+                    word_fma<FMT, NS, EW>(F<FMT>::ZW, xv, accz);
                 }
             }
+        }
+        if (FMT != B200Q_F32) {
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[t * 8 + r] -= accz[t];
         }
         __syncwarp();  // every lane is done with stage b before lane 0 refills it
         const float v = reduce_scatter<NV>(acc, lane);
@@ -430,7 +429,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     }
     __syncthreads();
 
-    // ---- combine segments in a fixed order, fold out the zero point, scale
+    // ---- combine segments in a fixed order, unscale, apply the row scale
     const int rows = (rg1 - rg0) * 8;
     for (int idx = tid; idx < rows * NS; idx += nthr) {
         const int t = idx / rows, r = idx - t * rows;
@@ -443,7 +442,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
         if (o < p.O) {
             float *yb = set ? p.y[1] : p.y[0];
             const float *sb = set ? p.scales[1] : p.scales[0];
-            const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum - F<FMT>::ZP * tok_sum[t], -tok_exp[t]);
+            const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[t]);
             yb[(long long)t * p.y_ld + o] = dot * sb[o];
         }
     }
