@@ -31,7 +31,8 @@
 // (cp.async.bulk, mbarrier completion) that lane 0 issues DEPTH-1 units
 // ahead; ~15 warps x 2 stages keep ~120 KB per SM in flight.  In a unit,
 // lane l takes 16-byte chunk l of all 8 rows, so the x values it loads from
-// shared memory serve 8 rows.  Lane sums are combined with a butterfly
+// shared memory serve 8 rows; x is staged lane-interleaved so those loads
+// are conflict-free (a warp reads 512 contiguous bytes per load).  Lane sums are combined with a butterfly
 // reduce-scatter, each unit's 8 x NS partial sums go to shared memory, and
 // after the CTA's last unit the segments of every row are added in a fixed
 // order.  Units (row group, segment) are dealt round-robin to the warps of
@@ -235,10 +236,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     constexpr int rp = kSeg + 16;                    // smem row pitch (bank spread)
     constexpr int stage_bytes = 8 * rp;
     const int nseg = (int)((p.ld + kSeg - 1) / kSeg);
+    // elements staged per token: whole segments (the lane-interleaved layout
+    // addresses every lane slot of a segment), or k_pad for f32
+    const int k_alloc = FMT == B200Q_F32 ? p.k_pad : nseg * (kSeg / 4) * EW;
 
-    // shared memory: x' [NS][k_pad] | rings | mbarriers | partials | per-token terms
+    // shared memory: x' [NS][k_alloc] | rings | mbarriers | partials | per-token terms
     float *xs = reinterpret_cast<float *>(smem);
-    uint8_t *ring = smem + (size_t)4 * NS * p.k_pad;
+    uint8_t *ring = smem + (size_t)4 * NS * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stage_bytes);
     float *part = reinterpret_cast<float *>(bars + nw * depth);        // [unit][NS][8]
     float *tok_sum = part + (size_t)p.max_units * NS * 8;             // [NS] sum of x * 2^T
@@ -332,7 +336,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
             if (FMT == B200Q_F32) {
                 xs[t * p.k_pad + k] = v;
             } else {
-                xs[t * p.k_pad + k] = ldexpf(v, T + 149 - bit_offset<FMT>(k % EW));
+                // lane-interleaved: element k of chunk c (lane c % 32 of segment c / 32)
+                // goes where that lane's 16-byte read for (word, quad) lands
+                // next to the other lanes' reads: [seg][word][quad][lane][4]
+                const int c = k / E, ec = k - c * E;
+                const int lane_c = c & 31, seg_c = c >> 5;
+                const int q = ec / EW, e = ec - q * EW;
+                const int pos = (((seg_c * 4 + q) * (EW / 4) + (e >> 2)) * 32 + lane_c) * 4 + (e & 3);
+                xs[t * k_alloc + pos] = ldexpf(v, T + 149 - bit_offset<FMT>(e));
             }
         }
     }
@@ -387,8 +398,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
                     for (int t = 0; t < NS; ++t)
 #pragma unroll
                         for (int e4 = 0; e4 < EW; e4 += 4) {
-                            const float4 v4 =
-                                *reinterpret_cast<const float4 *>(xs + (size_t)t * p.k_pad + k0 + q * EW + e4);
+                            const float4 v4 = *reinterpret_cast<const float4 *>(
+                                xs + (size_t)t * k_alloc + ((((size_t)sg * 4 + q) * (EW / 4) + (e4 >> 2)) * 32 + lane) * 4);
                             xv[t * EW + e4] = v4.x;
                             xv[t * EW + e4 + 1] = v4.y;
                             xv[t * EW + e4 + 2] = v4.z;
@@ -452,8 +463,10 @@ int g_sms = 0;
 
 template <int FMT, int NS>
 cudaError_t launch_ns(const DecParams &p, int grid, int nseg, cudaStream_t st) {
+    constexpr int EW = FMT == B200Q_F32 ? 1 : FMT == B200Q_I8 ? 4 : FMT == B200Q_I4 ? 8 : 16;
+    const size_t k_alloc = FMT == B200Q_F32 ? (size_t)p.k_pad : (size_t)nseg * (kSeg / 4) * EW;
     const size_t stage = (size_t)8 * (kSeg + 16) + 8;  // ring stage + its mbarrier
-    const size_t fixed = (size_t)4 * NS * p.k_pad + (size_t)p.max_units * NS * 8 * 4 + NS * 8 +
+    const size_t fixed = (size_t)4 * NS * k_alloc + (size_t)p.max_units * NS * 8 * 4 + NS * 8 +
                          (size_t)NS * kMaxWarps * 4;
     int depth = 3, nw = kMaxWarps;
     while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
@@ -471,7 +484,6 @@ cudaError_t launch_ns(const DecParams &p, int grid, int nseg, cudaStream_t st) {
     q.depth = depth;
     qmv_decode_kernel<FMT, NS><<<grid, nw * 32, fixed + (size_t)nw * depth * stage, st>>>(q);
     count_launch();
-    (void)nseg;
     return cudaGetLastError();
 }
 
