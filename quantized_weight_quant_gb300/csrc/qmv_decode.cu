@@ -93,40 +93,43 @@ __device__ __forceinline__ int bit_offset<B200Q_I4>(int e) { return e < 5 ? 4 * 
 template <>
 __device__ __forceinline__ int bit_offset<B200Q_I2>(int e) { return e < 11 ? 2 * e : 2 * (e - 11); }  // >> 22
 
-// FFMA the codes of one 32-bit word of a quantized row against the staged x.
-template <int FMT, int NS, int EW>
-__device__ __forceinline__ void word_fma(uint32_t w, const float (&xv)[NS * EW], float (&acc)[NS]) {
+// The EW codes of one 32-bit word as exact subnormal f32 (code * 2^b * 2^-149).
+template <int FMT, int EW>
+__device__ __forceinline__ void word_codes(uint32_t w, float (&d)[EW]) {
     if (FMT == B200Q_I8) {
-        const uint32_t u = w ^ 0x80808080u;
+        const uint32_t u = w ^ 0x80808080u;  // two's complement -> code + 128
         const uint32_t v = u >> 16;
-#pragma unroll
-        for (int t = 0; t < NS; ++t) {
-            acc[t] = fmaf(__uint_as_float(u & 0xFFu), xv[t * EW + 0], acc[t]);
-            acc[t] = fmaf(__uint_as_float(u & 0xFF00u), xv[t * EW + 1], acc[t]);
-            acc[t] = fmaf(__uint_as_float(v & 0xFFu), xv[t * EW + 2], acc[t]);
-            acc[t] = fmaf(__uint_as_float(v & 0xFF00u), xv[t * EW + 3], acc[t]);
-        }
+        d[0] = __uint_as_float(u & 0xFFu);
+        d[1] = __uint_as_float(u & 0xFF00u);
+        d[2] = __uint_as_float(v & 0xFFu);
+        d[3] = __uint_as_float(v & 0xFF00u);
     } else if (FMT == B200Q_I4) {
         const uint32_t v = w >> 12;
 #pragma unroll
-        for (int t = 0; t < NS; ++t) {
+        for (int e = 0; e < 5; ++e) d[e] = __uint_as_float(w & (0xFu << (4 * e)));
 #pragma unroll
-            for (int e = 0; e < 5; ++e) acc[t] = fmaf(__uint_as_float(w & (0xFu << (4 * e))), xv[t * EW + e], acc[t]);
-#pragma unroll
-            for (int e = 5; e < 8; ++e)
-                acc[t] = fmaf(__uint_as_float(v & (0xFu << (4 * (e - 3)))), xv[t * EW + e], acc[t]);
-        }
+        for (int e = 5; e < 8; ++e) d[e] = __uint_as_float(v & (0xFu << (4 * (e - 3))));
     } else if (FMT == B200Q_I2) {
         const uint32_t v = w >> 22;
 #pragma unroll
-        for (int t = 0; t < NS; ++t) {
+        for (int e = 0; e < 11; ++e) d[e] = __uint_as_float(w & (0x3u << (2 * e)));
 #pragma unroll
-            for (int e = 0; e < 11; ++e) acc[t] = fmaf(__uint_as_float(w & (0x3u << (2 * e))), xv[t * EW + e], acc[t]);
-#pragma unroll
-            for (int e = 11; e < 16; ++e)
-                acc[t] = fmaf(__uint_as_float(v & (0x3u << (2 * (e - 11)))), xv[t * EW + e], acc[t]);
-        }
+        for (int e = 11; e < 16; ++e) d[e] = __uint_as_float(v & (0x3u << (2 * (e - 11))));
     }
+}
+
+// acc[t] += codes of word w times the staged x pairs, two products per
+// packed FP32x2 FMA (the even and odd elements of a pair accumulate in .x
+// and .y).
+template <int FMT, int NS, int EW>
+__device__ __forceinline__ void word_fma2(uint32_t w, const float2 (&xv)[NS * EW / 2], float2 (&acc)[NS]) {
+    float d[EW];
+    word_codes<FMT, EW>(w, d);
+#pragma unroll
+    for (int t = 0; t < NS; ++t)
+#pragma unroll
+        for (int i = 0; i < EW / 2; ++i)
+            acc[t] = __ffma2_rn(make_float2(d[2 * i], d[2 * i + 1]), xv[t * (EW / 2) + i], acc[t]);
 }
 
 // ---- mbarrier / bulk-copy helpers (PTX ISA: mbarrier, cp.async.bulk)
@@ -331,6 +334,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     for (int t = 0; t < NS; ++t) {
         const float *xr = p.x + (long long)t * p.x_ld;
         const int T = FMT == B200Q_F32 ? 0 : tok_exp[t];
+        // 2^(T + 23) = 2^-ilogb(max|x|), a normal f32 unless max|x| is subnormal
+        const float tscale = ldexpf(1.0f, T + 23);
         for (int k = tid; k < p.k_pad; k += nthr) {
             const float v = k < p.I ? xr[k] : 0.f;
             if (FMT == B200Q_F32) {
@@ -343,7 +348,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
                 const int lane_c = c & 31, seg_c = c >> 5;
                 const int q = ec / EW, e = ec - q * EW;
                 const int pos = (((seg_c * 4 + q) * (EW / 4) + (e >> 2)) * 32 + lane_c) * 4 + (e & 3);
-                xs[t * k_alloc + pos] = ldexpf(v, T + 149 - bit_offset<FMT>(e));
+                // v * 2^(T + 149 - b) = (v * 2^(T + 23)) * 2^(126 - b): both factors are
+                // normal powers of two for any finite x, so both products are exact
+                xs[t * k_alloc + pos] = (v * tscale) * __int_as_float((253 - bit_offset<FMT>(e)) << 23);
             }
         }
     }
@@ -364,66 +371,65 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
         const int sg = u % nseg;
         const long long left = p.ld - (long long)sg * kSeg;
         const int chunks = (int)((left < kSeg ? left : kSeg) / 16);
-        float acc[NV], accz[NS];
+        float acc[NV];
 #pragma unroll
         for (int a = 0; a < NV; ++a) acc[a] = 0.f;
-#pragma unroll
-        for (int t = 0; t < NS; ++t) accz[t] = 0.f;
         if (lane < chunks) {
             const uint8_t *st = my_ring + (size_t)b * stage_bytes + lane * 16;
-            const int k0 = (sg * (kSeg / 16) + lane) * E;
             uint4 cw[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rp);
-            if (FMT == B200Q_F32) {
+            if constexpr (FMT == B200Q_F32) {
+                const int k0 = (sg * (kSeg / 16) + lane) * E;
                 float4 xf[NS];
 #pragma unroll
-                for (int t = 0; t < NS; ++t) xf[t] = *reinterpret_cast<const float4 *>(xs + (size_t)t * p.k_pad + k0);
+                for (int t = 0; t < NS; ++t) xf[t] = *reinterpret_cast<const float4 *>(xs + (size_t)t * k_alloc + k0);
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
 #pragma unroll
                     for (int t = 0; t < NS; ++t) {
-                        float a = acc[t * 8 + r];
-                        a = fmaf(__uint_as_float(cw[r].x), xf[t].x, a);
-                        a = fmaf(__uint_as_float(cw[r].y), xf[t].y, a);
-                        a = fmaf(__uint_as_float(cw[r].z), xf[t].z, a);
-                        a = fmaf(__uint_as_float(cw[r].w), xf[t].w, a);
-                        acc[t * 8 + r] = a;
+                        float2 a = make_float2(0.f, 0.f);
+                        a = __ffma2_rn(make_float2(__uint_as_float(cw[r].x), __uint_as_float(cw[r].y)),
+                                       make_float2(xf[t].x, xf[t].y), a);
+                        a = __ffma2_rn(make_float2(__uint_as_float(cw[r].z), __uint_as_float(cw[r].w)),
+                                       make_float2(xf[t].z, xf[t].w), a);
+                        acc[t * 8 + r] = a.x + a.y;
                     }
             } else {
+                float2 a2[8][NS], az[NS];
+#pragma unroll
+                for (int t = 0; t < NS; ++t) {
+                    az[t] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) a2[r][t] = make_float2(0.f, 0.f);
+                }
+                // one 16-byte chunk = 4 words; x' for one word at a time
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float xv[NS * EW];
+                    float2 xv[NS * EW / 2];
 #pragma unroll
                     for (int t = 0; t < NS; ++t)
 #pragma unroll
                         for (int e4 = 0; e4 < EW; e4 += 4) {
                             const float4 v4 = *reinterpret_cast<const float4 *>(
                                 xs + (size_t)t * k_alloc + ((((size_t)sg * 4 + q) * (EW / 4) + (e4 >> 2)) * 32 + lane) * 4);
-                            xv[t * EW + e4] = v4.x;
-                            xv[t * EW + e4 + 1] = v4.y;
-                            xv[t * EW + e4 + 2] = v4.z;
-                            xv[t * EW + e4 + 3] = v4.w;
+                            xv[t * (EW / 2) + e4 / 2] = make_float2(v4.x, v4.y);
+                            xv[t * (EW / 2) + e4 / 2 + 1] = make_float2(v4.z, v4.w);
                         }
 #pragma unroll
                     for (int r = 0; r < 8; ++r) {
                         const uint32_t w = q == 0 ? cw[r].x : q == 1 ? cw[r].y : q == 2 ? cw[r].z : cw[r].w;
-                        float a2[NS];
-#pragma unroll
-                        for (int t = 0; t < NS; ++t) a2[t] = acc[t * 8 + r];
-                        word_fma<FMT, NS, EW>(w, xv, a2);
-#pragma unroll
-                        for (int t = 0; t < NS; ++t) acc[t * 8 + r] = a2[t];
+                        word_fma2<FMT, NS, EW>(w, xv, a2[r]);
                     }
-                    word_fma<FMT, NS, EW>(F<FMT>::ZW, xv, accz);
+                    word_fma2<FMT, NS, EW>(F<FMT>::ZW, xv, az);
                 }
+                // identical chains: runs of zero-point codes cancel exactly
+#pragma unroll
+                for (int t = 0; t < NS; ++t)
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        acc[t * 8 + r] = (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y);
             }
-        }
-        if (FMT != B200Q_F32) {
-#pragma unroll
-            for (int t = 0; t < NS; ++t)
-#pragma unroll
-                for (int r = 0; r < 8; ++r) acc[t * 8 + r] -= accz[t];
         }
         __syncwarp();  // every lane is done with stage b before lane 0 refills it
         const float v = reduce_scatter<NV>(acc, lane);
