@@ -50,6 +50,7 @@ namespace {
 
 constexpr int kMaxWarps = 15;
 constexpr int kSeg = 512;            // bytes per row per stage: 32 lanes x 16 B
+constexpr int kXB = 16;              // x elements per thread per staging batch
 constexpr size_t kSmemMax = 220 * 1024;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
 
@@ -286,76 +287,85 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     }
     __syncwarp();
 
-    // ---- stage x: x'[t][k] = x[t][k] * 2^(T_t + 149 - b(k))
+    // Everything above touched only the weights, which no kernel writes; x
+    // (and y) may be written (read) by the kernel before this one in the
+    // stream, so wait for it here (programmatic dependent launch), and let
+    // the next kernel in the stream start its own weight prefetch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // ---- stage x: x'[t][k] = x[t][k] * 2^(T_t + 149 - b(k)), with every
+    // thread's loads in flight at once (one round trip when k_pad <= kXB * threads)
     const int nthr = blockDim.x;
-    if (FMT != B200Q_F32) {
-        for (int t = 0; t < NS; ++t) {
-            const float *xr = p.x + (long long)t * p.x_ld;
-            float m = 0.f;
-            if ((p.x_ld & 3) == 0) {
-                const float4 *x4 = reinterpret_cast<const float4 *>(xr);
-                const int n4 = p.I / 4;
-                for (int base = 0; base < n4; base += 4 * nthr) {
-                    float4 v[4];
+    const int n_batch = (p.k_pad + kXB * nthr - 1) / (kXB * nthr);
+    float xr[NS][kXB];
+    auto load_batch = [&](int bt) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int k4 = base + i * nthr + tid;
-                        v[i] = k4 < n4 ? x4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+        for (int t = 0; t < NS; ++t)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-                }
-            } else {
-                for (int base = 0; base < p.I; base += 4 * nthr) {
-                    float v[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int k = base + i * nthr + tid;
-                        v[i] = k < p.I ? xr[k] : 0.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(v[i]));
-                }
+            for (int j = 0; j < kXB; ++j) {
+                const int k = (bt * kXB + j) * nthr + tid;
+                xr[t][j] = k < p.I ? p.x[(long long)t * p.x_ld + k] : 0.f;
             }
+    };
+    if (FMT != B200Q_F32) {
+        float m[NS];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) red[t * kMaxWarps + warp] = m;
+        for (int t = 0; t < NS; ++t) m[t] = 0.f;
+        for (int bt = 0; bt < n_batch; ++bt) {
+            load_batch(bt);
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int j = 0; j < kXB; ++j) m[t] = fmaxf(m[t], fabsf(xr[t][j]));
+        }
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
+            float mt = m[t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            if (lane == 0) red[t * kMaxWarps + warp] = mt;
         }
         __syncthreads();
         if (tid < NS) {
-            float m = 0.f;
-            for (int w = 0; w < nw; ++w) m = fmaxf(m, red[tid * kMaxWarps + w]);
+            float mt = 0.f;
+            for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[tid * kMaxWarps + w]);
             // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
-            tok_exp[tid] = m > 0.f ? -23 - ilogbf(m) : 0;
+            tok_exp[tid] = mt > 0.f ? -23 - ilogbf(mt) : 0;
         }
         __syncthreads();
+    } else if (tid < NS) {
+        tok_exp[tid] = 0;      // read only after the final __syncthreads
     }
-    for (int t = 0; t < NS; ++t) {
-        const float *xr = p.x + (long long)t * p.x_ld;
-        const int T = FMT == B200Q_F32 ? 0 : tok_exp[t];
-        // 2^(T + 23) = 2^-ilogb(max|x|), a normal f32 unless max|x| is subnormal
-        const float tscale = ldexpf(1.0f, T + 23);
-        for (int k = tid; k < p.k_pad; k += nthr) {
-            const float v = k < p.I ? xr[k] : 0.f;
-            if (FMT == B200Q_F32) {
-                xs[t * p.k_pad + k] = v;
-            } else {
-                // lane-interleaved: element k of chunk c (lane c % 32 of segment c / 32)
-                // goes where that lane's 16-byte read for (word, quad) lands
-                // next to the other lanes' reads: [seg][word][quad][lane][4]
-                const int c = k / E, ec = k - c * E;
-                const int lane_c = c & 31, seg_c = c >> 5;
-                const int q = ec / EW, e = ec - q * EW;
-                const int pos = (((seg_c * 4 + q) * (EW / 4) + (e >> 2)) * 32 + lane_c) * 4 + (e & 3);
-                // v * 2^(T + 149 - b) = (v * 2^(T + 23)) * 2^(126 - b): both factors are
-                // normal powers of two for any finite x, so both products are exact
-                xs[t * k_alloc + pos] = (v * tscale) * __int_as_float((253 - bit_offset<FMT>(e)) << 23);
+    for (int bt = 0; bt < n_batch; ++bt) {
+        if (FMT == B200Q_F32 || n_batch > 1) load_batch(bt);
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
+            // 2^(T + 23) = 2^-ilogb(max|x|), a normal f32 unless max|x| is subnormal
+            const float tscale = FMT == B200Q_F32 ? 1.f : ldexpf(1.0f, tok_exp[t] + 23);
+#pragma unroll
+            for (int j = 0; j < kXB; ++j) {
+                const int k = (bt * kXB + j) * nthr + tid;
+                if (k < p.k_pad) {
+                    const float v = xr[t][j];
+                    if (FMT == B200Q_F32) {
+                        xs[t * k_alloc + k] = v;
+                    } else {
+                        // lane-interleaved: element k of chunk c (lane c % 32 of segment
+                        // c / 32) goes next to the other lanes' reads: [seg][word][quad][lane][4]
+                        const int c = k / E, ec = k - c * E;
+                        const int lane_c = c & 31, seg_c = c >> 5;
+                        const int q = ec / EW, e = ec - q * EW;
+                        const int pos = (((seg_c * 4 + q) * (EW / 4) + (e >> 2)) * 32 + lane_c) * 4 + (e & 3);
+                        // v * 2^(T + 149 - b) = (v * 2^(T + 23)) * 2^(126 - b): both factors are
+                        // normal powers of two for any finite x, so both products are exact
+                        xs[t * k_alloc + pos] = (v * tscale) * __int_as_float((253 - bit_offset<FMT>(e)) << 23);
+                    }
+                }
             }
         }
     }
     __syncthreads();
-    if (FMT == B200Q_F32 && tid < NS) tok_exp[tid] = 0;   // read only after the final __syncthreads
 
     // ---- main loop: unit = (row group, 512-byte segment); lane = 16-byte chunk
     int i = 0;
@@ -488,8 +498,22 @@ cudaError_t launch_ns(const DecParams &p, int grid, int nseg, cudaStream_t st) {
     }
     DecParams q = p;
     q.depth = depth;
-    qmv_decode_kernel<FMT, NS><<<grid, nw * 32, fixed + (size_t)nw * depth * stage, st>>>(q);
+    // programmatic dependent launch: this grid may start while the previous
+    // kernel in the stream drains; it waits (griddepcontrol.wait) before it
+    // touches x or y
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(nw * 32);
+    cfg.dynamicSmemBytes = fixed + (size_t)nw * depth * stage;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS>, q);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
