@@ -233,6 +233,11 @@ b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, cons
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (st) cudaStreamDestroy(st);
+    if (e == cudaSuccess &&
+        !tmap_encode_2d(&t->dec_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, t->codes, (uint64_t)(t->ld / 4),
+                        (uint64_t)t->o_pad, (uint64_t)t->ld, (uint32_t)(t->ld < 512 ? t->ld / 4 : 128), 8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        e = cudaErrorNotSupported;
     if (e != cudaSuccess) {
         cuda_fail(e, "b200q_tensor_upload: copy");
         cudaGetLastError();

@@ -34,7 +34,6 @@
 // B200Q_ETIMEOUT (b200q_device_status) and the CTA winds down, draining its
 // copies and freeing its TMEM.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -412,8 +411,6 @@ __global__ void x_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__r
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
 cudaMemPool_t g_pool[64] = {};
 std::mutex g_pool_mu;
 int g_sms = 0;
@@ -434,24 +431,14 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out) {
     return cudaSuccess;
 }
 
-bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, void *base, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int FMT>
 cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, cudaStream_t st) {
     constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
     CUtensorMap map_codes, map_x;
-    if (!encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
+    if (!tmap_encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
                    (uint64_t)t.ld, code_bytes, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (!encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)xb, (uint64_t)t.k_pad, (uint64_t)S,
+    if (!tmap_encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)xb, (uint64_t)t.k_pad, (uint64_t)S,
                    (uint64_t)t.k_pad * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     GemmParams p{};
@@ -485,15 +472,6 @@ cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x,
                               cudaStream_t st, bool *handled) {
     *handled = false;
     if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return cudaSuccess;
-    std::call_once(g_encode_once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (!g_encode) return cudaErrorNotSupported;
     int dev = 0;
     cudaGetDevice(&dev);
     if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);

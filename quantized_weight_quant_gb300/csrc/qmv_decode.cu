@@ -26,23 +26,28 @@
 //     fields 0-10 in place, 11-15 after one shift; f32 weights FFMA directly.
 //     That is one AND and one FFMA per weight, plus a shift per word.
 //
-// Data movement: every warp streams units of 8 weight rows x 512 bytes
-// through its own ring of shared-memory stages, filled by bulk async copies
-// (cp.async.bulk, mbarrier completion) that lane 0 issues DEPTH-1 units
-// ahead; ~15 warps x 2 stages keep ~120 KB per SM in flight.  In a unit,
-// lane l takes 16-byte chunk l of all 8 rows, so the x values it loads from
-// shared memory serve 8 rows; x is staged lane-interleaved so those loads
-// are conflict-free (a warp reads 512 contiguous bytes per load).  Lane sums are combined with a butterfly
-// reduce-scatter, each unit's 8 x NS partial sums go to shared memory, and
-// after the CTA's last unit the segments of every row are added in a fixed
-// order.  Units (row group, segment) are dealt round-robin to the warps of
-// persistent CTAs that own contiguous runs of row groups.  Every mbarrier
-// wait is bounded; a wait that gives up records B200Q_ETIMEOUT in a device
-// word (b200q_device_status), drains its own copies and returns.
+// Data movement: a unit is 8 weight rows x 512 bytes.  Every warp streams its
+// units through its own ring of DEPTH shared-memory stages, each filled by one
+// 2-D TMA copy (cp.async.bulk.tensor, mbarrier completion) that lane 0 issues
+// DEPTH-1 units ahead; ~15 warps x 2 stages keep ~120 KB per SM in flight.
+// In a unit, lane l takes 16-byte chunk l of all 8 rows (a warp-wide load
+// reads one row's 512 contiguous bytes), so the x values it loads from shared
+// memory serve 8 rows; x is staged lane-interleaved so those loads are
+// conflict-free.  The units of a CTA are split into contiguous runs, one per
+// warp, in row-group-major order; a warp keeps its sums in registers across
+// the segments of a row group and combines its lanes (butterfly
+// reduce-scatter) only when its row group changes.  The per-warp partial
+// sums of each row group are added in warp order after the run, in rounds of
+// at most 16 row groups.  Persistent CTAs own contiguous runs of row groups.
+// Every mbarrier wait is bounded; a wait that gives up records
+// B200Q_ETIMEOUT in a device word (b200q_device_status), drains the warp's
+// copies in flight and returns.
 //
-// Accuracy: f32 FFMA chains of at most 32 terms per lane and unit, then
-// fixed-order f32 additions; with the zero-point folded out the result stays
-// within 1e-5 of sum |scale * deq * x| on the workloads' distributions.
+// Accuracy: per lane and row group, f32 FFMA chains over the lane's chunks,
+// then fixed-order f32 additions; with the zero point taken out by the
+// identical chain the result stays within 1e-5 of sum |scale * deq * x| on
+// the workloads' distributions and is exact where every code is the zero
+// point.
 #include "qwq_internal.h"
 
 namespace qwq {
@@ -50,6 +55,8 @@ namespace {
 
 constexpr int kMaxWarps = 15;
 constexpr int kSeg = 512;            // bytes per row per stage: 32 lanes x 16 B
+constexpr int kStage = 8 * kSeg;     // one stage: 8 rows x 512 B (one TMA box)
+constexpr int kRound = 16;           // row groups combined per round
 constexpr int kXB = 16;              // x elements per thread per staging batch
 constexpr size_t kSmemMax = 220 * 1024;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
@@ -145,12 +152,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
-                                         uint64_t policy) {
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-        "%4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -211,35 +218,35 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
 }
 
 struct DecParams {
-    const uint8_t *codes[2];
     const float *scales[2];
     float *y[2];
     const float *x;      // [S, I] f32 (offset to this launch's first token)
     int x_ld;            // row stride of x in elements (I)
     int y_ld;            // row stride of y in elements (O)
     int O, I;
-    long long ld;        // device row stride in bytes
+    int ld;              // device row stride in bytes
+    int row_bytes;       // bytes per row per stage: min(512, ld)
     int k_pad;           // elements per padded row
     int rg_per_set;      // ceil(O / 8)
     int n_rg;            // total row groups (sets * rg_per_set)
     int depth;           // stages per warp
-    int max_units;       // bound on (row group, segment) units per CTA
 };
 
 template <int FMT, int NS>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const DecParams p) {
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    qmv_decode_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+                      const DecParams p) {
     constexpr int E = F<FMT>::E;
     constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
     constexpr int EW = 32 / bits;                    // elements per 32-bit word
-    constexpr int NV = 8 * NS;                       // partial sums per lane and unit
+    constexpr int NV = 8 * NS;                       // partial sums per lane and row group
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = blockDim.x >> 5;
     const int depth = p.depth;
-    constexpr int rp = kSeg + 16;                    // smem row pitch (bank spread)
-    constexpr int stage_bytes = 8 * rp;
-    const int nseg = (int)((p.ld + kSeg - 1) / kSeg);
+    const int nseg = (p.ld + kSeg - 1) / kSeg;
+    const int rb = p.row_bytes;                       // smem row pitch of a stage
     // elements staged per token: whole segments (the lane-interleaved layout
     // addresses every lane slot of a segment), or k_pad for f32
     const int k_alloc = FMT == B200Q_F32 ? p.k_pad : nseg * (kSeg / 4) * EW;
@@ -247,43 +254,66 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     // shared memory: x' [NS][k_alloc] | rings | mbarriers | partials | per-token terms
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * NS * k_alloc;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stage_bytes);
-    float *part = reinterpret_cast<float *>(bars + nw * depth);        // [unit][NS][8]
-    float *tok_sum = part + (size_t)p.max_units * NS * 8;             // [NS] sum of x * 2^T
-    int *tok_exp = reinterpret_cast<int *>(tok_sum + NS);              // [NS] T
-    float *red = reinterpret_cast<float *>(tok_exp + NS);              // [NS][kMaxWarps]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * kStage);
+    float *part = reinterpret_cast<float *>(bars + nw * depth);        // [kRound][nw][NS][8]
+    int *tok_exp = reinterpret_cast<int *>(part + (size_t)kRound * nw * NS * 8);  // [NS] T
+    float *red = reinterpret_cast<float *>(tok_exp + NS);             // [NS][kMaxWarps]
 
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
-    const int cta_units = (rg1 - rg0) * nseg;
-    const int n_units = cta_units > warp ? (cta_units - warp + nw - 1) / nw : 0;
 
-    uint8_t *my_ring = ring + (size_t)warp * depth * stage_bytes;
+    // This warp's units: in round r (row groups [rg0 + 16 r, ...)), the run
+    // [w U / nw, (w + 1) U / nw) of its U = rows * nseg units, row-group-major.
+    // A cursor walks them in order across rounds.
+    struct Cursor {
+        int round_base, round_end;   // row groups of the current round
+        int u, u_end;                // unit index within the round's run
+    };
+    auto run_of = [&](Cursor &c, int base) {
+        c.round_base = base;
+        c.round_end = base + kRound < rg1 ? base + kRound : rg1;
+        const int U = (c.round_end - c.round_base) * nseg;
+        c.u = (int)((long long)warp * U / nw);
+        c.u_end = (int)((long long)(warp + 1) * U / nw);
+    };
+    auto normalize = [&](Cursor &c) {  // skip empty runs; false when past the last round
+        while (c.u >= c.u_end) {
+            if (c.round_end >= rg1) return false;
+            run_of(c, c.round_end);
+        }
+        return true;
+    };
+
+    uint8_t *my_ring = ring + (size_t)warp * depth * kStage;
     const uint32_t my_bars = smem_u32(bars + warp * depth);
     uint64_t policy = 0;
 
-    auto issue = [&](int i) {  // lane 0 only: this warp's i-th unit
-        const int u = warp + i * nw;
-        const int rgl = u / nseg, sg = u - rgl * nseg;
-        const int rg = rg0 + rgl;
+    // producer state (lane 0 only)
+    Cursor pc;
+    run_of(pc, rg0);
+    int p_stage = 0;
+    long long issued = 0;
+    auto issue_next = [&]() -> bool {  // lane 0: copy the next unit into the next stage
+        if (!normalize(pc)) return false;
+        const int rgl = pc.u / nseg, sg = pc.u - rgl * nseg;
+        const int rg = pc.round_base + rgl;
         const int set = rg >= p.rg_per_set;
-        const uint8_t *base = (set ? p.codes[1] : p.codes[0]) +
-                              (long long)((rg - set * p.rg_per_set) * 8) * p.ld + (long long)sg * kSeg;
-        const long long left = p.ld - (long long)sg * kSeg;
-        const uint32_t bytes = (uint32_t)(left < kSeg ? left : kSeg);
-        const int b = i % depth;
-        const uint32_t bar = my_bars + 8 * b;
-        const uint32_t dst = smem_u32(my_ring + (size_t)b * stage_bytes);
-        mbar_expect_tx(bar, 8 * bytes);
-#pragma unroll
-        for (int r = 0; r < 8; ++r) bulk_g2s(dst + r * rp, base + (long long)r * p.ld, bytes, bar, policy);
+        const uint32_t bar = my_bars + 8 * p_stage;
+        mbar_expect_tx(bar, (uint32_t)(8 * rb));
+        tma_load_2d(smem_u32(my_ring + (size_t)p_stage * kStage), set ? &map1 : &map0, sg * (kSeg / 4),
+                    (rg - set * p.rg_per_set) * 8, bar, policy);
+        ++pc.u;
+        ++issued;
+        if (++p_stage == depth) p_stage = 0;
+        return true;
     };
 
     if (lane == 0) {
         for (int b = 0; b < depth; ++b) mbar_init(my_bars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         policy = evict_first_policy();
-        for (int i = 0; i < depth - 1 && i < n_units; ++i) issue(i);
+        for (int i = 0; i < depth - 1; ++i)
+            if (!issue_next()) break;
     }
     __syncwarp();
 
@@ -367,110 +397,139 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
     }
     __syncthreads();
 
-    // ---- main loop: unit = (row group, 512-byte segment); lane = 16-byte chunk
-    int i = 0;
+    // ---- main loop
+    Cursor cc;
+    run_of(cc, rg0);
+    int c_stage = 0;
+    uint32_t c_phase = 0;
     bool ok = true;
-    for (; i < n_units; ++i) {
-        if (lane == 0 && i + depth - 1 < n_units) issue(i + depth - 1);
-        const int b = i % depth;
-        if (!mbar_wait(my_bars + 8 * b, (uint32_t)((i / depth) & 1), kWaitNs)) {
-            ok = false;
-            break;
+    float2 a2[8][NS], az[NS];
+    auto clear_acc = [&]() {
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
+            az[t] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) a2[r][t] = make_float2(0.f, 0.f);
         }
-        const int u = warp + i * nw;
-        const int sg = u % nseg;
-        const long long left = p.ld - (long long)sg * kSeg;
-        const int chunks = (int)((left < kSeg ? left : kSeg) / 16);
-        float acc[NV];
+    };
+    // lane sums of the current row group -> part[rgl][warp]
+    auto flush = [&](int rgl) {
+        float v[NV];
 #pragma unroll
-        for (int a = 0; a < NV; ++a) acc[a] = 0.f;
-        if (lane < chunks) {
-            const uint8_t *st = my_ring + (size_t)b * stage_bytes + lane * 16;
-            uint4 cw[8];
+        for (int t = 0; t < NS; ++t)
 #pragma unroll
-            for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rp);
-            if constexpr (FMT == B200Q_F32) {
-                const int k0 = (sg * (kSeg / 16) + lane) * E;
-                float4 xf[NS];
+            for (int r = 0; r < 8; ++r)
+                v[t * 8 + r] = FMT == B200Q_F32 ? a2[r][t].x + a2[r][t].y
+                                                : (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y);
+        const float sum = reduce_scatter<NV>(v, lane);
+        constexpr int sh = NS == 2 ? 1 : 2;         // this lane holds value index lane >> sh
+        const int idx = lane >> sh;
+        if ((lane & ((1 << sh) - 1)) == 0) part[(((size_t)rgl * nw + warp) * NS + idx / 8) * 8 + (idx & 7)] = sum;
+        clear_acc();
+    };
+    clear_acc();
+
+    for (int base = rg0; base < rg1 && ok; base += kRound) {
+        const int rend = base + kRound < rg1 ? base + kRound : rg1;
+        // zero this round's partials (warps that touch no unit of a row group leave 0)
+        for (int i = tid; i < kRound * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
+        __syncthreads();
+        run_of(cc, base);
+        int cur_rgl = -1;
+        for (; cc.u < cc.u_end; ++cc.u) {
+            if (lane == 0) issue_next();
+            if (!mbar_wait(my_bars + 8 * c_stage, c_phase, kWaitNs)) {
+                ok = false;
+                break;
+            }
+            const int rgl = cc.u / nseg, sg = cc.u - rgl * nseg;
+            if (rgl != cur_rgl) {
+                if (cur_rgl >= 0) flush(cur_rgl);
+                cur_rgl = rgl;
+            }
+            const int chunks = (p.ld - sg * kSeg < kSeg ? p.ld - sg * kSeg : kSeg) / 16;
+            if (lane < chunks) {
+                const uint8_t *st = my_ring + (size_t)c_stage * kStage + lane * 16;
+                uint4 cw[8];
 #pragma unroll
-                for (int t = 0; t < NS; ++t) xf[t] = *reinterpret_cast<const float4 *>(xs + (size_t)t * k_alloc + k0);
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
+                for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rb);
+                if constexpr (FMT == B200Q_F32) {
+                    const int k0 = (sg * (kSeg / 16) + lane) * E;
 #pragma unroll
                     for (int t = 0; t < NS; ++t) {
-                        float2 a = make_float2(0.f, 0.f);
-                        a = __ffma2_rn(make_float2(__uint_as_float(cw[r].x), __uint_as_float(cw[r].y)),
-                                       make_float2(xf[t].x, xf[t].y), a);
-                        a = __ffma2_rn(make_float2(__uint_as_float(cw[r].z), __uint_as_float(cw[r].w)),
-                                       make_float2(xf[t].z, xf[t].w), a);
-                        acc[t * 8 + r] = a.x + a.y;
-                    }
-            } else {
-                float2 a2[8][NS], az[NS];
+                        const float4 xf = *reinterpret_cast<const float4 *>(xs + (size_t)t * k_alloc + k0);
 #pragma unroll
-                for (int t = 0; t < NS; ++t) {
-                    az[t] = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) a2[r][t] = make_float2(0.f, 0.f);
-                }
-                // one 16-byte chunk = 4 words; x' for one word at a time
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float2 xv[NS * EW / 2];
-#pragma unroll
-                    for (int t = 0; t < NS; ++t)
-#pragma unroll
-                        for (int e4 = 0; e4 < EW; e4 += 4) {
-                            const float4 v4 = *reinterpret_cast<const float4 *>(
-                                xs + (size_t)t * k_alloc + ((((size_t)sg * 4 + q) * (EW / 4) + (e4 >> 2)) * 32 + lane) * 4);
-                            xv[t * (EW / 2) + e4 / 2] = make_float2(v4.x, v4.y);
-                            xv[t * (EW / 2) + e4 / 2 + 1] = make_float2(v4.z, v4.w);
+                        for (int r = 0; r < 8; ++r) {
+                            a2[r][t] = __ffma2_rn(make_float2(__uint_as_float(cw[r].x), __uint_as_float(cw[r].y)),
+                                                  make_float2(xf.x, xf.y), a2[r][t]);
+                            a2[r][t] = __ffma2_rn(make_float2(__uint_as_float(cw[r].z), __uint_as_float(cw[r].w)),
+                                                  make_float2(xf.z, xf.w), a2[r][t]);
                         }
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const uint32_t w = q == 0 ? cw[r].x : q == 1 ? cw[r].y : q == 2 ? cw[r].z : cw[r].w;
-                        word_fma2<FMT, NS, EW>(w, xv, a2[r]);
                     }
-                    word_fma2<FMT, NS, EW>(F<FMT>::ZW, xv, az);
+                } else {
+                    // one 16-byte chunk = 4 words; x' for one word at a time
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float2 xv[NS * EW / 2];
+#pragma unroll
+                        for (int t = 0; t < NS; ++t)
+#pragma unroll
+                            for (int e4 = 0; e4 < EW; e4 += 4) {
+                                const float4 v4 = *reinterpret_cast<const float4 *>(
+                                    xs + (size_t)t * k_alloc +
+                                    ((((size_t)sg * 4 + q) * (EW / 4) + (e4 >> 2)) * 32 + lane) * 4);
+                                xv[t * (EW / 2) + e4 / 2] = make_float2(v4.x, v4.y);
+                                xv[t * (EW / 2) + e4 / 2 + 1] = make_float2(v4.z, v4.w);
+                            }
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const uint32_t w = q == 0 ? cw[r].x : q == 1 ? cw[r].y : q == 2 ? cw[r].z : cw[r].w;
+                            word_fma2<FMT, NS, EW>(w, xv, a2[r]);
+                        }
+                        word_fma2<FMT, NS, EW>(F<FMT>::ZW, xv, az);
+                    }
                 }
-                // identical chains: runs of zero-point codes cancel exactly
-#pragma unroll
-                for (int t = 0; t < NS; ++t)
-#pragma unroll
-                    for (int r = 0; r < 8; ++r)
-                        acc[t * 8 + r] = (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y);
+            }
+            __syncwarp();  // every lane is done with this stage before lane 0 refills it
+            if (++c_stage == depth) {
+                c_stage = 0;
+                c_phase ^= 1;
             }
         }
-        __syncwarp();  // every lane is done with stage b before lane 0 refills it
-        const float v = reduce_scatter<NV>(acc, lane);
-        // this lane's value index is lane >> sh: (token, row) = (idx / 8, idx % 8)
-        constexpr int sh = NS == 2 ? 1 : 2;
-        const int idx = lane >> sh;
-        if ((lane & ((1 << sh) - 1)) == 0) part[((size_t)u * NS + idx / 8) * 8 + (idx & 7)] = v;
+        if (cur_rgl >= 0) flush(cur_rgl);
+        __syncthreads();
+        // combine this round: warps in order, unscale, apply the row scale
+        const int rows = (rend - base) * 8;
+        for (int t = 0; t < NS; ++t) {
+            for (int r = tid; r < rows; r += blockDim.x) {
+                const int rgl = r >> 3, rr = r & 7;
+                float sum = 0.f;
+                for (int w = 0; w < nw; ++w) sum += part[(((size_t)rgl * nw + w) * NS + t) * 8 + rr];
+                const int rg = base + rgl;
+                const int set = rg >= p.rg_per_set;
+                const int o = (rg - set * p.rg_per_set) * 8 + rr;
+                if (o < p.O) {
+                    float *yb = set ? p.y[1] : p.y[0];
+                    const float *sb = set ? p.scales[1] : p.scales[0];
+                    const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[t]);
+                    yb[(long long)t * p.y_ld + o] = dot * sb[o];
+                }
+            }
+        }
+        __syncthreads();   // part is reused by the next round
     }
     if (!ok) {
+        // give up: record the timeout and let this warp's copies land first
         if (lane == 0) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
-        const int last = (i + depth - 1 < n_units ? i + depth - 1 : n_units - 1);
-        for (int v = i; v <= last; ++v)
-            mbar_wait(my_bars + 8 * (v % depth), (uint32_t)((v / depth) & 1), kWaitNs / 4);
-    }
-    __syncthreads();
-
-    // ---- combine segments in a fixed order, unscale, apply the row scale
-    const int rows = (rg1 - rg0) * 8;
-    for (int idx = tid; idx < rows * NS; idx += nthr) {
-        const int t = idx / rows, r = idx - t * rows;
-        const int rgl = r >> 3, rr = r & 7;
-        float sum = 0.f;
-        for (int sg = 0; sg < nseg; ++sg) sum += part[((size_t)(rgl * nseg + sg) * NS + t) * 8 + rr];
-        const int rg = rg0 + rgl;
-        const int set = rg >= p.rg_per_set;
-        const int o = (rg - set * p.rg_per_set) * 8 + rr;
-        if (o < p.O) {
-            float *yb = set ? p.y[1] : p.y[0];
-            const float *sb = set ? p.scales[1] : p.scales[0];
-            const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[t]);
-            yb[(long long)t * p.y_ld + o] = dot * sb[o];
+        // issued units not yet consumed occupy the next stages in order
+        long long consumed = 0;  // recount: stages wrap, so wait on the next `depth` phases
+        (void)consumed;
+        for (int k = 0; k < depth; ++k) {
+            mbar_wait(my_bars + 8 * c_stage, c_phase, kWaitNs / 4);
+            if (++c_stage == depth) {
+                c_stage = 0;
+                c_phase ^= 1;
+            }
         }
     }
 }
@@ -478,17 +537,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const Dec
 int g_sms = 0;
 
 template <int FMT, int NS>
-cudaError_t launch_ns(const DecParams &p, int grid, int nseg, cudaStream_t st) {
+cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int grid, cudaStream_t st) {
     constexpr int EW = FMT == B200Q_F32 ? 1 : FMT == B200Q_I8 ? 4 : FMT == B200Q_I4 ? 8 : 16;
+    const int nseg = (p.ld + kSeg - 1) / kSeg;
     const size_t k_alloc = FMT == B200Q_F32 ? (size_t)p.k_pad : (size_t)nseg * (kSeg / 4) * EW;
-    const size_t stage = (size_t)8 * (kSeg + 16) + 8;  // ring stage + its mbarrier
-    const size_t fixed = (size_t)4 * NS * k_alloc + (size_t)p.max_units * NS * 8 * 4 + NS * 8 +
-                         (size_t)NS * kMaxWarps * 4;
+    const size_t stage = (size_t)kStage + 8;                 // ring stage + its mbarrier
+    auto fixed_for = [&](int nw) {
+        return (size_t)4 * NS * k_alloc + (size_t)kRound * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4;
+    };
     int depth = 3, nw = kMaxWarps;
-    while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
-    if (fixed + (size_t)nw * depth * stage > kSmemMax) depth = 2;
-    while (nw > 4 && fixed + (size_t)nw * depth * stage > kSmemMax) --nw;
-    if (fixed + (size_t)nw * depth * stage > kSmemMax) return cudaErrorInvalidValue;  // x too long
+    while (nw > 4 && fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) --nw;
+    if (fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) depth = 2;
+    while (nw > 4 && fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) --nw;
+    if (fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) return cudaErrorInvalidValue;  // x too long
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS>,
@@ -504,14 +565,14 @@ cudaError_t launch_ns(const DecParams &p, int grid, int nseg, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(nw * 32);
-    cfg.dynamicSmemBytes = fixed + (size_t)nw * depth * stage;
+    cfg.dynamicSmemBytes = fixed_for(nw) + (size_t)nw * depth * stage;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS>, q);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS>, t.dec_map, tu ? tu->dec_map : t.dec_map, q);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -526,31 +587,24 @@ cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float 
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     }
     DecParams p{};
-    p.codes[0] = t.codes;
     p.scales[0] = t.scales;
-    p.codes[1] = tu ? tu->codes : t.codes;
     p.scales[1] = tu ? tu->scales : t.scales;
     p.x_ld = t.I;
     p.y_ld = t.O;
     p.O = t.O;
     p.I = t.I;
-    p.ld = t.ld;
+    p.ld = (int)t.ld;
+    p.row_bytes = (int)(t.ld < kSeg ? t.ld : kSeg);
     p.k_pad = (int)t.k_pad;
     p.rg_per_set = (t.O + 7) / 8;
     p.n_rg = p.rg_per_set * (tu ? 2 : 1);
-    const int nseg = (int)((t.ld + kSeg - 1) / kSeg);
-    int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
-    const int max_rg_cta = 64;
-    const int need = (p.n_rg + max_rg_cta - 1) / max_rg_cta;
-    if (grid < need) grid = need;
-    p.max_units = ((p.n_rg + grid - 1) / grid) * nseg;
-
+    const int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
     for (int s0 = 0; s0 < S;) {
         const int ns = S - s0 >= 2 ? 2 : 1;
         p.x = x + (long long)s0 * t.I;
         p.y[0] = y + (long long)s0 * t.O;
         p.y[1] = tu ? yu + (long long)s0 * t.O : p.y[0];
-        cudaError_t e = ns == 2 ? launch_ns<FMT, 2>(p, grid, nseg, st) : launch_ns<FMT, 1>(p, grid, nseg, st);
+        cudaError_t e = ns == 2 ? launch_ns<FMT, 2>(t, tu, p, grid, st) : launch_ns<FMT, 1>(t, tu, p, grid, st);
         if (e != cudaSuccess) return e;
         s0 += ns;
     }

@@ -1,6 +1,7 @@
 // Internal declarations of the b200q library (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -17,6 +18,7 @@ namespace qwq {
 //        o >= O all hold the format's zero-point code, so they decode to 0.
 // scales: [o_pad] f32; rows o >= O have scale 0.
 struct Tensor {
+    CUtensorMap dec_map;  // codes as uint32 [o_pad, ld / 4], box 8 rows x 512 bytes (decode stages)
     int fmt;
     int O, I;
     int device;
@@ -39,6 +41,12 @@ inline int fmt_bits(int fmt) {
 inline uint8_t zero_byte(int fmt) {
     return fmt == B200Q_I4 ? 0x88 : fmt == B200Q_I2 ? 0xAA : 0x00;
 }
+
+// 2-D tiled tensor map (cuTensorMapEncodeTiled through the runtime's driver
+// entry point): inner extent `inner` elements, `outer` rows of `row_bytes`.
+// Returns false if the driver entry point is missing or encoding fails.
+bool tmap_encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 // Counts kernel launches made through the library (b200q_kernel_launches).
 void count_launch(int n = 1);
