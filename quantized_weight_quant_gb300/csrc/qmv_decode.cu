@@ -230,6 +230,7 @@ struct DecParams {
     int rg_per_set;      // ceil(O / 8)
     int n_rg;            // total row groups (sets * rg_per_set)
     int depth;           // stages per warp
+    int round_rgs;       // row groups combined per round (partials buffer rows)
 };
 
 template <int FMT, int NS>
@@ -255,8 +256,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * NS * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * kStage);
-    float *part = reinterpret_cast<float *>(bars + nw * depth);        // [kRound][nw][NS][8]
-    int *tok_exp = reinterpret_cast<int *>(part + (size_t)kRound * nw * NS * 8);  // [NS] T
+    const int kR = p.round_rgs;
+    float *part = reinterpret_cast<float *>(bars + nw * depth);        // [kR][nw][NS][8]
+    int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [NS] T
     float *red = reinterpret_cast<float *>(tok_exp + NS);             // [NS][kMaxWarps]
 
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     };
     auto run_of = [&](Cursor &c, int base) {
         c.round_base = base;
-        c.round_end = base + kRound < rg1 ? base + kRound : rg1;
+        c.round_end = base + kR < rg1 ? base + kR : rg1;
         const int U = (c.round_end - c.round_base) * nseg;
         c.u = (int)((long long)warp * U / nw);
         c.u_end = (int)((long long)(warp + 1) * U / nw);
@@ -429,10 +431,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     };
     clear_acc();
 
-    for (int base = rg0; base < rg1 && ok; base += kRound) {
-        const int rend = base + kRound < rg1 ? base + kRound : rg1;
+    for (int base = rg0; base < rg1 && ok; base += kR) {
+        const int rend = base + kR < rg1 ? base + kR : rg1;
         // zero this round's partials (warps that touch no unit of a row group leave 0)
-        for (int i = tid; i < kRound * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
+        for (int i = tid; i < kR * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
         __syncthreads();
         run_of(cc, base);
         int cur_rgl = -1;
@@ -542,14 +544,25 @@ cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int
     const int nseg = (p.ld + kSeg - 1) / kSeg;
     const size_t k_alloc = FMT == B200Q_F32 ? (size_t)p.k_pad : (size_t)nseg * (kSeg / 4) * EW;
     const size_t stage = (size_t)kStage + 8;                 // ring stage + its mbarrier
-    auto fixed_for = [&](int nw) {
-        return (size_t)4 * NS * k_alloc + (size_t)kRound * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4;
+    const int rg_cta = (p.n_rg + grid - 1) / grid;
+    auto fixed_for = [&](int nw, int rr) {
+        return (size_t)4 * NS * k_alloc + (size_t)rr * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4;
     };
+    // warps and depth first (round of kRound), then grow the round to all of
+    // the CTA's row groups if the partials still fit (one round: no barrier)
     int depth = 3, nw = kMaxWarps;
-    while (nw > 4 && fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) --nw;
-    if (fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) depth = 2;
-    while (nw > 4 && fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) --nw;
-    if (fixed_for(nw) + (size_t)nw * depth * stage > kSmemMax) return cudaErrorInvalidValue;  // x too long
+    while (nw > 4 && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) --nw;
+    if (fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) depth = 2;
+    while (nw > 4 && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) --nw;
+    if (fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) return cudaErrorInvalidValue;  // x too long
+    int rr = kRound;
+    if (rg_cta <= kRound) {
+        rr = rg_cta;
+    } else {
+        int big = rg_cta;
+        while (big > kRound && fixed_for(nw, big) + (size_t)nw * depth * stage > kSmemMax) big = (big + kRound) / 2;
+        rr = big > kRound ? big : kRound;
+    }
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS>,
@@ -559,13 +572,14 @@ cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int
     }
     DecParams q = p;
     q.depth = depth;
+    q.round_rgs = rr;
     // programmatic dependent launch: this grid may start while the previous
     // kernel in the stream drains; it waits (griddepcontrol.wait) before it
     // touches x or y
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(nw * 32);
-    cfg.dynamicSmemBytes = fixed_for(nw) + (size_t)nw * depth * stage;
+    cfg.dynamicSmemBytes = fixed_for(nw, rr) + (size_t)nw * depth * stage;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
