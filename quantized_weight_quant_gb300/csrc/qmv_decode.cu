@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     float *part = reinterpret_cast<float *>(bars + nw * depth);        // [kR][nw][NS][8]
     int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [NS] T
     float *red = reinterpret_cast<float *>(tok_exp + NS);             // [NS][kMaxWarps]
+    int *done = reinterpret_cast<int *>(red + NS * kMaxWarps);         // warps done with the last round
 
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
@@ -319,6 +320,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     }
     __syncwarp();
 
+    // round-0 partials start at zero (warps that touch no unit of a row group
+    // leave 0); the counter picks the warp that combines the last round
+    for (int i = tid; i < kR * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
+    if (tid == 0) *done = 0;
+
     // Everything above touched only the weights, which no kernel writes; x
     // (and y) may be written (read) by the kernel before this one in the
     // stream, so wait for it here (programmatic dependent launch), and let
@@ -331,6 +337,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int nthr = blockDim.x;
     const int n_batch = (p.k_pad + kXB * nthr - 1) / (kXB * nthr);
     float xr[NS][kXB];
+    int texp[NS];
+#pragma unroll
+    for (int t = 0; t < NS; ++t) texp[t] = 0;
     auto load_batch = [&](int bt) {
 #pragma unroll
         for (int t = 0; t < NS; ++t)
@@ -359,22 +368,22 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             if (lane == 0) red[t * kMaxWarps + warp] = mt;
         }
         __syncthreads();
-        if (tid < NS) {
+        // every thread folds the per-warp maxima itself (broadcast reads)
+#pragma unroll
+        for (int t = 0; t < NS; ++t) {
             float mt = 0.f;
-            for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[tid * kMaxWarps + w]);
+            for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[t * kMaxWarps + w]);
             // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
-            tok_exp[tid] = mt > 0.f ? -23 - ilogbf(mt) : 0;
+            texp[t] = mt > 0.f ? -23 - ilogbf(mt) : 0;
         }
-        __syncthreads();
-    } else if (tid < NS) {
-        tok_exp[tid] = 0;      // read only after the final __syncthreads
     }
+    if (tid < NS) tok_exp[tid] = tid == 0 ? texp[0] : texp[NS - 1];   // read only after later barriers
     for (int bt = 0; bt < n_batch; ++bt) {
         if (FMT == B200Q_F32 || n_batch > 1) load_batch(bt);
 #pragma unroll
         for (int t = 0; t < NS; ++t) {
             // 2^(T + 23) = 2^-ilogb(max|x|), a normal f32 unless max|x| is subnormal
-            const float tscale = FMT == B200Q_F32 ? 1.f : ldexpf(1.0f, tok_exp[t] + 23);
+            const float tscale = FMT == B200Q_F32 ? 1.f : ldexpf(1.0f, texp[t] + 23);
 #pragma unroll
             for (int j = 0; j < kXB; ++j) {
                 const int k = (bt * kXB + j) * nthr + tid;
@@ -433,9 +442,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     for (int base = rg0; base < rg1 && ok; base += kR) {
         const int rend = base + kR < rg1 ? base + kR : rg1;
-        // zero this round's partials (warps that touch no unit of a row group leave 0)
-        for (int i = tid; i < kR * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
-        __syncthreads();
+        const bool last_round = rend >= rg1;
+        if (base != rg0) {
+            // zero this round's partials (round 0 was zeroed in the prologue)
+            for (int i = tid; i < kR * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
+            __syncthreads();
+        }
         run_of(cc, base);
         int cur_rgl = -1;
         for (; cc.u < cc.u_end; ++cc.u) {
@@ -499,11 +511,25 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             }
         }
         if (cur_rgl >= 0) flush(cur_rgl);
-        __syncthreads();
-        // combine this round: warps in order, unscale, apply the row scale
+        // combine this round: warps in order, unscale, apply the row scale.
+        // The last round is combined by whichever warp finishes last (no
+        // block barrier); earlier rounds by the whole block between barriers.
+        int c_first = tid, c_step = blockDim.x;
+        if (last_round) {
+            __threadfence_block();
+            int prev = 0;
+            if (lane == 0) prev = atomicAdd(done, 1);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev != nw - 1) break;               // not the last warp: done
+            __threadfence_block();
+            c_first = lane;
+            c_step = 32;
+        } else {
+            __syncthreads();
+        }
         const int rows = (rend - base) * 8;
         for (int t = 0; t < NS; ++t) {
-            for (int r = tid; r < rows; r += blockDim.x) {
+            for (int r = c_first; r < rows; r += c_step) {
                 const int rgl = r >> 3, rr = r & 7;
                 float sum = 0.f;
                 for (int w = 0; w < nw; ++w) sum += part[(((size_t)rgl * nw + w) * NS + t) * 8 + rr];
@@ -518,7 +544,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 }
             }
         }
-        __syncthreads();   // part is reused by the next round
+        if (!last_round) __syncthreads();   // part is reused by the next round
     }
     if (!ok) {
         // give up: record the timeout and let this warp's copies land first
@@ -546,7 +572,7 @@ cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int
     const size_t stage = (size_t)kStage + 8;                 // ring stage + its mbarrier
     const int rg_cta = (p.n_rg + grid - 1) / grid;
     auto fixed_for = [&](int nw, int rr) {
-        return (size_t)4 * NS * k_alloc + (size_t)rr * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4;
+        return (size_t)4 * NS * k_alloc + (size_t)rr * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4 + 16;
     };
     // warps and depth first (round of kRound), then grow the round to all of
     // the CTA's row groups if the partials still fit (one round: no barrier)
