@@ -160,6 +160,36 @@ int b200q_matmul_host(const b200q_tensor *t, const float *x_host, float *y_host,
                       void *stream);
 
 /*
+ * Tensor-core matmul that allocates nothing.  The pages have no counterpart
+ * of this call; it exists for callers that cannot allocate device memory
+ * while they run: their device memory is owned by another allocator (a
+ * framework's caching allocator or a pool that reserved the device), or they
+ * are latency-critical loops that must not wait on an allocator call, which
+ * may synchronize the device or fail.
+ *
+ * Same operation, arguments, numerics and tensor-core path as
+ * b200q_matmul_ex(t, x, y, S, B200Q_PATH_TC, stream) for int8 and int4
+ * tensors, but the bf16 copy of x is kept in a fixed device array of
+ * b200q_tc_noalloc_capacity() bytes (24 MiB) that the library defines at file
+ * scope: every GPU that loads the library holds it until the process exits.
+ * A call needs S * padded_I * 2 bytes of it (padded_I = I rounded up to the
+ * device row length, a multiple of 256 for int4 and 128 for int8) and returns
+ * B200Q_EINVAL with a clear message when that exceeds the capacity.  It calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * All calls on a device share the array, which keeps the last call's
+ * contents; calls whose work overlaps in time on the GPU (for instance on two
+ * streams without ordering between them) race on it and must be serialized by
+ * the caller.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.
+ */
+int b200q_matmul_tc_noalloc(const b200q_tensor *t, const float *x, float *y, int S, void *stream);
+
+/* Bytes of the fixed workspace behind b200q_matmul_tc_noalloc. */
+long long b200q_tc_noalloc_capacity(void);
+
+/*
  * Describe a tensor.  Any out pointer may be NULL.  device_bytes is the size of
  * the resident copy (codes with row padding plus scales).
  */

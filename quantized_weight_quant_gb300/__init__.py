@@ -57,6 +57,10 @@ def _load():
     L.b200q_tensor_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci),
                                     ctypes.POINTER(ci), ctypes.POINTER(cll)]
     L.b200q_tensor_info.restype = ci
+    L.b200q_matmul_tc_noalloc.argtypes = [vp, vp, vp, ci, vp]
+    L.b200q_matmul_tc_noalloc.restype = ci
+    L.b200q_tc_noalloc_capacity.argtypes = []
+    L.b200q_tc_noalloc_capacity.restype = cll
     L.b200q_device_status.argtypes = []
     L.b200q_device_status.restype = ci
     L.b200q_kernel_launches.argtypes = []
@@ -197,6 +201,16 @@ def matmul_path(t, S: int) -> int:
 def matmul_gate_up(tg, tu, x, yg, yu, S: int, stream=None) -> None:
     _check(lib.b200q_matmul_gate_up(_h(tg), _h(tu), _dptr(x), _dptr(yg), _dptr(yu), S,
                                     _stream(stream)))
+
+
+def matmul_tc_noalloc(t, x, y, S: int, stream=None) -> None:
+    """Tensor-core matmul with no allocation: the bf16 copy of x lives in a
+    fixed per-device array (see b200q_matmul_tc_noalloc in include/b200q.h)."""
+    _check(lib.b200q_matmul_tc_noalloc(_h(t), _dptr(x), _dptr(y), S, _stream(stream)))
+
+
+def tc_noalloc_capacity() -> int:
+    return int(lib.b200q_tc_noalloc_capacity())
 
 
 def silu_mul(g, u, h, n: int, stream=None) -> None:

@@ -22,6 +22,8 @@ cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, flo
 cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu,
                               int S, cudaStream_t st, bool *handled);
 cudaError_t decode_take_error(unsigned int *code);
+size_t noalloc_capacity();
+cudaError_t launch_prefill_tc_noalloc(const Tensor &t, const float *x, float *y, int S, cudaStream_t st);
 cudaError_t prefill_take_error(unsigned int *code);
 
 namespace {
@@ -313,6 +315,29 @@ int b200q_matmul_gate_up(const b200q_tensor *hg, const b200q_tensor *hu, const f
         return fail(B200Q_EINVAL, "b200q_matmul_gate_up: yg and yu overlap");
     return run_matmul(tg, &tu, x, yg, yu, S, B200Q_PATH_AUTO, (cudaStream_t)stream, "b200q_matmul_gate_up");
 }
+
+int b200q_matmul_tc_noalloc(const b200q_tensor *h, const float *x, float *y, int S, void *stream) {
+    int rc = check_tensor(h, "b200q_matmul_tc_noalloc");
+    if (rc) return rc;
+    const Tensor &t = *reinterpret_cast<const Tensor *>(h);
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
+        return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: takes int8 and int4 tensors only");
+    if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: S must be >= 0 (got %d)", S);
+    if (S == 0) return B200Q_OK;
+    const size_t need = (size_t)S * (size_t)t.k_pad * 2;
+    if (need > noalloc_capacity())
+        return fail(B200Q_EINVAL,
+                    "b200q_matmul_tc_noalloc: S=%d x %lld padded columns needs %zu bytes of workspace, more than "
+                    "the fixed %zu bytes (use b200q_matmul or a smaller S)",
+                    S, t.k_pad, need, noalloc_capacity());
+    rc = check_io(t, x, y, S, "b200q_matmul_tc_noalloc");
+    if (rc) return rc;
+    cudaError_t e = launch_prefill_tc_noalloc(t, x, y, S, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_matmul_tc_noalloc");
+    return B200Q_OK;
+}
+
+long long b200q_tc_noalloc_capacity(void) { return (long long)noalloc_capacity(); }
 
 int b200q_silu_mul(const float *g, const float *u, float *h, long n, void *stream) {
     if (n < 0) return fail(B200Q_EINVAL, "b200q_silu_mul: n must be >= 0");

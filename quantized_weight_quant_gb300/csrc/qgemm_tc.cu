@@ -501,6 +501,67 @@ cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x,
     return e;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the tensor-core path (b200q_matmul_tc_noalloc).
+//
+// Some callers cannot allocate device memory while they run: their device
+// memory is owned by another allocator (a framework's caching allocator or a
+// pool that reserved the device), or they are latency-critical loops that
+// must not wait on an allocator call that may synchronize or fail.  For them
+// the bf16 copy of x lives in a fixed file-scope device array instead of a
+// per-call workspace.  Every GPU that loads the library holds the array until
+// the process exits.  All calls on a device share it and it keeps the last
+// call's contents (the conversion kernel overwrites every element a call
+// reads, so nothing needs clearing); calls that overlap in time on the GPU
+// race on it.
+constexpr size_t kNoAllocBytes = 24u << 20;   // 24 MiB: S * k_pad bf16 values
+static __device__ __align__(256) uint8_t g_noalloc_ws[kNoAllocBytes];
+
+namespace {
+void *g_noalloc_ptr[64] = {};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+size_t noalloc_capacity() { return kNoAllocBytes; }
+
+// Device address of the array on the current device.  Resolved once per
+// device (with that device current) by the first call made on it.
+cudaError_t noalloc_workspace(int dev, void **out) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+// x -> bf16 into the caller-independent array, then the same GEMM kernel as
+// the tensor-core path.  The caller has checked fmt and that
+// S * k_pad * 2 <= kNoAllocBytes.
+cudaError_t launch_prefill_tc_noalloc(const Tensor &t, const float *x, float *y, int S, cudaStream_t st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    void *ws = nullptr;
+    e = noalloc_workspace(dev, &ws);
+    if (e != cudaSuccess) return e;
+    const long long groups = (long long)S * t.k_pad / 8;
+    long long blocks = (groups + 255) / 256;
+    if (blocks > (long long)g_sms * 16) blocks = (long long)g_sms * 16;
+    x_to_bf16_kernel<<<(int)blocks, 256, 0, st>>>(x, (__nv_bfloat16 *)ws, S, t.I, (int)t.k_pad,
+                                                   t.fmt == B200Q_I4 ? 1 : 0);
+    count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return t.fmt == B200Q_I4 ? run_gemm<B200Q_I4>(t, (__nv_bfloat16 *)ws, y, S, st)
+                             : run_gemm<B200Q_I8>(t, (__nv_bfloat16 *)ws, y, S, st);
+}
+
 cudaError_t prefill_take_error(unsigned int *code) {
     unsigned int zero = 0;
     cudaError_t e = cudaMemcpyFromSymbol(code, g_prefill_err, sizeof(unsigned int));
