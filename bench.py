@@ -161,13 +161,17 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- distributed
 
 def dist_init(n_gpus):
+    """One process per GPU (torchrun env); NCCL when GPUs are present, gloo
+    otherwise.  The workload is replicated: no data crosses ranks, only the
+    barrier and the max of the timings."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return rank, world, local
 
@@ -179,13 +183,20 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """Max of a host float over all ranks (NCCL on GPUs, gloo on the CPU)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, steps, world, ms_max):
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return bytes_per_rank_step * steps * world / (ms_max * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -367,8 +378,7 @@ def run_ours(args):
         ms_eager, _ = time_steps(wl, args.steps, args.warmup, stream, world, graph=False)
     clocks = clk.summary()
     ms_max = max_over_ranks(ms, world)
-    total_bytes = wl.bytes_per_step * args.steps * world
-    value = total_bytes / (ms_max * 1e-3) / 1e9
+    value = job_throughput(wl.bytes_per_step, args.steps, world, ms_max)
     per_launch_ms = ms / max(1, launches)
     achieved = per_copy / (per_launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic("decode_i4_12288x6144_s1")
