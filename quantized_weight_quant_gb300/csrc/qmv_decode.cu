@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     struct Cursor {
         int round_base, round_end;   // row groups of the current round
         int u, u_end;                // unit index within the round's run
+        int rgl, sg;                 // u = rgl * nseg + sg
     };
     auto run_of = [&](Cursor &c, int base) {
         c.round_base = base;
@@ -278,6 +279,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const int U = (c.round_end - c.round_base) * nseg;
         c.u = (int)((long long)warp * U / nw);
         c.u_end = (int)((long long)(warp + 1) * U / nw);
+        c.rgl = c.u / nseg;
+        c.sg = c.u - c.rgl * nseg;
+    };
+    auto advance = [&](Cursor &c) {
+        ++c.u;
+        if (++c.sg == nseg) {
+            c.sg = 0;
+            ++c.rgl;
+        }
     };
     auto normalize = [&](Cursor &c) {  // skip empty runs; false when past the last round
         while (c.u >= c.u_end) {
@@ -298,14 +308,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     long long issued = 0;
     auto issue_next = [&]() -> bool {  // lane 0: copy the next unit into the next stage
         if (!normalize(pc)) return false;
-        const int rgl = pc.u / nseg, sg = pc.u - rgl * nseg;
+        const int rgl = pc.rgl, sg = pc.sg;
         const int rg = pc.round_base + rgl;
         const int set = rg >= p.rg_per_set;
         const uint32_t bar = my_bars + 8 * p_stage;
         mbar_expect_tx(bar, (uint32_t)(8 * rb));
         tma_load_2d(smem_u32(my_ring + (size_t)p_stage * kStage), set ? &map1 : &map0, sg * (kSeg / 4),
                     (rg - set * p.rg_per_set) * 8, bar, policy);
-        ++pc.u;
+        advance(pc);
         ++issued;
         if (++p_stage == depth) p_stage = 0;
         return true;
@@ -378,31 +388,54 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         }
     }
     if (tid < NS) tok_exp[tid] = tid == 0 ? texp[0] : texp[NS - 1];   // read only after later barriers
-    for (int bt = 0; bt < n_batch; ++bt) {
-        if (FMT == B200Q_F32 || n_batch > 1) load_batch(bt);
+    if constexpr (FMT == B200Q_F32) {
+        for (int bt = 0; bt < n_batch; ++bt) {
+            load_batch(bt);
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int j = 0; j < kXB; ++j) {
+                    const int k = (bt * kXB + j) * nthr + tid;
+                    if (k < p.k_pad) xs[t * k_alloc + k] = xr[t][j];
+                }
+        }
+    } else {
+        // Destination order: 16-byte slot d of the lane-interleaved layout
+        // [seg][word q][quad e4][lane][4] holds elements (e4*4 .. e4*4+3) of
+        // word q of chunk c = seg * 32 + lane, which are 4 consecutive
+        // elements of x.  So staging is a permutation of 16-byte groups plus
+        // two exact power-of-two products per element:
+        //     x' = (x * 2^(T + 23)) * 2^(126 - b),  b = the code's bit offset.
+        constexpr int Q4 = EW / 4;                    // quads per word
+        const int n_chunks = p.ld / 16;
+        const int n_slots = nseg * 4 * Q4 * 32;
+        const bool vec = (p.x_ld & 3) == 0;
 #pragma unroll
         for (int t = 0; t < NS; ++t) {
-            // 2^(T + 23) = 2^-ilogb(max|x|), a normal f32 unless max|x| is subnormal
-            const float tscale = FMT == B200Q_F32 ? 1.f : ldexpf(1.0f, texp[t] + 23);
-#pragma unroll
-            for (int j = 0; j < kXB; ++j) {
-                const int k = (bt * kXB + j) * nthr + tid;
-                if (k < p.k_pad) {
-                    const float v = xr[t][j];
-                    if (FMT == B200Q_F32) {
-                        xs[t * k_alloc + k] = v;
-                    } else {
-                        // lane-interleaved: element k of chunk c (lane c % 32 of segment
-                        // c / 32) goes next to the other lanes' reads: [seg][word][quad][lane][4]
-                        const int c = k / E, ec = k - c * E;
-                        const int lane_c = c & 31, seg_c = c >> 5;
-                        const int q = ec / EW, e = ec - q * EW;
-                        const int pos = (((seg_c * 4 + q) * (EW / 4) + (e >> 2)) * 32 + lane_c) * 4 + (e & 3);
-                        // v * 2^(T + 149 - b) = (v * 2^(T + 23)) * 2^(126 - b): both factors are
-                        // normal powers of two for any finite x, so both products are exact
-                        xs[t * k_alloc + pos] = (v * tscale) * __int_as_float((253 - bit_offset<FMT>(e)) << 23);
-                    }
+            const float tscale = ldexpf(1.0f, texp[t] + 23);
+            const float *xr_t = p.x + (long long)t * p.x_ld;
+            float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * k_alloc);
+            for (int d = tid; d < n_slots; d += nthr) {
+                const int ln = d & 31, rest = d >> 5;
+                const int e4 = rest % Q4, q = (rest / Q4) & 3, seg = (rest / Q4) >> 2;
+                const int c = seg * 32 + ln;
+                if (c >= n_chunks) continue;          // past the row: never read
+                const int k0 = c * E + q * EW + e4 * 4;
+                float4 v;
+                if (vec && k0 + 3 < p.I) {
+                    v = *reinterpret_cast<const float4 *>(xr_t + k0);
+                } else {
+                    v.x = k0 < p.I ? xr_t[k0] : 0.f;
+                    v.y = k0 + 1 < p.I ? xr_t[k0 + 1] : 0.f;
+                    v.z = k0 + 2 < p.I ? xr_t[k0 + 2] : 0.f;
+                    v.w = k0 + 3 < p.I ? xr_t[k0 + 3] : 0.f;
                 }
+                const int e0 = e4 * 4;
+                v.x = (v.x * tscale) * __int_as_float((253 - bit_offset<FMT>(e0)) << 23);
+                v.y = (v.y * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 1)) << 23);
+                v.z = (v.z * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 2)) << 23);
+                v.w = (v.w * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 3)) << 23);
+                dst[d] = v;
             }
         }
     }
@@ -450,13 +483,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         }
         run_of(cc, base);
         int cur_rgl = -1;
-        for (; cc.u < cc.u_end; ++cc.u) {
+        for (; cc.u < cc.u_end; advance(cc)) {
             if (lane == 0) issue_next();
             if (!mbar_wait(my_bars + 8 * c_stage, c_phase, kWaitNs)) {
                 ok = false;
                 break;
             }
-            const int rgl = cc.u / nseg, sg = cc.u - rgl * nseg;
+            const int rgl = cc.rgl, sg = cc.sg;
             if (rgl != cur_rgl) {
                 if (cur_rgl >= 0) flush(cur_rgl);
                 cur_rgl = rgl;
