@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [NS] T
     float *red = reinterpret_cast<float *>(tok_exp + NS);             // [NS][kMaxWarps]
     int *done = reinterpret_cast<int *>(red + NS * kMaxWarps);         // warps done with the last round
+    float *row_scale = reinterpret_cast<float *>(done + 4);           // [rows of this CTA]
 
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
@@ -321,14 +322,33 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         return true;
     };
 
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map0)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map1)) : "memory");
+    }
     if (lane == 0) {
         for (int b = 0; b < depth; ++b) mbar_init(my_bars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         policy = evict_first_policy();
-        for (int i = 0; i < depth - 1; ++i)
-            if (!issue_next()) break;
+        issue_next();           // one unit per warp before x: x's loads must not queue behind more
     }
     __syncwarp();
+
+    // the row scales are read-only too: start loading this CTA's now (kept
+    // in registers, written to shared memory once x is staged)
+    constexpr int kSc = 4;
+    float sc_reg[kSc];
+#pragma unroll
+    for (int i = 0; i < kSc; ++i) {
+        const int r = i * blockDim.x + tid;
+        sc_reg[i] = 0.f;
+        if (r < (rg1 - rg0) * 8) {
+            const int rg = rg0 + (r >> 3);
+            const int set = rg >= p.rg_per_set;
+            const int o = (rg - set * p.rg_per_set) * 8 + (r & 7);
+            if (o < p.O) sc_reg[i] = (set ? p.scales[1] : p.scales[0])[o];
+        }
+    }
 
     // round-0 partials start at zero (warps that touch no unit of a row group
     // leave 0); the counter picks the warp that combines the last round
@@ -342,33 +362,85 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // ---- stage x: x'[t][k] = x[t][k] * 2^(T_t + 149 - b(k)), with every
-    // thread's loads in flight at once (one round trip when k_pad <= kXB * threads)
+    // ---- stage x.  Quantized formats: 16-byte slot d of the lane-interleaved
+    // layout [seg][word q][quad e4][lane][4] holds elements (e4*4 .. e4*4+3) of
+    // word q of chunk c = seg * 32 + lane, 4 consecutive elements of x, so each
+    // thread gathers its slots' 16-byte groups of x into registers (one round
+    // trip), the per-token max of |x| comes from them, and they are stored as
+    //     x' = (x * 2^(T + 23)) * 2^(126 - b),  b = the code's bit offset,
+    // two exact power-of-two products per element.  f32 weights: x as is.
     const int nthr = blockDim.x;
-    const int n_batch = (p.k_pad + kXB * nthr - 1) / (kXB * nthr);
-    float xr[NS][kXB];
     int texp[NS];
 #pragma unroll
     for (int t = 0; t < NS; ++t) texp[t] = 0;
-    auto load_batch = [&](int bt) {
-#pragma unroll
-        for (int t = 0; t < NS; ++t)
-#pragma unroll
-            for (int j = 0; j < kXB; ++j) {
-                const int k = (bt * kXB + j) * nthr + tid;
-                xr[t][j] = k < p.I ? p.x[(long long)t * p.x_ld + k] : 0.f;
-            }
-    };
-    if (FMT != B200Q_F32) {
-        float m[NS];
-#pragma unroll
-        for (int t = 0; t < NS; ++t) m[t] = 0.f;
-        for (int bt = 0; bt < n_batch; ++bt) {
-            load_batch(bt);
+    if constexpr (FMT == B200Q_F32) {
+        for (int base = 0; base < p.k_pad; base += kXB * nthr) {
+            float v[NS][kXB];                         // all loads of a batch in flight at once
 #pragma unroll
             for (int t = 0; t < NS; ++t)
 #pragma unroll
-                for (int j = 0; j < kXB; ++j) m[t] = fmaxf(m[t], fabsf(xr[t][j]));
+                for (int j = 0; j < kXB; ++j) {
+                    const int k = base + j * nthr + tid;
+                    v[t][j] = k < p.I ? p.x[(long long)t * p.x_ld + k] : 0.f;
+                }
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int j = 0; j < kXB; ++j) {
+                    const int k = base + j * nthr + tid;
+                    if (k < p.k_pad) xs[t * k_alloc + k] = v[t][j];
+                }
+        }
+    } else {
+        constexpr int Q4 = EW / 4;                    // quads per word
+        const int n_chunks = p.ld / 16;
+        const int n_slots = nseg * 4 * Q4 * 32;
+        const bool vec = (p.x_ld & 3) == 0;
+        auto slot_src = [&](int d) {                  // first x element of slot d, or -1 past the row
+            const int ln = d & 31, rest = d >> 5;
+            const int e4 = rest % Q4, q = (rest / Q4) & 3, seg = (rest / Q4) >> 2;
+            const int c = seg * 32 + ln;
+            return c < n_chunks ? c * E + q * EW + e4 * 4 : -1;
+        };
+        auto gather = [&](int t, int k0) {
+            const float *xr_t = p.x + (long long)t * p.x_ld;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k0 < 0) return v;
+            if (vec && k0 + 3 < p.I) return *reinterpret_cast<const float4 *>(xr_t + k0);
+            v.x = k0 < p.I ? xr_t[k0] : 0.f;
+            v.y = k0 + 1 < p.I ? xr_t[k0 + 1] : 0.f;
+            v.z = k0 + 2 < p.I ? xr_t[k0 + 2] : 0.f;
+            v.w = k0 + 3 < p.I ? xr_t[k0 + 3] : 0.f;
+            return v;
+        };
+        auto put = [&](int t, int d, float4 v, float tscale) {
+            const int e0 = ((d >> 5) % Q4) * 4;
+            v.x = (v.x * tscale) * __int_as_float((253 - bit_offset<FMT>(e0)) << 23);
+            v.y = (v.y * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 1)) << 23);
+            v.z = (v.z * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 2)) << 23);
+            v.w = (v.w * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 3)) << 23);
+            reinterpret_cast<float4 *>(xs + (size_t)t * k_alloc)[d] = v;
+        };
+        constexpr int kG = kXB / 4;                   // slots per thread held in registers
+        const bool one_pass = n_slots <= kG * nthr;
+        float4 held[NS][kG];
+        float m[NS];
+#pragma unroll
+        for (int t = 0; t < NS; ++t) m[t] = 0.f;
+        for (int base = 0; base < n_slots; base += kG * nthr) {
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int j = 0; j < kG; ++j) {
+                    const int d = base + j * nthr + tid;
+                    held[t][j] = d < n_slots ? gather(t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int j = 0; j < kG; ++j)
+                    m[t] = fmaxf(m[t], fmaxf(fmaxf(fabsf(held[t][j].x), fabsf(held[t][j].y)),
+                                             fmaxf(fabsf(held[t][j].z), fabsf(held[t][j].w))));
         }
 #pragma unroll
         for (int t = 0; t < NS; ++t) {
@@ -378,7 +450,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             if (lane == 0) red[t * kMaxWarps + warp] = mt;
         }
         __syncthreads();
-        // every thread folds the per-warp maxima itself (broadcast reads)
 #pragma unroll
         for (int t = 0; t < NS; ++t) {
             float mt = 0.f;
@@ -386,60 +457,35 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
             texp[t] = mt > 0.f ? -23 - ilogbf(mt) : 0;
         }
-    }
-    if (tid < NS) tok_exp[tid] = tid == 0 ? texp[0] : texp[NS - 1];   // read only after later barriers
-    if constexpr (FMT == B200Q_F32) {
-        for (int bt = 0; bt < n_batch; ++bt) {
-            load_batch(bt);
-#pragma unroll
-            for (int t = 0; t < NS; ++t)
-#pragma unroll
-                for (int j = 0; j < kXB; ++j) {
-                    const int k = (bt * kXB + j) * nthr + tid;
-                    if (k < p.k_pad) xs[t * k_alloc + k] = xr[t][j];
-                }
-        }
-    } else {
-        // Destination order: 16-byte slot d of the lane-interleaved layout
-        // [seg][word q][quad e4][lane][4] holds elements (e4*4 .. e4*4+3) of
-        // word q of chunk c = seg * 32 + lane, which are 4 consecutive
-        // elements of x.  So staging is a permutation of 16-byte groups plus
-        // two exact power-of-two products per element:
-        //     x' = (x * 2^(T + 23)) * 2^(126 - b),  b = the code's bit offset.
-        constexpr int Q4 = EW / 4;                    // quads per word
-        const int n_chunks = p.ld / 16;
-        const int n_slots = nseg * 4 * Q4 * 32;
-        const bool vec = (p.x_ld & 3) == 0;
 #pragma unroll
         for (int t = 0; t < NS; ++t) {
             const float tscale = ldexpf(1.0f, texp[t] + 23);
-            const float *xr_t = p.x + (long long)t * p.x_ld;
-            float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * k_alloc);
-            for (int d = tid; d < n_slots; d += nthr) {
-                const int ln = d & 31, rest = d >> 5;
-                const int e4 = rest % Q4, q = (rest / Q4) & 3, seg = (rest / Q4) >> 2;
-                const int c = seg * 32 + ln;
-                if (c >= n_chunks) continue;          // past the row: never read
-                const int k0 = c * E + q * EW + e4 * 4;
-                float4 v;
-                if (vec && k0 + 3 < p.I) {
-                    v = *reinterpret_cast<const float4 *>(xr_t + k0);
-                } else {
-                    v.x = k0 < p.I ? xr_t[k0] : 0.f;
-                    v.y = k0 + 1 < p.I ? xr_t[k0 + 1] : 0.f;
-                    v.z = k0 + 2 < p.I ? xr_t[k0 + 2] : 0.f;
-                    v.w = k0 + 3 < p.I ? xr_t[k0 + 3] : 0.f;
+            if (one_pass) {
+#pragma unroll
+                for (int j = 0; j < kG; ++j) {
+                    const int d = j * nthr + tid;
+                    if (d < n_slots) put(t, d, held[t][j], tscale);
                 }
-                const int e0 = e4 * 4;
-                v.x = (v.x * tscale) * __int_as_float((253 - bit_offset<FMT>(e0)) << 23);
-                v.y = (v.y * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 1)) << 23);
-                v.z = (v.z * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 2)) << 23);
-                v.w = (v.w * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 3)) << 23);
-                dst[d] = v;
+            } else {
+                for (int d = tid; d < n_slots; d += nthr) put(t, d, gather(t, slot_src(d)), tscale);
             }
         }
     }
+    if (tid < NS) tok_exp[tid] = tid == 0 ? texp[0] : texp[NS - 1];   // read only after later barriers
+#pragma unroll
+    for (int i = 0; i < kSc; ++i)
+        if (i * blockDim.x + tid < (rg1 - rg0) * 8) row_scale[i * blockDim.x + tid] = sc_reg[i];
+    for (int r = kSc * blockDim.x + tid; r < (rg1 - rg0) * 8; r += blockDim.x) {   // very tall CTAs
+        const int rg = rg0 + (r >> 3);
+        const int set = rg >= p.rg_per_set;
+        const int o = (rg - set * p.rg_per_set) * 8 + (r & 7);
+        row_scale[r] = o < p.O ? (set ? p.scales[1] : p.scales[0])[o] : 0.f;
+    }
     __syncthreads();
+
+    if (lane == 0)
+        for (int i = 1; i < depth - 1; ++i)
+            if (!issue_next()) break;
 
     // ---- main loop
     Cursor cc;
@@ -571,9 +617,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 const int o = (rg - set * p.rg_per_set) * 8 + rr;
                 if (o < p.O) {
                     float *yb = set ? p.y[1] : p.y[0];
-                    const float *sb = set ? p.scales[1] : p.scales[0];
                     const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[t]);
-                    yb[(long long)t * p.y_ld + o] = dot * sb[o];
+                    yb[(long long)t * p.y_ld + o] = dot * row_scale[(rg - rg0) * 8 + rr];
                 }
             }
         }
@@ -605,7 +650,8 @@ cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int
     const size_t stage = (size_t)kStage + 8;                 // ring stage + its mbarrier
     const int rg_cta = (p.n_rg + grid - 1) / grid;
     auto fixed_for = [&](int nw, int rr) {
-        return (size_t)4 * NS * k_alloc + (size_t)rr * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4 + 16;
+        return (size_t)4 * NS * k_alloc + (size_t)rr * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4 + 16 +
+               (size_t)rg_cta * 8 * 4;
     };
     // warps and depth first (round of kRound), then grow the round to all of
     // the CTA's row groups if the partials still fit (one round: no barrier)

@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/b200q.h"
+#include "b200q.h"
 
 namespace qwq {
 
