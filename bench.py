@@ -494,7 +494,9 @@ def run_single(args):
 def moe_measure(q, steps, warmup, stream):
     """MoE expert layer at S=1: 256 resident experts (int4 gate/up [2048,6144],
     down [6144,2048]); each step routes one token to 8 distinct experts
-    (pre-drawn seeded ids) and runs fused gate/up -> silu*up -> down for each."""
+    (pre-drawn seeded ids).  Two forms of the same layer: per expert (fused
+    gate/up -> silu*up -> down, 24 launches) and grouped (the 16 gate/up
+    tensors in one call, the 8 down tensors on silu(g)*u in a second)."""
     import torch
     import synth
     D, F, E, K = 6144, 2048, 256, 8
@@ -520,9 +522,17 @@ def moe_measure(q, steps, warmup, stream):
             q.silu_mul(yg[k], yu[k], h[k], F, stream)
             q.matmul(downs[e], h[k], y[k], 1, stream)
 
+    def step_grouped(r):
+        sel = [int(e) for e in ids[r]]
+        q.matmul_grouped([t for e in sel for t in (gates[e], ups[e])], [x] * (2 * K),
+                         [v for k in range(K) for v in (yg[k], yu[k])], 1, stream)
+        q.matmul_grouped_silu([downs[e] for e in sel], [yg[k] for k in range(K)], [yu[k] for k in range(K)],
+                              [y[k] for k in range(K)], 1, stream)
+
     with torch.cuda.stream(stream):
         for r in range(warmup):
             step(r)
+            step_grouped(r)
     torch.cuda.synchronize()
 
     def timed(fn):
@@ -545,17 +555,34 @@ def moe_measure(q, steps, warmup, stream):
         g.replay()
     torch.cuda.synchronize()
     ms_graph = timed(g.replay)
+    ms_grp = timed(lambda: [step_grouped(warmup + r) for r in range(steps)])
+    gg = torch.cuda.CUDAGraph()
+    n0 = q.kernel_launches()
+    with torch.cuda.graph(gg, stream=stream):
+        for r in range(steps):
+            step_grouped(warmup + r)
+    grp_launches = (q.kernel_launches() - n0) / steps
+    with torch.cuda.stream(stream):
+        gg.replay()
+    torch.cuda.synchronize()
+    ms_grp_graph = timed(gg.replay)
     layer_bytes = K * (2 * algorithmic_bytes(4, F, D, 1) - 4 * D + algorithmic_bytes(4, D, F, 1) + 4 * 2 * F)
     for lst in (gates, ups, downs):
         for t in lst:
             t.free()
     hbm = peaks()["hbm_gbs"]
-    return {"workload": "MoE expert layer S=1, 8 of 256 experts (gate_up, silu*up, down per expert)",
-            "graph": {"us_per_layer": round(ms_graph * 1e3, 2), "layer_tokens_per_s": round(1e3 / ms_graph, 1),
-                      "GB/s": round(layer_bytes / (ms_graph * 1e-3) / 1e9, 1),
-                      "frac_hbm": round(layer_bytes / (ms_graph * 1e-3) / 1e9 / hbm, 4)},
-            "plain_launches": {"us_per_layer": round(ms * 1e3, 2), "layer_tokens_per_s": round(1e3 / ms, 1),
-                               "GB/s": round(layer_bytes / (ms * 1e-3) / 1e9, 1)},
+    def rate(ms_):
+        return {"us_per_layer": round(ms_ * 1e3, 2), "layer_tokens_per_s": round(1e3 / ms_, 1),
+                "GB/s": round(layer_bytes / (ms_ * 1e-3) / 1e9, 1),
+                "frac_hbm": round(layer_bytes / (ms_ * 1e-3) / 1e9 / hbm, 4)}
+
+    return {"workload": "MoE expert layer S=1, 8 of 256 experts",
+            "grouped_graph": dict(rate(ms_grp_graph), launches_per_layer=grp_launches,
+                                  form="matmul_grouped (16 gate/up tensors, one x) + matmul_grouped_silu "
+                                       "(8 down tensors on silu(g)*u)"),
+            "grouped_plain": rate(ms_grp),
+            "per_expert_graph": rate(ms_graph),
+            "per_expert_plain": rate(ms),
             "bytes_per_layer": layer_bytes}
 
 
@@ -601,7 +628,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill"])
+    ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill", "moe"])
     ap.add_argument("--fmt", default="i4", choices=["f32", "i8", "i4", "i2"])
     ap.add_argument("--O", type=int, default=12288)
     ap.add_argument("--I", type=int, default=6144)
@@ -616,6 +643,11 @@ def main():
         run_sweep(args)
     elif args.workload in ("decode", "prefill"):
         run_single(args)
+    elif args.workload == "moe":
+        import torch
+        import quantized_weight_quant_gb300 as q
+        torch.cuda.set_device(0)
+        print(json.dumps(moe_measure(q, args.steps, args.warmup, torch.cuda.Stream())), flush=True)
     else:
         run_ours(args)
 

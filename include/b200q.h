@@ -137,6 +137,53 @@ int b200q_tc_min_s(void);
 int b200q_matmul_gate_up(const b200q_tensor *tg, const b200q_tensor *tu, const float *x,
                          float *yg, float *yu, int S, void *stream);
 
+/* Most tensors one grouped call takes. */
+enum { B200Q_GROUP_MAX = 16 };
+
+/*
+ * Grouped matmul: ys[j] = matmul(ts[j], xs[j]) for j < n, in one kernel
+ * launch per pair of activation rows on the f32 path.  This is the decode step
+ * of a mixture-of-experts layer: the gate and up tensors of k routed experts
+ * (2k tensors on one x, the pairing of qmatmul_gate_up.comp in the
+ * three-backends chapter, section 四, widened to several experts) or their k
+ * down tensors (one input each).  The pages run one expert at a time ("The
+ * GPU-resident pipeline" section of the colibri CUDA docs keeps the expert
+ * loop and groups expert uploads at prefill); launching the experts of a
+ * layer together is this library's own step.
+ *
+ *   ts      HOST array of n tensor handles, 1 <= n <= B200Q_GROUP_MAX; all of
+ *           one format and one I, on the current device; O may differ
+ *   xs      HOST array of n DEVICE pointers, xs[j] = [S, I] f32 as in
+ *           b200q_matmul; entries may repeat (consecutive sets with the same
+ *           x stage it once per block)
+ *   ys      HOST array of n DEVICE pointers, ys[j] = [S, O_j] f32, fully
+ *           overwritten; no ys[j] may overlap another ys[k] or any xs[k]
+ *   S       activation rows, >= 0 (0 is a no-op)
+ *
+ * The host arrays are read during the call only.  Same numerics and path rule
+ * as b200q_matmul: below b200q_tc_min_s() (or for f32 / int2 tensors) the
+ * whole group is one launch per two rows; from the threshold on, int8 / int4
+ * tensors run one tensor-core call each.  If the group's inputs do not fit
+ * the kernel's shared memory the tensors run one call each.  Returns
+ * B200Q_OK, B200Q_EINVAL or B200Q_ECUDA.
+ */
+int b200q_matmul_grouped(const b200q_tensor *const *ts, int n, const float *const *xs,
+                         float *const *ys, int S, void *stream);
+
+/*
+ * As b200q_matmul_grouped with the expert glue fused into the input:
+ * ys[j] = matmul(ts[j], silu(gs[j]) * us[j]), silu(z) = z / (1 + e^-z), the
+ * product taken elementwise over [S, I] (the down projection of k experts on
+ * their own gate and up outputs).  gs[j] and us[j] follow the rules of xs[j];
+ * the gated input is formed while it is staged and never written to memory
+ * on the f32 path.  From b200q_tc_min_s() rows on it is formed in a
+ * stream-ordered workspace of the library's pool and the tensors run one
+ * tensor-core call each.  The f32 path's bound is taken on the f32 value of
+ * silu(g) * u, which lies within a few ulp of the exact one.
+ */
+int b200q_matmul_grouped_silu(const b200q_tensor *const *ts, int n, const float *const *gs,
+                              const float *const *us, float *const *ys, int S, void *stream);
+
 /*
  * Expert glue: h[k] = silu(g[k]) * u[k], silu(z) = z / (1 + e^-z), for
  * k < n, f32, on `stream`.  g, u, h are DEVICE pointers to n floats, 16-byte

@@ -18,6 +18,7 @@ import numpy as np
 F32, I8, I4, I2 = 0, 1, 2, 3
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4
 PATH_AUTO, PATH_F32, PATH_TC = 0, 1, 2
+GROUP_MAX = 16
 FORMATS = {"f32": F32, "i8": I8, "i4": I4, "i2": I2}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +51,10 @@ def _load():
     L.b200q_tc_min_s.restype = ci
     L.b200q_matmul_gate_up.argtypes = [vp, vp, vp, vp, vp, ci, vp]
     L.b200q_matmul_gate_up.restype = ci
+    L.b200q_matmul_grouped.argtypes = [vp, ci, vp, vp, ci, vp]
+    L.b200q_matmul_grouped.restype = ci
+    L.b200q_matmul_grouped_silu.argtypes = [vp, ci, vp, vp, vp, ci, vp]
+    L.b200q_matmul_grouped_silu.restype = ci
     L.b200q_silu_mul.argtypes = [vp, vp, vp, cl, vp]
     L.b200q_silu_mul.restype = ci
     L.b200q_matmul_host.argtypes = [vp, vp, vp, ci, vp]
@@ -201,6 +206,33 @@ def matmul_path(t, S: int) -> int:
 def matmul_gate_up(tg, tu, x, yg, yu, S: int, stream=None) -> None:
     _check(lib.b200q_matmul_gate_up(_h(tg), _h(tu), _dptr(x), _dptr(yg), _dptr(yu), S,
                                     _stream(stream)))
+
+
+def _ptr_array(items, conv):
+    """A host array of pointers (kept alive by the caller's reference)."""
+    arr = (ctypes.c_void_p * max(len(items), 1))()
+    for j, a in enumerate(items):
+        arr[j] = conv(a) or None
+    return arr
+
+
+def matmul_grouped(ts, xs, ys, S: int, stream=None) -> None:
+    """ys[j] = matmul(ts[j], xs[j]) for every j, in one launch per two rows on
+    the f32 path (b200q_matmul_grouped).  ts, xs, ys: equal-length sequences."""
+    if not (len(ts) == len(xs) == len(ys)):
+        raise ValueError("ts, xs and ys must have the same length")
+    th, xh, yh = _ptr_array(ts, _h), _ptr_array(xs, _dptr), _ptr_array(ys, _dptr)
+    _check(lib.b200q_matmul_grouped(th, len(ts), xh, yh, S, _stream(stream)))
+
+
+def matmul_grouped_silu(ts, gs, us, ys, S: int, stream=None) -> None:
+    """ys[j] = matmul(ts[j], silu(gs[j]) * us[j]) for every j
+    (b200q_matmul_grouped_silu)."""
+    if not (len(ts) == len(gs) == len(us) == len(ys)):
+        raise ValueError("ts, gs, us and ys must have the same length")
+    th, gh, uh, yh = (_ptr_array(ts, _h), _ptr_array(gs, _dptr), _ptr_array(us, _dptr),
+                      _ptr_array(ys, _dptr))
+    _check(lib.b200q_matmul_grouped_silu(th, len(ts), gh, uh, yh, S, _stream(stream)))
 
 
 def matmul_tc_noalloc(t, x, y, S: int, stream=None) -> None:

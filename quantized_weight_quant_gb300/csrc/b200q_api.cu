@@ -25,6 +25,10 @@ cudaError_t decode_take_error(unsigned int *code);
 size_t noalloc_capacity();
 cudaError_t launch_prefill_tc_noalloc(const Tensor &t, const float *x, float *y, int S, cudaStream_t st);
 cudaError_t prefill_take_error(unsigned int *code);
+cudaError_t launch_decode_group(const Tensor *const *ts, int n, const float *const *xa, const float *const *xb,
+                                float *const *ys, bool silu, int S, cudaStream_t st, bool *handled);
+cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st);
+cudaError_t workspace_free(void *ptr, cudaStream_t st);
 
 namespace {
 
@@ -314,6 +318,92 @@ int b200q_matmul_gate_up(const b200q_tensor *hg, const b200q_tensor *hu, const f
     if (overlap(yg, (size_t)S * tg.O * 4, yu, (size_t)S * tu.O * 4))
         return fail(B200Q_EINVAL, "b200q_matmul_gate_up: yg and yu overlap");
     return run_matmul(tg, &tu, x, yg, yu, S, B200Q_PATH_AUTO, (cudaStream_t)stream, "b200q_matmul_gate_up");
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks of a grouped call; on success ts[] holds the tensors.
+int check_group(const b200q_tensor *const *hs, int n, const float *const *xa, const float *const *xb,
+                float *const *ys, int S, const Tensor **ts, const char *who) {
+    if (n < 1 || n > B200Q_GROUP_MAX)
+        return fail(B200Q_EINVAL, "%s: n must be in [1, %d] (got %d)", who, B200Q_GROUP_MAX, n);
+    if (!hs || !xa || !ys) return fail(B200Q_EINVAL, "%s: NULL host array", who);
+    if (S < 0) return fail(B200Q_EINVAL, "%s: S must be >= 0 (got %d)", who, S);
+    for (int j = 0; j < n; ++j) {
+        int rc = check_tensor(hs[j], who);
+        if (rc) return rc;
+        ts[j] = reinterpret_cast<const Tensor *>(hs[j]);
+        if (ts[j]->fmt != ts[0]->fmt || ts[j]->I != ts[0]->I)
+            return fail(B200Q_EINVAL, "%s: tensor %d differs from tensor 0 in format or I", who, j);
+    }
+    if (S == 0) return B200Q_OK;
+    const size_t xbytes = (size_t)S * ts[0]->I * 4;
+    for (int j = 0; j < n; ++j) {
+        const size_t yb = (size_t)S * ts[j]->O * 4;
+        if (!xa[j] || !ys[j] || (xb && !xb[j]))
+            return fail(B200Q_EINVAL, "%s: set %d: device pointers must not be NULL", who, j);
+        if (!aligned16(xa[j]) || !aligned16(ys[j]) || (xb && !aligned16(xb[j])))
+            return fail(B200Q_EINVAL, "%s: set %d: device pointers must be 16-byte aligned", who, j);
+        for (int k = 0; k < n; ++k) {
+            if (overlap(ys[j], yb, xa[k], xbytes) || (xb && overlap(ys[j], yb, xb[k], xbytes)))
+                return fail(B200Q_EINVAL, "%s: output %d overlaps input %d", who, j, k);
+            if (k != j && overlap(ys[j], yb, ys[k], (size_t)S * ts[k]->O * 4))
+                return fail(B200Q_EINVAL, "%s: outputs %d and %d overlap", who, j, k);
+        }
+    }
+    return B200Q_OK;
+}
+
+int run_group(const b200q_tensor *const *hs, int n, const float *const *xa, const float *const *xb,
+              float *const *ys, int S, cudaStream_t st, const char *who) {
+    const Tensor *ts[B200Q_GROUP_MAX];
+    int rc = check_group(hs, n, xa, xb, ys, S, ts, who);
+    if (rc || S == 0) return rc;
+    const bool silu = xb != nullptr;
+    if (select_path(*ts[0], S, B200Q_PATH_AUTO) == B200Q_PATH_F32) {
+        bool handled = false;
+        cudaError_t e = launch_decode_group(ts, n, xa, xb, ys, silu, S, st, &handled);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        if (handled) return B200Q_OK;
+    }
+    // one call per tensor; the gated inputs go through a workspace first
+    float *h = nullptr;
+    const size_t xn = (size_t)S * ts[0]->I;
+    if (silu) {
+        cudaError_t e = workspace_alloc((void **)&h, (size_t)n * xn * 4, st);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
+    for (int j = 0; j < n && rc == B200Q_OK; ++j) {
+        const float *x = xa[j];
+        if (silu) {
+            cudaError_t e = launch_silu_mul(xa[j], xb[j], h + j * xn, (long)xn, st);
+            if (e != cudaSuccess) rc = cuda_fail(e, who);
+            x = h + j * xn;
+        }
+        if (rc == B200Q_OK) rc = run_matmul(*ts[j], nullptr, x, ys[j], nullptr, S, B200Q_PATH_AUTO, st, who);
+    }
+    if (h) {
+        cudaError_t e = workspace_free(h, st);
+        if (rc == B200Q_OK && e != cudaSuccess) rc = cuda_fail(e, who);
+    }
+    return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int b200q_matmul_grouped(const b200q_tensor *const *ts, int n, const float *const *xs, float *const *ys, int S,
+                         void *stream) {
+    return run_group(ts, n, xs, nullptr, ys, S, (cudaStream_t)stream, "b200q_matmul_grouped");
+}
+
+int b200q_matmul_grouped_silu(const b200q_tensor *const *ts, int n, const float *const *gs,
+                              const float *const *us, float *const *ys, int S, void *stream) {
+    if (!us) return fail(B200Q_EINVAL, "b200q_matmul_grouped_silu: NULL host array");
+    return run_group(ts, n, gs, us, ys, S, (cudaStream_t)stream, "b200q_matmul_grouped_silu");
 }
 
 int b200q_matmul_tc_noalloc(const b200q_tensor *h, const float *x, float *y, int S, void *stream) {

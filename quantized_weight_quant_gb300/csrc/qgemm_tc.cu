@@ -501,6 +501,20 @@ cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x,
     return e;
 }
 
+// Stream-ordered workspace from the library's per-device pool (the one the
+// tensor-core path uses for its bf16 copy of x).
+cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaMemPool_t pool;
+    e = get_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
+}
+
+cudaError_t workspace_free(void *ptr, cudaStream_t st) { return cudaFreeAsync(ptr, st); }
+
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the tensor-core path (b200q_matmul_tc_noalloc).
 //

@@ -48,12 +48,15 @@
 // identical chain the result stays within 1e-5 of sum |scale * deq * x| on
 // the workloads' distributions and is exact where every code is the zero
 // point.
+#include <cstring>
+
 #include "qwq_internal.h"
 
 namespace qwq {
 namespace {
 
 constexpr int kMaxWarps = 15;
+constexpr int kMaxSets = B200Q_GROUP_MAX;  // tensors per launch
 constexpr int kSeg = 512;            // bytes per row per stage: 32 lanes x 16 B
 constexpr int kStage = 8 * kSeg;     // one stage: 8 rows x 512 B (one TMA box)
 constexpr int kRound = 16;           // row groups combined per round
@@ -217,26 +220,38 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
     return v[0];
 }
 
+// One launch: nsets weight tensors ("sets") of one format and one I.  The
+// row groups of all sets are numbered consecutively (set j owns
+// [rg_start[j], rg_start[j+1])); CTAs own contiguous runs of that numbering,
+// so a CTA's rows may span several sets.  Sets that read the same x share an
+// x slot: slots are numbered in set order, a new slot wherever a set's input
+// differs from the previous set's, and a CTA stages the slots of its sets.
+template <int MS>
 struct DecParams {
-    const float *scales[2];
-    float *y[2];
-    const float *x;      // [S, I] f32 (offset to this launch's first token)
-    int x_ld;            // row stride of x in elements (I)
-    int y_ld;            // row stride of y in elements (O)
-    int O, I;
-    int ld;              // device row stride in bytes
-    int row_bytes;       // bytes per row per stage: min(512, ld)
-    int k_pad;           // elements per padded row
-    int rg_per_set;      // ceil(O / 8)
-    int n_rg;            // total row groups (sets * rg_per_set)
-    int depth;           // stages per warp
-    int round_rgs;       // row groups combined per round (partials buffer rows)
+    CUtensorMap map[MS];      // decode tensor map of each set
+    const float *scales[MS];
+    float *y[MS];             // [S, O[j]] per set, at this launch's first token
+    const float *xa[MS];      // per x slot: x, or g when silu(g) * u is staged
+    const float *xb[MS];      // per x slot: u when silu(g) * u is staged
+    int rg_start[MS + 1];     // first row group of each set; rg_start[nsets] = n_rg
+    int O[MS];
+    int xslot[MS];            // x slot of each set, nondecreasing
+    int nsets;
+    int silu;                 // stage silu(xa) * xb instead of xa
+    int I;                    // elements per x row (also the row stride of x)
+    int ld;                   // device row stride in bytes
+    int row_bytes;            // bytes per row per stage: min(512, ld)
+    int k_pad;                // elements per padded row
+    int n_rg;                 // total row groups
+    int depth;                // stages per warp
+    int round_rgs;            // row groups combined per round (partials buffer rows)
+    int nx_max;               // most x slots any CTA stages (shared-memory layout)
 };
 
-template <int FMT, int NS>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
-    qmv_decode_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
-                      const DecParams p) {
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+template <int FMT, int NS, int MS>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __grid_constant__ DecParams<MS> p) {
     constexpr int E = F<FMT>::E;
     constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
     constexpr int EW = 32 / bits;                    // elements per 32-bit word
@@ -251,22 +266,33 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     // elements staged per token: whole segments (the lane-interleaved layout
     // addresses every lane slot of a segment), or k_pad for f32
     const int k_alloc = FMT == B200Q_F32 ? p.k_pad : nseg * (kSeg / 4) * EW;
+    const int nxr = p.nx_max * NS;                    // staged x rows (slot-major)
 
-    // shared memory: x' [NS][k_alloc] | rings | mbarriers | partials | per-token terms
+    // shared memory: x' [nx_max][NS][k_alloc] | rings | mbarriers | partials |
+    // per-row exponents | max scratch | done counter | row scales
     float *xs = reinterpret_cast<float *>(smem);
-    uint8_t *ring = smem + (size_t)4 * NS * k_alloc;
+    uint8_t *ring = smem + (size_t)4 * nxr * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * kStage);
     const int kR = p.round_rgs;
     float *part = reinterpret_cast<float *>(bars + nw * depth);        // [kR][nw][NS][8]
-    int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [NS] T
-    float *red = reinterpret_cast<float *>(tok_exp + NS);             // [NS][kMaxWarps]
-    int *done = reinterpret_cast<int *>(red + NS * kMaxWarps);         // warps done with the last round
+    int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [nxr] T
+    float *red = reinterpret_cast<float *>(tok_exp + nxr);            // [nxr][kMaxWarps]
+    int *done = reinterpret_cast<int *>(red + nxr * kMaxWarps);        // warps done with the last round
     float *row_scale = reinterpret_cast<float *>(done + 4);           // [rows of this CTA]
 
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
+    // set of row group rg, scanning forward from set s (rg never decreases
+    // along a scan)
+    auto set_of = [&](int rg, int s) {
+        while (s + 1 < p.nsets && rg >= p.rg_start[s + 1]) ++s;
+        return s;
+    };
+    const int s_lo = set_of(rg0, 0), s_hi = set_of(rg1 - 1, s_lo);
+    const int slot_lo = p.xslot[s_lo];
+    const int nx = p.xslot[s_hi] - slot_lo + 1;       // x slots this CTA stages
 
-    // This warp's units: in round r (row groups [rg0 + 16 r, ...)), the run
+    // This warp's units: in round r (row groups [rg0 + kR r, ...)), the run
     // [w U / nw, (w + 1) U / nw) of its U = rows * nseg units, row-group-major.
     // A cursor walks them in order across rounds.
     struct Cursor {
@@ -305,27 +331,22 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     // producer state (lane 0 only)
     Cursor pc;
     run_of(pc, rg0);
-    int p_stage = 0;
-    long long issued = 0;
+    int p_stage = 0, pset = s_lo;
     auto issue_next = [&]() -> bool {  // lane 0: copy the next unit into the next stage
         if (!normalize(pc)) return false;
-        const int rgl = pc.rgl, sg = pc.sg;
-        const int rg = pc.round_base + rgl;
-        const int set = rg >= p.rg_per_set;
+        const int rg = pc.round_base + pc.rgl;
+        pset = set_of(rg, pset);
         const uint32_t bar = my_bars + 8 * p_stage;
         mbar_expect_tx(bar, (uint32_t)(8 * rb));
-        tma_load_2d(smem_u32(my_ring + (size_t)p_stage * kStage), set ? &map1 : &map0, sg * (kSeg / 4),
-                    (rg - set * p.rg_per_set) * 8, bar, policy);
+        tma_load_2d(smem_u32(my_ring + (size_t)p_stage * kStage), &p.map[pset], pc.sg * (kSeg / 4),
+                    (rg - p.rg_start[pset]) * 8, bar, policy);
         advance(pc);
-        ++issued;
         if (++p_stage == depth) p_stage = 0;
         return true;
     };
 
-    if (tid == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map0)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map1)) : "memory");
-    }
+    if (tid <= s_hi - s_lo)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.map[s_lo + tid])) : "memory");
     if (lane == 0) {
         for (int b = 0; b < depth; ++b) mbar_init(my_bars + 8 * b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -336,18 +357,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     // the row scales are read-only too: start loading this CTA's now (kept
     // in registers, written to shared memory once x is staged)
+    auto scale_of = [&](int r) {
+        const int rg = rg0 + (r >> 3);
+        const int s = set_of(rg, s_lo);
+        const int o = (rg - p.rg_start[s]) * 8 + (r & 7);
+        return o < p.O[s] ? p.scales[s][o] : 0.f;
+    };
     constexpr int kSc = 4;
     float sc_reg[kSc];
 #pragma unroll
     for (int i = 0; i < kSc; ++i) {
         const int r = i * blockDim.x + tid;
-        sc_reg[i] = 0.f;
-        if (r < (rg1 - rg0) * 8) {
-            const int rg = rg0 + (r >> 3);
-            const int set = rg >= p.rg_per_set;
-            const int o = (rg - set * p.rg_per_set) * 8 + (r & 7);
-            if (o < p.O) sc_reg[i] = (set ? p.scales[1] : p.scales[0])[o];
-        }
+        sc_reg[i] = r < (rg1 - rg0) * 8 ? scale_of(r) : 0.f;
     }
 
     // round-0 partials start at zero (warps that touch no unit of a row group
@@ -362,6 +383,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // one staged input value: x, or silu(g) * u
+    auto xval = [&](int j, int t, int k) {
+        const long long off = (long long)t * p.I + k;
+        if (k >= p.I) return 0.f;
+        const float a = p.xa[slot_lo + j][off];
+        return p.silu ? silu_f(a) * p.xb[slot_lo + j][off] : a;
+    };
+
     // ---- stage x.  Quantized formats: 16-byte slot d of the lane-interleaved
     // layout [seg][word q][quad e4][lane][4] holds elements (e4*4 .. e4*4+3) of
     // word q of chunk c = seg * 32 + lane, 4 consecutive elements of x, so each
@@ -370,117 +399,143 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     //     x' = (x * 2^(T + 23)) * 2^(126 - b),  b = the code's bit offset,
     // two exact power-of-two products per element.  f32 weights: x as is.
     const int nthr = blockDim.x;
-    int texp[NS];
-#pragma unroll
-    for (int t = 0; t < NS; ++t) texp[t] = 0;
     if constexpr (FMT == B200Q_F32) {
-        for (int base = 0; base < p.k_pad; base += kXB * nthr) {
-            float v[NS][kXB];                         // all loads of a batch in flight at once
+        for (int j = 0; j < nx; ++j)
+            for (int base = 0; base < p.k_pad; base += kXB * nthr) {
+                float v[NS][kXB];                     // all loads of a batch in flight at once
 #pragma unroll
-            for (int t = 0; t < NS; ++t)
+                for (int t = 0; t < NS; ++t)
 #pragma unroll
-                for (int j = 0; j < kXB; ++j) {
-                    const int k = base + j * nthr + tid;
-                    v[t][j] = k < p.I ? p.x[(long long)t * p.x_ld + k] : 0.f;
-                }
+                    for (int jj = 0; jj < kXB; ++jj) v[t][jj] = xval(j, t, base + jj * nthr + tid);
 #pragma unroll
-            for (int t = 0; t < NS; ++t)
+                for (int t = 0; t < NS; ++t)
 #pragma unroll
-                for (int j = 0; j < kXB; ++j) {
-                    const int k = base + j * nthr + tid;
-                    if (k < p.k_pad) xs[t * k_alloc + k] = v[t][j];
-                }
-        }
+                    for (int jj = 0; jj < kXB; ++jj) {
+                        const int k = base + jj * nthr + tid;
+                        if (k < p.k_pad) xs[(size_t)(j * NS + t) * k_alloc + k] = v[t][jj];
+                    }
+            }
+        if (tid < nxr) tok_exp[tid] = 0;
     } else {
         constexpr int Q4 = EW / 4;                    // quads per word
         const int n_chunks = p.ld / 16;
         const int n_slots = nseg * 4 * Q4 * 32;
-        const bool vec = (p.x_ld & 3) == 0;
+        const bool vec = (p.I & 3) == 0;
         auto slot_src = [&](int d) {                  // first x element of slot d, or -1 past the row
             const int ln = d & 31, rest = d >> 5;
             const int e4 = rest % Q4, q = (rest / Q4) & 3, seg = (rest / Q4) >> 2;
             const int c = seg * 32 + ln;
             return c < n_chunks ? c * E + q * EW + e4 * 4 : -1;
         };
-        auto gather = [&](int t, int k0) {
-            const float *xr_t = p.x + (long long)t * p.x_ld;
+        auto ld4 = [&](const float *r, int k0) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (k0 < 0) return v;
-            if (vec && k0 + 3 < p.I) return *reinterpret_cast<const float4 *>(xr_t + k0);
-            v.x = k0 < p.I ? xr_t[k0] : 0.f;
-            v.y = k0 + 1 < p.I ? xr_t[k0 + 1] : 0.f;
-            v.z = k0 + 2 < p.I ? xr_t[k0 + 2] : 0.f;
-            v.w = k0 + 3 < p.I ? xr_t[k0 + 3] : 0.f;
+            if (vec && k0 + 3 < p.I) return *reinterpret_cast<const float4 *>(r + k0);
+            v.x = k0 < p.I ? r[k0] : 0.f;
+            v.y = k0 + 1 < p.I ? r[k0 + 1] : 0.f;
+            v.z = k0 + 2 < p.I ? r[k0 + 2] : 0.f;
+            v.w = k0 + 3 < p.I ? r[k0 + 3] : 0.f;
             return v;
         };
-        auto put = [&](int t, int d, float4 v, float tscale) {
+        auto gather = [&](int j, int t, int k0) {
+            if (k0 < 0) return make_float4(0.f, 0.f, 0.f, 0.f);
+            const long long off = (long long)t * p.I;
+            float4 v = ld4(p.xa[slot_lo + j] + off, k0);
+            if (p.silu) {
+                const float4 u = ld4(p.xb[slot_lo + j] + off, k0);
+                v = make_float4(silu_f(v.x) * u.x, silu_f(v.y) * u.y, silu_f(v.z) * u.z, silu_f(v.w) * u.w);
+            }
+            return v;
+        };
+        auto absmax4 = [](float4 v) { return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))); };
+        auto put = [&](float *dst, int d, float4 v, float tscale) {
             const int e0 = ((d >> 5) % Q4) * 4;
             v.x = (v.x * tscale) * __int_as_float((253 - bit_offset<FMT>(e0)) << 23);
             v.y = (v.y * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 1)) << 23);
             v.z = (v.z * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 2)) << 23);
             v.w = (v.w * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 3)) << 23);
-            reinterpret_cast<float4 *>(xs + (size_t)t * k_alloc)[d] = v;
+            reinterpret_cast<float4 *>(dst)[d] = v;
         };
-        constexpr int kG = kXB / 4;                   // slots per thread held in registers
-        const bool one_pass = n_slots <= kG * nthr;
-        float4 held[NS][kG];
-        float m[NS];
+        // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
+        auto tok_exponent = [](float mt) { return mt > 0.f ? -23 - ilogbf(mt) : 0; };
+        if (nx == 1) {
+            // one x slot (every CTA of a single tensor or of sets sharing x)
+            constexpr int kG = kXB / 4;               // slots per thread held in registers
+            const bool one_pass = n_slots <= kG * nthr;
+            float4 held[NS][kG];
+            float m[NS];
 #pragma unroll
-        for (int t = 0; t < NS; ++t) m[t] = 0.f;
-        for (int base = 0; base < n_slots; base += kG * nthr) {
+            for (int t = 0; t < NS; ++t) m[t] = 0.f;
+            for (int base = 0; base < n_slots; base += kG * nthr) {
 #pragma unroll
-            for (int t = 0; t < NS; ++t)
+                for (int t = 0; t < NS; ++t)
 #pragma unroll
-                for (int j = 0; j < kG; ++j) {
-                    const int d = base + j * nthr + tid;
-                    held[t][j] = d < n_slots ? gather(t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                    for (int j = 0; j < kG; ++j) {
+                        const int d = base + j * nthr + tid;
+                        held[t][j] = d < n_slots ? gather(0, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
 #pragma unroll
-            for (int t = 0; t < NS; ++t)
+                for (int t = 0; t < NS; ++t)
 #pragma unroll
-                for (int j = 0; j < kG; ++j)
-                    m[t] = fmaxf(m[t], fmaxf(fmaxf(fabsf(held[t][j].x), fabsf(held[t][j].y)),
-                                             fmaxf(fabsf(held[t][j].z), fabsf(held[t][j].w))));
-        }
-#pragma unroll
-        for (int t = 0; t < NS; ++t) {
-            float mt = m[t];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-            if (lane == 0) red[t * kMaxWarps + warp] = mt;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int t = 0; t < NS; ++t) {
-            float mt = 0.f;
-            for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[t * kMaxWarps + w]);
-            // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
-            texp[t] = mt > 0.f ? -23 - ilogbf(mt) : 0;
-        }
-#pragma unroll
-        for (int t = 0; t < NS; ++t) {
-            const float tscale = ldexpf(1.0f, texp[t] + 23);
-            if (one_pass) {
-#pragma unroll
-                for (int j = 0; j < kG; ++j) {
-                    const int d = j * nthr + tid;
-                    if (d < n_slots) put(t, d, held[t][j], tscale);
-                }
-            } else {
-                for (int d = tid; d < n_slots; d += nthr) put(t, d, gather(t, slot_src(d)), tscale);
+                    for (int j = 0; j < kG; ++j) m[t] = fmaxf(m[t], absmax4(held[t][j]));
             }
+#pragma unroll
+            for (int t = 0; t < NS; ++t) {
+                float mt = m[t];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+                if (lane == 0) red[t * kMaxWarps + warp] = mt;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < NS; ++t) {
+                float mt = 0.f;
+                for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[t * kMaxWarps + w]);
+                const int te = tok_exponent(mt);
+                if (tid == t) tok_exp[t] = te;        // read only after later barriers
+                const float tscale = ldexpf(1.0f, te + 23);
+                float *dst = xs + (size_t)t * k_alloc;
+                if (one_pass) {
+#pragma unroll
+                    for (int j = 0; j < kG; ++j) {
+                        const int d = j * nthr + tid;
+                        if (d < n_slots) put(dst, d, held[t][j], tscale);
+                    }
+                } else {
+                    for (int d = tid; d < n_slots; d += nthr) put(dst, d, gather(0, t, slot_src(d)), tscale);
+                }
+            }
+        } else {
+            // several x slots: the maxima first, then a second (L2-resident)
+            // read of x to store it
+            for (int j = 0; j < nx; ++j)
+#pragma unroll
+                for (int t = 0; t < NS; ++t) {
+                    float mt = 0.f;
+#pragma unroll 4
+                    for (int d = tid; d < n_slots; d += nthr) mt = fmaxf(mt, absmax4(gather(j, t, slot_src(d))));
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+                    if (lane == 0) red[(j * NS + t) * kMaxWarps + warp] = mt;
+                }
+            __syncthreads();
+            for (int j = 0; j < nx; ++j)
+#pragma unroll
+                for (int t = 0; t < NS; ++t) {
+                    float mt = 0.f;
+                    for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[(j * NS + t) * kMaxWarps + w]);
+                    const int te = tok_exponent(mt);
+                    if (tid == 0) tok_exp[j * NS + t] = te;
+                    const float tscale = ldexpf(1.0f, te + 23);
+                    float *dst = xs + (size_t)(j * NS + t) * k_alloc;
+#pragma unroll 4
+                    for (int d = tid; d < n_slots; d += nthr) put(dst, d, gather(j, t, slot_src(d)), tscale);
+                }
         }
     }
-    if (tid < NS) tok_exp[tid] = tid == 0 ? texp[0] : texp[NS - 1];   // read only after later barriers
 #pragma unroll
     for (int i = 0; i < kSc; ++i)
         if (i * blockDim.x + tid < (rg1 - rg0) * 8) row_scale[i * blockDim.x + tid] = sc_reg[i];
-    for (int r = kSc * blockDim.x + tid; r < (rg1 - rg0) * 8; r += blockDim.x) {   // very tall CTAs
-        const int rg = rg0 + (r >> 3);
-        const int set = rg >= p.rg_per_set;
-        const int o = (rg - set * p.rg_per_set) * 8 + (r & 7);
-        row_scale[r] = o < p.O ? (set ? p.scales[1] : p.scales[0])[o] : 0.f;
-    }
+    for (int r = kSc * blockDim.x + tid; r < (rg1 - rg0) * 8; r += blockDim.x) row_scale[r] = scale_of(r);  // tall CTAs
     __syncthreads();
 
     if (lane == 0)
@@ -490,9 +545,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     // ---- main loop
     Cursor cc;
     run_of(cc, rg0);
-    int c_stage = 0;
+    int c_stage = 0, cset = s_lo;
     uint32_t c_phase = 0;
     bool ok = true;
+    const float *xsb = xs;                            // x' rows of the current set's slot
     float2 a2[8][NS], az[NS];
     auto clear_acc = [&]() {
 #pragma unroll
@@ -539,6 +595,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             if (rgl != cur_rgl) {
                 if (cur_rgl >= 0) flush(cur_rgl);
                 cur_rgl = rgl;
+                cset = set_of(base + rgl, cset);
+                xsb = xs + (size_t)(p.xslot[cset] - slot_lo) * NS * k_alloc;
             }
             const int chunks = (p.ld - sg * kSeg < kSeg ? p.ld - sg * kSeg : kSeg) / 16;
             if (lane < chunks) {
@@ -550,7 +608,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                     const int k0 = (sg * (kSeg / 16) + lane) * E;
 #pragma unroll
                     for (int t = 0; t < NS; ++t) {
-                        const float4 xf = *reinterpret_cast<const float4 *>(xs + (size_t)t * k_alloc + k0);
+                        const float4 xf = *reinterpret_cast<const float4 *>(xsb + (size_t)t * k_alloc + k0);
 #pragma unroll
                         for (int r = 0; r < 8; ++r) {
                             a2[r][t] = __ffma2_rn(make_float2(__uint_as_float(cw[r].x), __uint_as_float(cw[r].y)),
@@ -569,7 +627,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 #pragma unroll
                             for (int e4 = 0; e4 < EW; e4 += 4) {
                                 const float4 v4 = *reinterpret_cast<const float4 *>(
-                                    xs + (size_t)t * k_alloc +
+                                    xsb + (size_t)t * k_alloc +
                                     ((((size_t)sg * 4 + q) * (EW / 4) + (e4 >> 2)) * 32 + lane) * 4);
                                 xv[t * (EW / 2) + e4 / 2] = make_float2(v4.x, v4.y);
                                 xv[t * (EW / 2) + e4 / 2 + 1] = make_float2(v4.z, v4.w);
@@ -608,17 +666,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         }
         const int rows = (rend - base) * 8;
         for (int t = 0; t < NS; ++t) {
+            int s = s_lo;
             for (int r = c_first; r < rows; r += c_step) {
                 const int rgl = r >> 3, rr = r & 7;
                 float sum = 0.f;
                 for (int w = 0; w < nw; ++w) sum += part[(((size_t)rgl * nw + w) * NS + t) * 8 + rr];
                 const int rg = base + rgl;
-                const int set = rg >= p.rg_per_set;
-                const int o = (rg - set * p.rg_per_set) * 8 + rr;
-                if (o < p.O) {
-                    float *yb = set ? p.y[1] : p.y[0];
-                    const float dot = FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[t]);
-                    yb[(long long)t * p.y_ld + o] = dot * row_scale[(rg - rg0) * 8 + rr];
+                s = set_of(rg, s);
+                const int o = (rg - p.rg_start[s]) * 8 + rr;
+                if (o < p.O[s]) {
+                    const float dot =
+                        FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[(p.xslot[s] - slot_lo) * NS + t]);
+                    p.y[s][(long long)t * p.O[s] + o] = dot * row_scale[(rg - rg0) * 8 + rr];
                 }
             }
         }
@@ -626,10 +685,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     }
     if (!ok) {
         // give up: record the timeout and let this warp's copies land first
+        // (issued units not yet consumed occupy the next stages in order)
         if (lane == 0) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
-        // issued units not yet consumed occupy the next stages in order
-        long long consumed = 0;  // recount: stages wrap, so wait on the next `depth` phases
-        (void)consumed;
         for (int k = 0; k < depth; ++k) {
             mbar_wait(my_bars + 8 * c_stage, c_phase, kWaitNs / 4);
             if (++c_stage == depth) {
@@ -642,15 +699,26 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
 int g_sms = 0;
 
-template <int FMT, int NS>
-cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int grid, cudaStream_t st) {
+// One group: n sets, each a tensor with its input(s) and output at token 0.
+struct Group {
+    const Tensor *t[kMaxSets];
+    const float *xa[kMaxSets];
+    const float *xb[kMaxSets];
+    float *y[kMaxSets];
+    int n;
+    bool silu;
+};
+
+template <int FMT, int NS, int MS>
+cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     constexpr int EW = FMT == B200Q_F32 ? 1 : FMT == B200Q_I8 ? 4 : FMT == B200Q_I4 ? 8 : 16;
     const int nseg = (p.ld + kSeg - 1) / kSeg;
     const size_t k_alloc = FMT == B200Q_F32 ? (size_t)p.k_pad : (size_t)nseg * (kSeg / 4) * EW;
     const size_t stage = (size_t)kStage + 8;                 // ring stage + its mbarrier
     const int rg_cta = (p.n_rg + grid - 1) / grid;
+    const size_t nxr = (size_t)p.nx_max * NS;
     auto fixed_for = [&](int nw, int rr) {
-        return (size_t)4 * NS * k_alloc + (size_t)rr * nw * NS * 8 * 4 + NS * 4 + (size_t)NS * kMaxWarps * 4 + 16 +
+        return 4 * nxr * k_alloc + (size_t)rr * nw * NS * 8 * 4 + nxr * 4 + nxr * kMaxWarps * 4 + 16 +
                (size_t)rg_cta * 8 * 4;
     };
     // warps and depth first (round of kRound), then grow the round to all of
@@ -668,14 +736,18 @@ cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int
         while (big > kRound && fixed_for(nw, big) + (size_t)nw * depth * stage > kSmemMax) big = (big + kRound) / 2;
         rr = big > kRound ? big : kRound;
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS, MS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemMax);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
-    DecParams q = p;
+    DecParams<MS> q = p;
     q.depth = depth;
     q.round_rgs = rr;
     // programmatic dependent launch: this grid may start while the previous
@@ -691,43 +763,85 @@ cudaError_t launch_ns(const Tensor &t, const Tensor *tu, const DecParams &p, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS>, t.dec_map, tu ? tu->dec_map : t.dec_map, q);
+    e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS, MS>, q);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int FMT>
-cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
-                       cudaStream_t st) {
+template <int FMT, int MS>
+cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
     if (!g_sms) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     }
-    DecParams p{};
-    p.scales[0] = t.scales;
-    p.scales[1] = tu ? tu->scales : t.scales;
-    p.x_ld = t.I;
-    p.y_ld = t.O;
-    p.O = t.O;
-    p.I = t.I;
-    p.ld = (int)t.ld;
-    p.row_bytes = (int)(t.ld < kSeg ? t.ld : kSeg);
-    p.k_pad = (int)t.k_pad;
-    p.rg_per_set = (t.O + 7) / 8;
-    p.n_rg = p.rg_per_set * (tu ? 2 : 1);
-    const int grid = p.n_rg < g_sms ? p.n_rg : g_sms;
+    const Tensor &t0 = *g.t[0];
+    DecParams<MS> p;
+    memset(&p, 0, sizeof p);
+    p.nsets = g.n;
+    p.silu = g.silu ? 1 : 0;
+    p.I = t0.I;
+    p.ld = (int)t0.ld;
+    p.row_bytes = (int)(t0.ld < kSeg ? t0.ld : kSeg);
+    p.k_pad = (int)t0.k_pad;
+    int slot = -1, n_rg = 0;
+    for (int j = 0; j < g.n; ++j) {
+        p.map[j] = g.t[j]->dec_map;
+        p.scales[j] = g.t[j]->scales;
+        p.O[j] = g.t[j]->O;
+        p.rg_start[j] = n_rg;
+        n_rg += (g.t[j]->O + 7) / 8;
+        if (j == 0 || g.xa[j] != g.xa[j - 1] || g.xb[j] != g.xb[j - 1]) ++slot;
+        p.xslot[j] = slot;
+    }
+    p.rg_start[g.n] = n_rg;
+    p.n_rg = n_rg;
+    const int grid = n_rg < g_sms ? n_rg : g_sms;
+    // most x slots a CTA spans (the same partition as the kernel's)
+    int nx_max = 1;
+    for (int b = 0, s = 0; b < grid; ++b) {
+        const int r0 = (int)((long long)b * n_rg / grid), r1 = (int)((long long)(b + 1) * n_rg / grid);
+        while (s + 1 < g.n && r0 >= p.rg_start[s + 1]) ++s;
+        int e = s;
+        while (e + 1 < g.n && r1 - 1 >= p.rg_start[e + 1]) ++e;
+        const int nx = p.xslot[e] - p.xslot[s] + 1;
+        if (nx > nx_max) nx_max = nx;
+    }
+    p.nx_max = nx_max;
     for (int s0 = 0; s0 < S;) {
         const int ns = S - s0 >= 2 ? 2 : 1;
-        p.x = x + (long long)s0 * t.I;
-        p.y[0] = y + (long long)s0 * t.O;
-        p.y[1] = tu ? yu + (long long)s0 * t.O : p.y[0];
-        cudaError_t e = ns == 2 ? launch_ns<FMT, 2>(t, tu, p, grid, st) : launch_ns<FMT, 1>(t, tu, p, grid, st);
+        for (int j = 0; j < g.n; ++j) {
+            p.xa[p.xslot[j]] = g.xa[j] + (long long)s0 * t0.I;
+            p.xb[p.xslot[j]] = g.xb[j] ? g.xb[j] + (long long)s0 * t0.I : nullptr;
+            p.y[j] = g.y[j] + (long long)s0 * g.t[j]->O;
+        }
+        cudaError_t e = ns == 2 ? launch_ns<FMT, 2, MS>(p, grid, st) : launch_ns<FMT, 1, MS>(p, grid, st);
         if (e != cudaSuccess) return e;
         s0 += ns;
     }
     return cudaSuccess;
+}
+
+template <int FMT>
+cudaError_t launch_group_fmt(const Group &g, int S, cudaStream_t st) {
+    return g.n <= 2 ? launch_group_ms<FMT, 2>(g, S, st) : launch_group_ms<FMT, kMaxSets>(g, S, st);
+}
+
+cudaError_t launch_group(const Group &g, int S, cudaStream_t st, bool *handled) {
+    *handled = false;
+    if (S < 1 || S > 15 || g.n < 1 || g.n > kMaxSets) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    switch (g.t[0]->fmt) {
+    case B200Q_F32: e = launch_group_fmt<B200Q_F32>(g, S, st); break;
+    case B200Q_I8: e = launch_group_fmt<B200Q_I8>(g, S, st); break;
+    case B200Q_I4: e = launch_group_fmt<B200Q_I4>(g, S, st); break;
+    case B200Q_I2: e = launch_group_fmt<B200Q_I2>(g, S, st); break;
+    default: return cudaSuccess;
+    }
+    if (e == cudaErrorInvalidValue) return cudaSuccess;
+    *handled = (e == cudaSuccess);
+    return e;
 }
 
 }  // namespace
@@ -737,19 +851,37 @@ cudaError_t launch_fmt(const Tensor &t, const Tensor *tu, const float *x, float 
 // shared memory).
 cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
                           cudaStream_t st, bool *handled) {
-    *handled = false;
-    if (S < 1 || S > 15) return cudaSuccess;
-    cudaError_t e = cudaSuccess;
-    switch (t.fmt) {
-    case B200Q_F32: e = launch_fmt<B200Q_F32>(t, tu, x, y, yu, S, st); break;
-    case B200Q_I8: e = launch_fmt<B200Q_I8>(t, tu, x, y, yu, S, st); break;
-    case B200Q_I4: e = launch_fmt<B200Q_I4>(t, tu, x, y, yu, S, st); break;
-    case B200Q_I2: e = launch_fmt<B200Q_I2>(t, tu, x, y, yu, S, st); break;
-    default: return cudaSuccess;
+    Group g{};
+    g.n = tu ? 2 : 1;
+    g.t[0] = &t;
+    g.xa[0] = x;
+    g.y[0] = y;
+    if (tu) {
+        g.t[1] = tu;
+        g.xa[1] = x;
+        g.y[1] = yu;
     }
-    if (e == cudaErrorInvalidValue) return cudaSuccess;
-    *handled = (e == cudaSuccess);
-    return e;
+    return launch_group(g, S, st, handled);
+}
+
+// n (<= 16) tensors of one format and I in one launch per token pair; input
+// j is xa[j], or silu(xa[j]) * xb[j] when silu is set.  *handled = false when
+// the staged inputs do not fit in shared memory (the caller then runs the
+// tensors one at a time).
+cudaError_t launch_decode_group(const Tensor *const *ts, int n, const float *const *xa, const float *const *xb,
+                                float *const *ys, bool silu, int S, cudaStream_t st, bool *handled) {
+    *handled = false;
+    if (n < 1 || n > kMaxSets) return cudaSuccess;
+    Group g{};
+    g.n = n;
+    g.silu = silu;
+    for (int j = 0; j < n; ++j) {
+        g.t[j] = ts[j];
+        g.xa[j] = xa[j];
+        g.xb[j] = silu ? xb[j] : nullptr;
+        g.y[j] = ys[j];
+    }
+    return launch_group(g, S, st, handled);
 }
 
 // Reads and clears the decode kernel's device error word.

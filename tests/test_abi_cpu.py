@@ -94,3 +94,21 @@ def test_tc_threshold_default(built_lib):
     import quantized_weight_quant_gb300 as q
     if "B200Q_TC_MIN_S" not in os.environ:
         assert q.tc_min_s() == 16
+
+
+def test_grouped_argument_errors_without_gpu(built_lib):
+    import quantized_weight_quant_gb300 as q
+    L = q.lib
+    arr = (ctypes.c_void_p * 17)()
+    assert L.b200q_matmul_grouped(arr, 0, arr, arr, 1, None) == q.EINVAL
+    assert "n must be" in q.last_error()
+    assert L.b200q_matmul_grouped(arr, 17, arr, arr, 1, None) == q.EINVAL
+    assert L.b200q_matmul_grouped(None, 2, arr, arr, 1, None) == q.EINVAL
+    assert "NULL host array" in q.last_error()
+    assert L.b200q_matmul_grouped(arr, 2, arr, arr, 1, None) == q.EINVAL    # NULL handles
+    assert "tensor is NULL" in q.last_error()
+    assert L.b200q_matmul_grouped_silu(arr, 2, arr, None, arr, 1, None) == q.EINVAL
+    assert L.b200q_matmul_grouped_silu(arr, 2, arr, arr, arr, 1, None) == q.EINVAL
+    assert q.GROUP_MAX == 16
+    with pytest.raises(ValueError):
+        q.matmul_grouped([1, 2], [3], [4, 5], 1)
