@@ -26,10 +26,13 @@
 //     fields 0-10 in place, 11-15 after one shift; f32 weights FFMA directly.
 //     That is one AND and one FFMA per weight, plus a shift per word.
 //
-// Data movement: a unit is 8 weight rows x 512 bytes.  Every warp streams its
-// units through its own ring of DEPTH shared-memory stages, each filled by one
-// 2-D TMA copy (cp.async.bulk.tensor, mbarrier completion) that lane 0 issues
-// DEPTH-1 units ahead; ~15 warps x 2 stages keep ~120 KB per SM in flight.
+// Data movement: a unit is 8 weight rows x 512 bytes.  Every consumer warp
+// reads its units from its own ring of DEPTH shared-memory stages, each filled
+// by one 2-D TMA copy (cp.async.bulk.tensor) with full / empty mbarrier
+// pairs.  One extra producer warp issues all copies: its lane c feeds consumer
+// warp c, first one unit per ring before the dependency wait (weights are
+// read-only), the rest once x is staged, then a refill whenever a stage is
+// handed back.  The consumers only wait, compute and release.
 // In a unit, lane l takes 16-byte chunk l of all 8 rows (a warp-wide load
 // reads one row's 512 contiguous bytes), so the x values it loads from shared
 // memory serve 8 rows; x is staged lane-interleaved so those loads are
@@ -191,6 +194,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// Non-blocking probe of a phase (true once it has completed).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Barrier among the first n threads of the block (the consumer warps),
+// which leaves the producer warp out.
+__device__ __forceinline__ void consumers_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
+
 // Butterfly reduce-scatter of N values (N a power of two <= 32) over the 32
 // lanes: afterwards every lane holds the full sum of value index
 // lane >> (5 - log2 N) (lanes that differ only in the low bits hold the same).
@@ -251,7 +273,8 @@ struct DecParams {
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 template <int FMT, int NS, int MS>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __grid_constant__ DecParams<MS> p) {
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
+    qmv_decode_kernel(const __grid_constant__ DecParams<MS> p) {
     constexpr int E = F<FMT>::E;
     constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
     constexpr int EW = 32 / bits;                    // elements per 32-bit word
@@ -259,7 +282,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nw = blockDim.x >> 5;
+    const int nw = (blockDim.x >> 5) - 1;            // consumer warps; warp nw copies the weights
+    const int nct = nw * 32;                          // consumer threads
     const int depth = p.depth;
     const int nseg = (p.ld + kSeg - 1) / kSeg;
     const int rb = p.row_bytes;                       // smem row pitch of a stage
@@ -268,17 +292,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
     const int k_alloc = FMT == B200Q_F32 ? p.k_pad : nseg * (kSeg / 4) * EW;
     const int nxr = p.nx_max * NS;                    // staged x rows (slot-major)
 
-    // shared memory: x' [nx_max][NS][k_alloc] | rings | mbarriers | partials |
-    // per-row exponents | max scratch | done counter | row scales
+    // shared memory: x' [nx_max][NS][k_alloc] | rings [nw][depth] | full and
+    // empty mbarriers [2][nw][depth] | partials | per-row exponents | max
+    // scratch | done counter | row scales
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * nxr * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * kStage);
     const int kR = p.round_rgs;
-    float *part = reinterpret_cast<float *>(bars + nw * depth);        // [kR][nw][NS][8]
+    float *part = reinterpret_cast<float *>(bars + 2 * nw * depth + 1);  // [kR][nw][NS][8]
     int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [nxr] T
     float *red = reinterpret_cast<float *>(tok_exp + nxr);            // [nxr][kMaxWarps]
     int *done = reinterpret_cast<int *>(red + nxr * kMaxWarps);        // warps done with the last round
     float *row_scale = reinterpret_cast<float *>(done + 4);           // [rows of this CTA]
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nw * depth);
+    const uint32_t x_ready = smem_u32(bars + 2 * nw * depth);   // completes once x is staged
 
     const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
     const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
@@ -292,20 +319,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
     const int slot_lo = p.xslot[s_lo];
     const int nx = p.xslot[s_hi] - slot_lo + 1;       // x slots this CTA stages
 
-    // This warp's units: in round r (row groups [rg0 + kR r, ...)), the run
-    // [w U / nw, (w + 1) U / nw) of its U = rows * nseg units, row-group-major.
-    // A cursor walks them in order across rounds.
+    // Consumer warp c's units: in round r (row groups [rg0 + kR r, ...)), the
+    // run [c U / nw, (c + 1) U / nw) of its U = rows * nseg units,
+    // row-group-major.  A cursor walks them in order across rounds.
     struct Cursor {
         int round_base, round_end;   // row groups of the current round
         int u, u_end;                // unit index within the round's run
         int rgl, sg;                 // u = rgl * nseg + sg
     };
-    auto run_of = [&](Cursor &c, int base) {
+    auto run_of = [&](Cursor &c, int base, int w) {
         c.round_base = base;
         c.round_end = base + kR < rg1 ? base + kR : rg1;
         const int U = (c.round_end - c.round_base) * nseg;
-        c.u = (int)((long long)warp * U / nw);
-        c.u_end = (int)((long long)(warp + 1) * U / nw);
+        c.u = (int)((long long)w * U / nw);
+        c.u_end = (int)((long long)(w + 1) * U / nw);
         c.rgl = c.u / nseg;
         c.sg = c.u - c.rgl * nseg;
     };
@@ -316,45 +343,88 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
             ++c.rgl;
         }
     };
-    auto normalize = [&](Cursor &c) {  // skip empty runs; false when past the last round
-        while (c.u >= c.u_end) {
-            if (c.round_end >= rg1) return false;
-            run_of(c, c.round_end);
-        }
-        return true;
-    };
-
-    uint8_t *my_ring = ring + (size_t)warp * depth * kStage;
-    const uint32_t my_bars = smem_u32(bars + warp * depth);
-    uint64_t policy = 0;
-
-    // producer state (lane 0 only)
-    Cursor pc;
-    run_of(pc, rg0);
-    int p_stage = 0, pset = s_lo;
-    auto issue_next = [&]() -> bool {  // lane 0: copy the next unit into the next stage
-        if (!normalize(pc)) return false;
-        const int rg = pc.round_base + pc.rgl;
-        pset = set_of(rg, pset);
-        const uint32_t bar = my_bars + 8 * p_stage;
-        mbar_expect_tx(bar, (uint32_t)(8 * rb));
-        tma_load_2d(smem_u32(my_ring + (size_t)p_stage * kStage), &p.map[pset], pc.sg * (kSeg / 4),
-                    (rg - p.rg_start[pset]) * 8, bar, policy);
-        advance(pc);
-        if (++p_stage == depth) p_stage = 0;
-        return true;
-    };
 
     if (tid <= s_hi - s_lo)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.map[s_lo + tid])) : "memory");
-    if (lane == 0) {
-        for (int b = 0; b < depth; ++b) mbar_init(my_bars + 8 * b, 1);
+    if (warp == nw && lane < nw) {
+        for (int b = 0; b < depth; ++b) {
+            mbar_init(full0 + 8 * (lane * depth + b), 1);
+            mbar_init(empty0 + 8 * (lane * depth + b), 1);
+        }
+        if (lane == 0) mbar_init(x_ready, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        policy = evict_first_policy();
-        issue_next();           // one unit per warp before x: x's loads must not queue behind more
     }
-    __syncwarp();
+    __syncthreads();
 
+    if (warp == nw) {
+        // ---- producer: lane c keeps consumer warp c's ring full.  Weights
+        // are read-only, so the first unit of every ring goes out at once,
+        // before the dependency wait the consumers make; the rest of the
+        // rings fill once x is staged (x's loads must not queue behind them).
+        const unsigned pmask = __ballot_sync(0xffffffffu, lane < nw);
+        if (lane >= nw) return;
+        const uint64_t policy = evict_first_policy();
+        Cursor pc;
+        run_of(pc, rg0, lane);
+        auto next = [&]() {          // skip empty runs; false when past the last round
+            while (pc.u >= pc.u_end) {
+                if (pc.round_end >= rg1) return false;
+                run_of(pc, pc.round_end, lane);
+            }
+            return true;
+        };
+        int ps = 0, pset = s_lo;
+        uint32_t eph = 0;
+        const uint32_t my_full = full0 + 8 * lane * depth, my_empty = empty0 + 8 * lane * depth;
+        auto issue = [&]() {
+            const int rg = pc.round_base + pc.rgl;
+            pset = set_of(rg, pset);
+            const uint32_t bar = my_full + 8 * ps;
+            mbar_expect_tx(bar, (uint32_t)(8 * rb));
+            tma_load_2d(smem_u32(ring + ((size_t)lane * depth + ps) * kStage), &p.map[pset], pc.sg * (kSeg / 4),
+                        (rg - p.rg_start[pset]) * 8, bar, policy);
+            advance(pc);
+            if (++ps == depth) {
+                ps = 0;
+                eph ^= 1;
+            }
+        };
+        bool more = next();
+        if (more) {
+            issue();
+            more = next();
+        }
+        if (!mbar_wait(x_ready, 0, kWaitNs)) more = false;   // the consumers report the same timeout
+        for (int k = 1; k < depth && more; ++k) {
+            issue();
+            more = next();
+        }
+        eph = 0;                     // the first refill of each stage waits for its first release
+        unsigned long long t0 = global_ns();
+        while (__any_sync(pmask, more)) {
+            bool progressed = false;
+            if (more && mbar_test(my_empty + 8 * ps, eph)) {
+                issue();
+                more = next();
+                progressed = true;
+            }
+            if (__any_sync(pmask, progressed)) {
+                t0 = global_ns();
+                continue;
+            }
+            // nothing was released: back off; lane 0 decides, for all lanes,
+            // when the consumers have stopped releasing stages
+            const bool late = global_ns() - t0 > kWaitNs;
+            if (__shfl_sync(pmask, late ? 1 : 0, 0)) {
+                if (more) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
+                break;
+            }
+            __nanosleep(64);
+        }
+        return;
+    }
+
+    // ---- consumers
     // the row scales are read-only too: start loading this CTA's now (kept
     // in registers, written to shared memory once x is staged)
     auto scale_of = [&](int r) {
@@ -367,13 +437,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
     float sc_reg[kSc];
 #pragma unroll
     for (int i = 0; i < kSc; ++i) {
-        const int r = i * blockDim.x + tid;
+        const int r = i * nct + tid;
         sc_reg[i] = r < (rg1 - rg0) * 8 ? scale_of(r) : 0.f;
     }
 
     // round-0 partials start at zero (warps that touch no unit of a row group
     // leave 0); the counter picks the warp that combines the last round
-    for (int i = tid; i < kR * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
+    for (int i = tid; i < kR * nw * NS * 8; i += nct) part[i] = 0.f;
     if (tid == 0) *done = 0;
 
     // Everything above touched only the weights, which no kernel writes; x
@@ -398,7 +468,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
     // trip), the per-token max of |x| comes from them, and they are stored as
     //     x' = (x * 2^(T + 23)) * 2^(126 - b),  b = the code's bit offset,
     // two exact power-of-two products per element.  f32 weights: x as is.
-    const int nthr = blockDim.x;
+    const int nthr = nct;
     if constexpr (FMT == B200Q_F32) {
         for (int j = 0; j < nx; ++j)
             for (int base = 0; base < p.k_pad; base += kXB * nthr) {
@@ -485,7 +555,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
                 for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
                 if (lane == 0) red[t * kMaxWarps + warp] = mt;
             }
-            __syncthreads();
+            consumers_sync(nct);
 #pragma unroll
             for (int t = 0; t < NS; ++t) {
                 float mt = 0.f;
@@ -517,7 +587,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
                     for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
                     if (lane == 0) red[(j * NS + t) * kMaxWarps + warp] = mt;
                 }
-            __syncthreads();
+            consumers_sync(nct);
             for (int j = 0; j < nx; ++j)
 #pragma unroll
                 for (int t = 0; t < NS; ++t) {
@@ -534,17 +604,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
     }
 #pragma unroll
     for (int i = 0; i < kSc; ++i)
-        if (i * blockDim.x + tid < (rg1 - rg0) * 8) row_scale[i * blockDim.x + tid] = sc_reg[i];
-    for (int r = kSc * blockDim.x + tid; r < (rg1 - rg0) * 8; r += blockDim.x) row_scale[r] = scale_of(r);  // tall CTAs
-    __syncthreads();
-
-    if (lane == 0)
-        for (int i = 1; i < depth - 1; ++i)
-            if (!issue_next()) break;
+        if (i * nct + tid < (rg1 - rg0) * 8) row_scale[i * nct + tid] = sc_reg[i];
+    for (int r = kSc * nct + tid; r < (rg1 - rg0) * 8; r += nct) row_scale[r] = scale_of(r);  // tall CTAs
+    consumers_sync(nct);
+    if (tid == 0) mbar_arrive(x_ready);
 
     // ---- main loop
+    const uint32_t my_full = full0 + 8 * warp * depth, my_empty = empty0 + 8 * warp * depth;
+    const uint8_t *my_ring = ring + (size_t)warp * depth * kStage;
     Cursor cc;
-    run_of(cc, rg0);
     int c_stage = 0, cset = s_lo;
     uint32_t c_phase = 0;
     bool ok = true;
@@ -580,14 +648,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
         const bool last_round = rend >= rg1;
         if (base != rg0) {
             // zero this round's partials (round 0 was zeroed in the prologue)
-            for (int i = tid; i < kR * nw * NS * 8; i += blockDim.x) part[i] = 0.f;
-            __syncthreads();
+            for (int i = tid; i < kR * nw * NS * 8; i += nct) part[i] = 0.f;
+            consumers_sync(nct);
         }
-        run_of(cc, base);
+        run_of(cc, base, warp);
         int cur_rgl = -1;
         for (; cc.u < cc.u_end; advance(cc)) {
-            if (lane == 0) issue_next();
-            if (!mbar_wait(my_bars + 8 * c_stage, c_phase, kWaitNs)) {
+            if (!mbar_wait(my_full + 8 * c_stage, c_phase, kWaitNs)) {
                 ok = false;
                 break;
             }
@@ -641,7 +708,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
                     }
                 }
             }
-            __syncwarp();  // every lane is done with this stage before lane 0 refills it
+            __syncwarp();  // every lane is done with this stage: hand it back to the producer
+            if (lane == 0) mbar_arrive(my_empty + 8 * c_stage);
             if (++c_stage == depth) {
                 c_stage = 0;
                 c_phase ^= 1;
@@ -650,8 +718,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
         if (cur_rgl >= 0) flush(cur_rgl);
         // combine this round: warps in order, unscale, apply the row scale.
         // The last round is combined by whichever warp finishes last (no
-        // block barrier); earlier rounds by the whole block between barriers.
-        int c_first = tid, c_step = blockDim.x;
+        // block barrier); earlier rounds by all consumers between barriers.
+        int c_first = tid, c_step = nct;
         if (last_round) {
             __threadfence_block();
             int prev = 0;
@@ -662,7 +730,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
             c_first = lane;
             c_step = 32;
         } else {
-            __syncthreads();
+            consumers_sync(nct);
         }
         const int rows = (rend - base) * 8;
         for (int t = 0; t < NS; ++t) {
@@ -681,14 +749,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) qmv_decode_kernel(const __g
                 }
             }
         }
-        if (!last_round) __syncthreads();   // part is reused by the next round
+        if (!last_round) consumers_sync(nct);   // part is reused by the next round
     }
     if (!ok) {
-        // give up: record the timeout and let this warp's copies land first
-        // (issued units not yet consumed occupy the next stages in order)
+        // give up: record the timeout and let the copies the producer issued
+        // into this warp's ring land first (at most `depth` stages ahead)
         if (lane == 0) atomicExch(&g_decode_err, (unsigned)(-B200Q_ETIMEOUT));
         for (int k = 0; k < depth; ++k) {
-            mbar_wait(my_bars + 8 * c_stage, c_phase, kWaitNs / 4);
+            mbar_wait(my_full + 8 * c_stage, c_phase, kWaitNs / 4);
             if (++c_stage == depth) {
                 c_stage = 0;
                 c_phase ^= 1;
@@ -714,11 +782,11 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     constexpr int EW = FMT == B200Q_F32 ? 1 : FMT == B200Q_I8 ? 4 : FMT == B200Q_I4 ? 8 : 16;
     const int nseg = (p.ld + kSeg - 1) / kSeg;
     const size_t k_alloc = FMT == B200Q_F32 ? (size_t)p.k_pad : (size_t)nseg * (kSeg / 4) * EW;
-    const size_t stage = (size_t)kStage + 8;                 // ring stage + its mbarrier
+    const size_t stage = (size_t)kStage + 16;                // ring stage + its full and empty mbarriers
     const int rg_cta = (p.n_rg + grid - 1) / grid;
     const size_t nxr = (size_t)p.nx_max * NS;
     auto fixed_for = [&](int nw, int rr) {
-        return 4 * nxr * k_alloc + (size_t)rr * nw * NS * 8 * 4 + nxr * 4 + nxr * kMaxWarps * 4 + 16 +
+        return 4 * nxr * k_alloc + 8 + (size_t)rr * nw * NS * 8 * 4 + nxr * 4 + nxr * kMaxWarps * 4 + 16 +
                (size_t)rg_cta * 8 * 4;
     };
     // warps and depth first (round of kRound), then grow the round to all of
@@ -755,7 +823,7 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     // touches x or y
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(nw * 32);
+    cfg.blockDim = dim3((nw + 1) * 32);              // consumers + the producer warp
     cfg.dynamicSmemBytes = fixed_for(nw, rr) + (size_t)nw * depth * stage;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
