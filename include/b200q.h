@@ -28,7 +28,16 @@
  *                   rounded to bf16 (nearest, ties to even) inside the call,
  *                   products and sums are f32 on the tensor cores:
  *                   |y - y_exact| <= 4e-3 * |scale[o]| * sum_i |deq * x|
- * NaN and Inf inputs are outside the contract.
+ * NaN and Inf inputs are outside the contract, and so are f32-weight products
+ * |w * x| below the f32 normal range (2^-126): f32 arithmetic rounds them on
+ * the subnormal grid.  Quantized formats stage each row of x scaled by an
+ * exact power of two taken from the row's largest |x|, so the bound also holds
+ * for subnormal or very large x.  On the f32 path they accumulate code * x and
+ * the zero point's z * x in f32 and subtract, so the rounding error follows
+ * sum_i (|code| + z) |x| rather than sum_i |code - z| |x|: the bound holds
+ * for rows whose largest |x| is up to ~1e5 times their typical |x| at
+ * I = 6144 (less at smaller I); a larger isolated outlier that meets
+ * zero-point codes can exceed it.
  *
  * Devices.  A tensor lives on the device that was current when it was
  * uploaded; every call on it must be made with that device current.

@@ -51,6 +51,7 @@
 // identical chain the result stays within 1e-5 of sum |scale * deq * x| on
 // the workloads' distributions and is exact where every code is the zero
 // point.
+#include <climits>
 #include <cstring>
 
 #include "qwq_internal.h"
@@ -194,6 +195,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// floor(log2 m) for finite m > 0, subnormals included (from the bits).
+__device__ __forceinline__ int ilogb_bits(float m) {
+    const int b = __float_as_int(m);
+    const int e = (b >> 23) & 0xFF;
+    return e ? e - 127 : -118 - __clz(b);
+}
+
+// 2^k exactly, for -149 <= k <= 127.
+__device__ __forceinline__ float pow2i(int k) {
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+// Per-token power-of-two factors of the staged x (see the staging code).
+struct TokScale {
+    float s1, s2;        // x * 2^k = (x * s1) * s2
+    float u1, u2;        // 2^-T = u1 * u2
+};
+
 // Non-blocking probe of a phase (true once it has completed).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -242,6 +261,25 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
     return v[0];
 }
 
+// Division by a launch constant d >= 1 as a multiply and a shift, exact for
+// dividends 0 <= n < 2^31: with s = ceil(log2 d) and m = ceil(2^(31+s) / d),
+// n m / 2^(31+s) = n / d + e with 0 <= e < n / 2^(31+s) < 2^-s <= 1/d, which
+// is below the gap from n / d up to the next integer.
+struct FastDiv {
+    uint32_t m;
+    int sh;                   // 31 + s
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    int s = 0;
+    while ((1ull << s) < d) ++s;
+    return FastDiv{(uint32_t)(((1ull << (31 + s)) + d - 1) / d), 31 + s};
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv &f) {
+    return (int)(((unsigned long long)(unsigned)n * f.m) >> f.sh);
+}
+
 // One launch: nsets weight tensors ("sets") of one format and one I.  The
 // row groups of all sets are numbered consecutively (set j owns
 // [rg_start[j], rg_start[j+1])); CTAs own contiguous runs of that numbering,
@@ -268,6 +306,7 @@ struct DecParams {
     int depth;                // stages per warp
     int round_rgs;            // row groups combined per round (partials buffer rows)
     int nx_max;               // most x slots any CTA stages (shared-memory layout)
+    FastDiv div_grid, div_nw, div_nseg;   // by gridDim.x, the consumer warps, the segments per row
 };
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
@@ -293,22 +332,23 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     const int nxr = p.nx_max * NS;                    // staged x rows (slot-major)
 
     // shared memory: x' [nx_max][NS][k_alloc] | rings [nw][depth] | full and
-    // empty mbarriers [2][nw][depth] | partials | per-row exponents | max
-    // scratch | done counter | row scales
+    // empty mbarriers [2][nw][depth] + x-staged | partials | per-row unscale
+    // factors | max scratch | done counter | row scales
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * nxr * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * kStage);
     const int kR = p.round_rgs;
     float *part = reinterpret_cast<float *>(bars + 2 * nw * depth + 1);  // [kR][nw][NS][8]
-    int *tok_exp = reinterpret_cast<int *>(part + (size_t)kR * nw * NS * 8);  // [nxr] T
-    float *red = reinterpret_cast<float *>(tok_exp + nxr);            // [nxr][kMaxWarps]
+    float *unscale = part + (size_t)kR * nw * NS * 8;                  // [nxr][2]: 2^-T as two factors
+    float *red = unscale + 2 * nxr;                                    // [nxr][kMaxWarps]
     int *done = reinterpret_cast<int *>(red + nxr * kMaxWarps);        // warps done with the last round
     float *row_scale = reinterpret_cast<float *>(done + 4);           // [rows of this CTA]
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nw * depth);
     const uint32_t x_ready = smem_u32(bars + 2 * nw * depth);   // completes once x is staged
 
-    const int rg0 = (int)((long long)blockIdx.x * p.n_rg / gridDim.x);
-    const int rg1 = (int)((long long)(blockIdx.x + 1) * p.n_rg / gridDim.x);
+    // (32-bit products: the host keeps grid * n_rg and nw * round units below 2^31)
+    const int rg0 = fdiv(blockIdx.x * p.n_rg, p.div_grid);
+    const int rg1 = fdiv((blockIdx.x + 1) * p.n_rg, p.div_grid);
     // set of row group rg, scanning forward from set s (rg never decreases
     // along a scan)
     auto set_of = [&](int rg, int s) {
@@ -331,9 +371,9 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         c.round_base = base;
         c.round_end = base + kR < rg1 ? base + kR : rg1;
         const int U = (c.round_end - c.round_base) * nseg;
-        c.u = (int)((long long)w * U / nw);
-        c.u_end = (int)((long long)(w + 1) * U / nw);
-        c.rgl = c.u / nseg;
+        c.u = fdiv(w * U, p.div_nw);
+        c.u_end = fdiv((w + 1) * U, p.div_nw);
+        c.rgl = fdiv(c.u, p.div_nseg);
         c.sg = c.u - c.rgl * nseg;
     };
     auto advance = [&](Cursor &c) {
@@ -346,6 +386,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 
     if (tid <= s_hi - s_lo)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.map[s_lo + tid])) : "memory");
+    if (tid < nxr) reinterpret_cast<unsigned *>(red)[tid] = 0u;   // row maxima of x (atomicMax)
     if (warp == nw && lane < nw) {
         for (int b = 0; b < depth; ++b) {
             mbar_init(full0 + 8 * (lane * depth + b), 1);
@@ -433,12 +474,22 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         const int o = (rg - p.rg_start[s]) * 8 + (r & 7);
         return o < p.O[s] ? p.scales[s][o] : 0.f;
     };
+    // a volatile load stays here, ahead of the dependency wait, instead of
+    // being scheduled next to its use after x is staged
+    auto scale_early = [&](int r) {
+        const int rg = rg0 + (r >> 3);
+        const int s = set_of(rg, s_lo);
+        const int o = (rg - p.rg_start[s]) * 8 + (r & 7);
+        float v = 0.f;
+        if (o < p.O[s]) asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p.scales[s] + o));
+        return v;
+    };
     constexpr int kSc = 4;
     float sc_reg[kSc];
 #pragma unroll
     for (int i = 0; i < kSc; ++i) {
         const int r = i * nct + tid;
-        sc_reg[i] = r < (rg1 - rg0) * 8 ? scale_of(r) : 0.f;
+        sc_reg[i] = r < (rg1 - rg0) * 8 ? scale_early(r) : 0.f;
     }
 
     // round-0 partials start at zero (warps that touch no unit of a row group
@@ -469,6 +520,70 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     //     x' = (x * 2^(T + 23)) * 2^(126 - b),  b = the code's bit offset,
     // two exact power-of-two products per element.  f32 weights: x as is.
     const int nthr = nct;
+    constexpr int Q4 = EW >= 4 ? EW / 4 : 1;      // quads per word (quantized formats)
+    const int n_chunks = p.ld / 16;
+    const int n_slots = nseg * 4 * Q4 * 32;
+    const bool vec = (p.I & 3) == 0;
+    auto slot_src = [&](int d) {                  // first x element of slot d, or -1 past the row
+        const int ln = d & 31, rest = d >> 5;
+        const int e4 = rest % Q4, q = (rest / Q4) & 3, seg = (rest / Q4) >> 2;
+        const int c = seg * 32 + ln;
+        return c < n_chunks ? c * E + q * EW + e4 * 4 : -1;
+    };
+    auto ld4 = [&](const float *r, int k0) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vec && k0 + 3 < p.I) return *reinterpret_cast<const float4 *>(r + k0);
+        v.x = k0 < p.I ? r[k0] : 0.f;
+        v.y = k0 + 1 < p.I ? r[k0 + 1] : 0.f;
+        v.z = k0 + 2 < p.I ? r[k0 + 2] : 0.f;
+        v.w = k0 + 3 < p.I ? r[k0 + 3] : 0.f;
+        return v;
+    };
+    auto gather = [&](int j, int t, int k0) {
+        if (k0 < 0) return make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long off = (long long)t * p.I;
+        float4 v = ld4(p.xa[slot_lo + j] + off, k0);
+        if (p.silu) {
+            const float4 u = ld4(p.xb[slot_lo + j] + off, k0);
+            v = make_float4(silu_f(v.x) * u.x, silu_f(v.y) * u.y, silu_f(v.z) * u.z, silu_f(v.w) * u.w);
+        }
+        return v;
+    };
+    auto absmax4 = [](float4 v) { return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))); };
+    // 2^(126 - b) for element i of quad e4 (a constant once both are known)
+    auto post = [](int e4, int i) { return __int_as_float((253 - bit_offset<FMT>(e4 * 4 + i)) << 23); };
+    auto put = [&](float *dst, int d, float4 v, const TokScale &ts) {
+        const int e4 = (d >> 5) % Q4;
+        float4 f = make_float4(post(0, 0), post(0, 1), post(0, 2), post(0, 3));
+#pragma unroll
+        for (int qq = 1; qq < Q4; ++qq)
+            if (e4 == qq) f = make_float4(post(qq, 0), post(qq, 1), post(qq, 2), post(qq, 3));
+        if (ts.s1 != 1.f) {                       // largest |x| subnormal: 2^k in two factors
+            v.x *= ts.s1;
+            v.y *= ts.s1;
+            v.z *= ts.s1;
+            v.w *= ts.s1;
+        }
+        v.x = (v.x * ts.s2) * f.x;
+        v.y = (v.y * ts.s2) * f.y;
+        v.z = (v.z * ts.s2) * f.z;
+        v.w = (v.w * ts.s2) * f.w;
+        reinterpret_cast<float4 *>(dst)[d] = v;
+    };
+    // With max |x| in [2^E, 2^(E+1)) and k = -E, x * 2^k stays below 2 and
+    // the products code * x * 2^T, T = k - 23, below 2^-14.  2^k needs two
+    // factors when max |x| is subnormal (k up to 149), and so does 2^-T
+    // when max |x| >= 2^105.  Every factor is an exact power of two.
+    auto tok_scale_k = [](int k) {
+        TokScale r;
+        const int ku = 23 - k;
+        r.u1 = ku > 127 ? pow2i(64) : 1.f;
+        r.u2 = pow2i(ku > 127 ? ku - 64 : ku);
+        r.s1 = k > 127 ? pow2i(64) : 1.f;
+        r.s2 = pow2i(k > 127 ? k - 64 : k);
+        return r;
+    };
+    auto tok_scale = [&](float mt) { return tok_scale_k(mt > 0.f ? -ilogb_bits(mt) : 0); };
     if constexpr (FMT == B200Q_F32) {
         for (int j = 0; j < nx; ++j)
             for (int base = 0; base < p.k_pad; base += kXB * nthr) {
@@ -485,121 +600,60 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                         if (k < p.k_pad) xs[(size_t)(j * NS + t) * k_alloc + k] = v[t][jj];
                     }
             }
-        if (tid < nxr) tok_exp[tid] = 0;
+        if (tid < 2 * nxr) unscale[tid] = 1.f;
     } else {
-        constexpr int Q4 = EW / 4;                    // quads per word
-        const int n_chunks = p.ld / 16;
-        const int n_slots = nseg * 4 * Q4 * 32;
-        const bool vec = (p.I & 3) == 0;
-        auto slot_src = [&](int d) {                  // first x element of slot d, or -1 past the row
-            const int ln = d & 31, rest = d >> 5;
-            const int e4 = rest % Q4, q = (rest / Q4) & 3, seg = (rest / Q4) >> 2;
-            const int c = seg * 32 + ln;
-            return c < n_chunks ? c * E + q * EW + e4 * 4 : -1;
+        // First pass: every row with the fixed exponent k = -20, exact for
+        // rows whose largest |x| lies in [2^-20, 2^20) (or that are all zero);
+        // the largest |x| of each row is gathered on the side (atomicMax on
+        // the bits of non-negative floats) and checked after the barrier.
+        constexpr int kFix = -20;
+        const TokScale ts_fix = tok_scale_k(kFix);
+        unsigned *tokmax = reinterpret_cast<unsigned *>(red);   // [nxr], zeroed before the first barrier
+        auto note_max = [&](int row, float mt) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            if (lane == 0) atomicMax(tokmax + row, __float_as_uint(mt));
         };
-        auto ld4 = [&](const float *r, int k0) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (vec && k0 + 3 < p.I) return *reinterpret_cast<const float4 *>(r + k0);
-            v.x = k0 < p.I ? r[k0] : 0.f;
-            v.y = k0 + 1 < p.I ? r[k0 + 1] : 0.f;
-            v.z = k0 + 2 < p.I ? r[k0 + 2] : 0.f;
-            v.w = k0 + 3 < p.I ? r[k0 + 3] : 0.f;
-            return v;
-        };
-        auto gather = [&](int j, int t, int k0) {
-            if (k0 < 0) return make_float4(0.f, 0.f, 0.f, 0.f);
-            const long long off = (long long)t * p.I;
-            float4 v = ld4(p.xa[slot_lo + j] + off, k0);
-            if (p.silu) {
-                const float4 u = ld4(p.xb[slot_lo + j] + off, k0);
-                v = make_float4(silu_f(v.x) * u.x, silu_f(v.y) * u.y, silu_f(v.z) * u.z, silu_f(v.w) * u.w);
-            }
-            return v;
-        };
-        auto absmax4 = [](float4 v) { return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))); };
-        auto put = [&](float *dst, int d, float4 v, float tscale) {
-            const int e0 = ((d >> 5) % Q4) * 4;
-            v.x = (v.x * tscale) * __int_as_float((253 - bit_offset<FMT>(e0)) << 23);
-            v.y = (v.y * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 1)) << 23);
-            v.z = (v.z * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 2)) << 23);
-            v.w = (v.w * tscale) * __int_as_float((253 - bit_offset<FMT>(e0 + 3)) << 23);
-            reinterpret_cast<float4 *>(dst)[d] = v;
-        };
-        // max |x| in [2^E, 2^(E+1)): products code * x * 2^T stay below 2^-14
-        auto tok_exponent = [](float mt) { return mt > 0.f ? -23 - ilogbf(mt) : 0; };
-        if (nx == 1) {
-            // one x slot (every CTA of a single tensor or of sets sharing x)
-            constexpr int kG = kXB / 4;               // slots per thread held in registers
-            const bool one_pass = n_slots <= kG * nthr;
+        constexpr int kG = kXB / 4;                   // slots per thread held in registers
+        if (nx == 1 && n_slots <= kG * nthr) {
+            // one x slot, one round trip: every load of the thread in flight at once
             float4 held[NS][kG];
-            float m[NS];
 #pragma unroll
-            for (int t = 0; t < NS; ++t) m[t] = 0.f;
-            for (int base = 0; base < n_slots; base += kG * nthr) {
+            for (int t = 0; t < NS; ++t)
 #pragma unroll
-                for (int t = 0; t < NS; ++t)
-#pragma unroll
-                    for (int j = 0; j < kG; ++j) {
-                        const int d = base + j * nthr + tid;
-                        held[t][j] = d < n_slots ? gather(0, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                for (int t = 0; t < NS; ++t)
-#pragma unroll
-                    for (int j = 0; j < kG; ++j) m[t] = fmaxf(m[t], absmax4(held[t][j]));
-            }
-#pragma unroll
-            for (int t = 0; t < NS; ++t) {
-                float mt = m[t];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-                if (lane == 0) red[t * kMaxWarps + warp] = mt;
-            }
-            consumers_sync(nct);
+                for (int j = 0; j < kG; ++j) {
+                    const int d = j * nthr + tid;
+                    held[t][j] = d < n_slots ? gather(0, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
             for (int t = 0; t < NS; ++t) {
                 float mt = 0.f;
-                for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[t * kMaxWarps + w]);
-                const int te = tok_exponent(mt);
-                if (tid == t) tok_exp[t] = te;        // read only after later barriers
-                const float tscale = ldexpf(1.0f, te + 23);
-                float *dst = xs + (size_t)t * k_alloc;
-                if (one_pass) {
 #pragma unroll
-                    for (int j = 0; j < kG; ++j) {
-                        const int d = j * nthr + tid;
-                        if (d < n_slots) put(dst, d, held[t][j], tscale);
-                    }
-                } else {
-                    for (int d = tid; d < n_slots; d += nthr) put(dst, d, gather(0, t, slot_src(d)), tscale);
+                for (int j = 0; j < kG; ++j) {
+                    const int d = j * nthr + tid;
+                    mt = fmaxf(mt, absmax4(held[t][j]));
+                    if (d < n_slots) put(xs + (size_t)t * k_alloc, d, held[t][j], ts_fix);
                 }
+                note_max(t, mt);
             }
         } else {
-            // several x slots: the maxima first, then a second (L2-resident)
-            // read of x to store it
             for (int j = 0; j < nx; ++j)
 #pragma unroll
                 for (int t = 0; t < NS; ++t) {
-                    float mt = 0.f;
-#pragma unroll 4
-                    for (int d = tid; d < n_slots; d += nthr) mt = fmaxf(mt, absmax4(gather(j, t, slot_src(d))));
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-                    if (lane == 0) red[(j * NS + t) * kMaxWarps + warp] = mt;
-                }
-            consumers_sync(nct);
-            for (int j = 0; j < nx; ++j)
-#pragma unroll
-                for (int t = 0; t < NS; ++t) {
-                    float mt = 0.f;
-                    for (int w = 0; w < nw; ++w) mt = fmaxf(mt, red[(j * NS + t) * kMaxWarps + w]);
-                    const int te = tok_exponent(mt);
-                    if (tid == 0) tok_exp[j * NS + t] = te;
-                    const float tscale = ldexpf(1.0f, te + 23);
                     float *dst = xs + (size_t)(j * NS + t) * k_alloc;
+                    float mt = 0.f;
 #pragma unroll 4
-                    for (int d = tid; d < n_slots; d += nthr) put(dst, d, gather(j, t, slot_src(d)), tscale);
+                    for (int d = tid; d < n_slots; d += nthr) {
+                        const float4 v = gather(j, t, slot_src(d));
+                        mt = fmaxf(mt, absmax4(v));
+                        put(dst, d, v, ts_fix);
+                    }
+                    note_max(j * NS + t, mt);
                 }
+        }
+        if (tid < nxr) {
+            unscale[2 * tid] = ts_fix.u1;
+            unscale[2 * tid + 1] = ts_fix.u2;
         }
     }
 #pragma unroll
@@ -607,6 +661,30 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         if (i * nct + tid < (rg1 - rg0) * 8) row_scale[i * nct + tid] = sc_reg[i];
     for (int r = kSc * nct + tid; r < (rg1 - rg0) * 8; r += nct) row_scale[r] = scale_of(r);  // tall CTAs
     consumers_sync(nct);
+    if constexpr (FMT != B200Q_F32) {
+        // rows outside the fixed exponent's range: staged again with their own
+        // exponent (every thread reads the same maxima, so the branch is uniform)
+        const unsigned *tokmax = reinterpret_cast<const unsigned *>(red);
+        auto in_range = [](float mt) { return mt == 0.f || (mt >= 0x1p-20f && mt < 0x1p20f); };
+        bool redo = false;
+        for (int r = 0; r < nx * NS; ++r) redo |= !in_range(__uint_as_float(tokmax[r]));
+        if (redo) {
+            for (int j = 0; j < nx; ++j)
+                for (int t = 0; t < NS; ++t) {
+                    const int row = j * NS + t;
+                    const float mt = __uint_as_float(tokmax[row]);
+                    if (in_range(mt)) continue;
+                    const TokScale ts = tok_scale(mt);
+                    if (tid == 0) {
+                        unscale[2 * row] = ts.u1;
+                        unscale[2 * row + 1] = ts.u2;
+                    }
+                    float *dst = xs + (size_t)row * k_alloc;
+                    for (int d = tid; d < n_slots; d += nct) put(dst, d, gather(j, t, slot_src(d)), ts);
+                }
+            consumers_sync(nct);
+        }
+    }
     if (tid == 0) mbar_arrive(x_ready);
 
     // ---- main loop
@@ -732,20 +810,35 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         } else {
             consumers_sync(nct);
         }
+        // partials added in warp order (warps that ran no unit of a row group
+        // hold +0 there); the set's fields stay in registers until the row
+        // groups move into the next set
         const int rows = (rend - base) * 8;
         for (int t = 0; t < NS; ++t) {
             int s = s_lo;
+            int s_start = p.rg_start[s], s_next = s + 1 < p.nsets ? p.rg_start[s + 1] : INT_MAX, s_O = p.O[s];
+            float *s_y = p.y[s];
+            int s_xr = (p.xslot[s] - slot_lo) * NS + t;
             for (int r = c_first; r < rows; r += c_step) {
                 const int rgl = r >> 3, rr = r & 7;
+                const float *pp = part + ((size_t)rgl * nw * NS + t) * 8 + rr;
                 float sum = 0.f;
-                for (int w = 0; w < nw; ++w) sum += part[(((size_t)rgl * nw + w) * NS + t) * 8 + rr];
+#pragma unroll
+                for (int w = 0; w < kMaxWarps; ++w)
+                    if (w < nw) sum += pp[(size_t)w * NS * 8];
                 const int rg = base + rgl;
-                s = set_of(rg, s);
-                const int o = (rg - p.rg_start[s]) * 8 + rr;
-                if (o < p.O[s]) {
-                    const float dot =
-                        FMT == B200Q_F32 ? sum : ldexpf(sum, -tok_exp[(p.xslot[s] - slot_lo) * NS + t]);
-                    p.y[s][(long long)t * p.O[s] + o] = dot * row_scale[(rg - rg0) * 8 + rr];
+                if (rg >= s_next) {
+                    s = set_of(rg, s);
+                    s_start = p.rg_start[s];
+                    s_next = s + 1 < p.nsets ? p.rg_start[s + 1] : INT_MAX;
+                    s_O = p.O[s];
+                    s_y = p.y[s];
+                    s_xr = (p.xslot[s] - slot_lo) * NS + t;
+                }
+                const int o = (rg - s_start) * 8 + rr;
+                if (o < s_O) {
+                    const float dot = (sum * unscale[2 * s_xr]) * unscale[2 * s_xr + 1];   // exact: powers of two
+                    s_y[(long long)t * s_O + o] = dot * row_scale[(rg - rg0) * 8 + rr];
                 }
             }
         }
@@ -786,7 +879,7 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     const int rg_cta = (p.n_rg + grid - 1) / grid;
     const size_t nxr = (size_t)p.nx_max * NS;
     auto fixed_for = [&](int nw, int rr) {
-        return 4 * nxr * k_alloc + 8 + (size_t)rr * nw * NS * 8 * 4 + nxr * 4 + nxr * kMaxWarps * 4 + 16 +
+        return 4 * nxr * k_alloc + 8 + (size_t)rr * nw * NS * 8 * 4 + nxr * 8 + nxr * kMaxWarps * 4 + 16 +
                (size_t)rg_cta * 8 * 4;
     };
     // warps and depth first (round of kRound), then grow the round to all of
@@ -804,6 +897,9 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
         while (big > kRound && fixed_for(nw, big) + (size_t)nw * depth * stage > kSmemMax) big = (big + kRound) / 2;
         rr = big > kRound ? big : kRound;
     }
+    // the kernel's row-group and unit arithmetic is 32-bit
+    if ((long long)grid * p.n_rg >= (1ll << 31) || (long long)nw * rr * nseg >= (1ll << 31))
+        return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -818,6 +914,9 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     DecParams<MS> q = p;
     q.depth = depth;
     q.round_rgs = rr;
+    q.div_grid = make_fastdiv((uint32_t)grid);
+    q.div_nw = make_fastdiv((uint32_t)nw);
+    q.div_nseg = make_fastdiv((uint32_t)nseg);
     // programmatic dependent launch: this grid may start while the previous
     // kernel in the stream drains; it waits (griddepcontrol.wait) before it
     // touches x or y

@@ -63,6 +63,31 @@ def test_onehot_dequant_bit_exact(q, fmt):
             assert np.array_equal(y, y_ref[s0:s0 + 8]), (fmt, s0)
 
 
+@pytest.mark.parametrize("fmt", list(FMTS.values()), ids=list(FMTS))
+def test_extreme_x_magnitudes(q, fmt):
+    """Tokens far from unit scale: every |x| subnormal (largest below 2^-127),
+    every |x| near 1e33 (largest above 2^105), and an outlier 1e3 times the
+    rest of its row.  The per-token power-of-two staging of the quantized formats must
+    stay exact and finite.  f32 weights multiply x as stored, so their
+    subnormal case is a normal-range token instead (their products below the
+    f32 normal range round as f32 arithmetic does, a documented limit)."""
+    O, I, S = 72, 300, 4
+    codes, scales, x = inputs(fmt, O, I, S, seed=17)
+    g = synth.rng(17, 5)
+    x = x.astype(np.float64)
+    if fmt != 0:
+        x[0] = np.sign(x[0]) * g.uniform(1.0, 3.0, I) * 2.0 ** -140  # all subnormal in f32
+    x[1] = x[1] * 1e33
+    x[2, 7] = 1e3                                                   # an activation outlier
+    x[3] = 0.0                                                       # an all-zero token
+    x = x.astype(np.float32)
+    y_ref, bound = oracle.matmul(fmt, O, I, codes, scales, x)
+    with q.tensor_upload(fmt, O, I, codes, scales) as t:
+        y = gpu_matmul(q, t, x, S, O)
+    assert_within(y, y_ref, bound, TOL_F32, "extreme x fmt%d" % fmt)
+    assert np.all(y[3] == 0)
+
+
 def test_exhaustive_codes_through_the_api(q):
     """Every int8 byte, int4 nibble and int2 field value through the device
     path: a row holding all codes, one-hot x per position."""
