@@ -419,6 +419,9 @@ def run_ours(args):
                              "unit": "TFLOP/s", "frac": round(pf["tflops"] / peak_tc, 4),
                              "traffic": recorded_traffic("prefill_i4_12288x6144_s1571"),
                              "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}}
+    # MoE expert layer at S=1 (8 of 256 resident experts), grouped and per expert
+    if not args.no_moe:
+        line["moe_layer"] = moe_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
     # end to end through the host-buffer C-ABI call
     e2e_steps = max(3, min(args.steps, 20))
     e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 2)
@@ -628,6 +631,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill", "moe"])
     ap.add_argument("--fmt", default="i4", choices=["f32", "i8", "i4", "i2"])
     ap.add_argument("--O", type=int, default=12288)
