@@ -345,7 +345,8 @@ def prefill_measure(q, steps, warmup, stream):
         torch.cuda.synchronize()
         times = []
         for _ in range(steps):
-            flush.zero_()                                   # L2 flush between iterations
+            with torch.cuda.stream(stream):
+                flush.zero_()                               # L2 flush, ordered before the timed call
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)

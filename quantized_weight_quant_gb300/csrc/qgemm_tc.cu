@@ -18,15 +18,17 @@
 //      warp 0     TMA producer: per 64-wide k-block, one 2-D load of the
 //                 128-row code tile and one of the 176 x 64 bf16 x tile
 //                 (128-byte swizzle), completion on an mbarrier;
-//      warps 2-5  dequantizers, one thread per weight row: codes -> exact
-//                 bf16 (int4: OR the nibble into the mantissa of 128.0 and
-//                 subtract 136; int8: exact via f32), written in the
-//                 128-byte-swizzled K-major layout the MMA reads;
+//      warps 2-9  dequantizers, two threads per weight row (each half of
+//                 the row's k-block): codes -> exact bf16 (int4: OR the
+//                 nibble into the mantissa of 128.0 and subtract 136; int8:
+//                 exact via f32), written in the 128-byte-swizzled K-major
+//                 layout the MMA reads; two warps per scheduler hide each
+//                 other's load / convert / store latency;
 //      warp 1     MMA issuer (one thread): 4 x tcgen05.mma (kind::f16,
 //                 bf16 in, f32 accumulate, 128 x 176 x 16) per k-block into
 //                 one of two TMEM accumulators; tcgen05.commit releases the
 //                 stage and, after the last k-block, hands the tile to ...
-//      warps 6-9  epilogue: tcgen05.ld of its 32 TMEM lanes, times scale[o],
+//      warps 10-13 epilogue: tcgen05.ld of its 32 TMEM lanes, times scale[o],
 //                 coalesced f32 stores of y (32 consecutive o per store).
 //    Integer codes are exact in bf16 and products are exact in f32, so the
 //    only approximation is x's rounding to bf16 plus f32 accumulation.
@@ -44,8 +46,13 @@ namespace qwq {
 namespace {
 
 constexpr int BM = 128, BN = 176, BK = 64;
-constexpr int kStages = 4;
-constexpr int kThreads = 320;        // 10 warps
+// Pipeline stages (code tile + x tile + dequantized A tile, 42.5 KB for int4,
+// 46.5 KB for int8): as many as fit in 227 KB of shared memory, since the
+// stage ring has to cover a TMA round trip plus dequantization.
+template <int FMT>
+constexpr int kStagesFor = FMT == B200Q_I4 ? 5 : 4;
+constexpr int kThreads = 448;        // 14 warps
+constexpr int kDeqWarps = 8;
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
 constexpr int kAccStride = 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -199,6 +206,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const GemmParams p) {
+    constexpr int kStages = kStagesFor<FMT>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -219,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&tma_full[s]), 1);
-            mbar_init(smem_u32(&a_full[s]), 4);
+            mbar_init(smem_u32(&a_full[s]), kDeqWarps);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -303,9 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) mma_commit(smem_u32(&acc_full[ab]));
             }
         }
-    } else if (warp >= 2 && warp < 6) {
-        // ---------------- dequantizers: thread r owns row r of every A tile
-        const int r = (warp - 2) * 32 + lane;
+    } else if (warp >= 2 && warp < 2 + kDeqWarps) {
+        // ---------------- dequantizers: thread (r, half) owns half of row r
+        // of every A tile (16-byte output chunks 4 half .. 4 half + 3)
+        const int r = ((warp - 2) & 3) * 32 + lane;
+        const int half = (warp - 2) >> 2;
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -319,15 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *arow = a_s + stage * A_BYTES + r * 128;
                 const int sw = r & 7;
                 if (FMT == B200Q_I4) {
-                    const uint4 c0 = *reinterpret_cast<const uint4 *>(crow);
-                    const uint4 c1 = *reinterpret_cast<const uint4 *>(crow + 16);
-                    const uint32_t wv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * half);
+                    const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = deq_i4_word(wv[c]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = 4 * half + i;
+                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = deq_i4_word(wv[i]);
+                    }
                 } else {
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int h = 2 * half + hh;
                         const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * h);
                         const uint2 lo = deq_i8_word(cw.x), hi = deq_i8_word(cw.y);
                         const uint2 lo2 = deq_i8_word(cw.z), hi2 = deq_i8_word(cw.w);
@@ -451,6 +463,7 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, 
     p.nk = (int)(t.k_pad / BK);
     p.code_bytes = code_bytes;
     constexpr int C_BYTES = BM * code_bytes;
+    constexpr int kStages = kStagesFor<FMT>;
     const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BN * BK * 2 + C_BYTES) + (3 * kStages + 4) * 8 + 16;
     static bool attr = false;
     if (!attr) {
