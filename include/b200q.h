@@ -21,9 +21,15 @@
  * (4*I for f32); the unused high bits of a row's last byte are ignored.
  *
  * Numerics.  Every path computes from exact dequantized integers (or the
- * stored floats) and accumulates in f32.  Two paths:
+ * stored floats) and accumulates in f32.  Three paths:
  *   f32 path        (S < b200q_tc_min_s(), every S for f32 and int2 tensors):
- *                   |y - y_exact| <= 1e-5 * |scale[o]| * sum_i |deq * x|
+ *                   |y - y_exact| <= 1e-5 * |scale[o]| * sum_i |deq * x|;
+ *                   int8 / int4 tensors from b200q_tcx_min_s() rows run it on
+ *                   the tensor cores (B200Q_PATH_TCX): each row of x is scaled
+ *                   by an exact power of two and split exactly into three
+ *                   bf16 pieces, so every product is exact and only the f32
+ *                   accumulation rounds; S = 1 and the other formats run
+ *                   SIMT kernels (B200Q_PATH_F32)
  *   tensor-core path (int8 / int4 tensors at S >= b200q_tc_min_s()): x is
  *                   rounded to bf16 (nearest, ties to even) inside the call,
  *                   products and sums are f32 on the tensor cores:
@@ -67,7 +73,7 @@ enum {
 };
 
 /* Path selection for b200q_matmul_ex. */
-enum { B200Q_PATH_AUTO = 0, B200Q_PATH_F32 = 1, B200Q_PATH_TC = 2 };
+enum { B200Q_PATH_AUTO = 0, B200Q_PATH_F32 = 1, B200Q_PATH_TC = 2, B200Q_PATH_TCX = 3 };
 
 /*
  * Upload one weight tensor to the current device and keep it resident.
@@ -115,16 +121,18 @@ int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *s
 
 /*
  * As b200q_matmul with an explicit path: B200Q_PATH_AUTO (same as
- * b200q_matmul), B200Q_PATH_F32 (the f32-accurate path at any S, any format)
- * or B200Q_PATH_TC (the bf16 tensor-core path at any S >= 1; int8 and int4
- * tensors only, B200Q_EINVAL otherwise).
+ * b200q_matmul), B200Q_PATH_F32 (the f32-accurate SIMT kernels at any S, any
+ * format), B200Q_PATH_TCX (the f32-accurate tensor-core path, x in three bf16
+ * pieces, any S >= 1, at most 15 rows per launch) or B200Q_PATH_TC (the bf16
+ * tensor-core path at any S >= 1).  The tensor-core paths take int8 and int4
+ * tensors only (B200Q_EINVAL otherwise).
  */
 int b200q_matmul_ex(const b200q_tensor *t, const float *x, float *y, int S, int path,
                     void *stream);
 
 /*
- * The path b200q_matmul takes for this tensor at this S: B200Q_PATH_F32 or
- * B200Q_PATH_TC, or a negative status for a bad argument.
+ * The path b200q_matmul takes for this tensor at this S: B200Q_PATH_F32,
+ * B200Q_PATH_TCX or B200Q_PATH_TC, or a negative status for a bad argument.
  */
 int b200q_matmul_path(const b200q_tensor *t, int S);
 
@@ -135,6 +143,14 @@ int b200q_matmul_path(const b200q_tensor *t, int S);
  * environment variable B200Q_TC_MIN_S (>= 1) read at the first call.
  */
 int b200q_tc_min_s(void);
+
+/*
+ * Threshold S from which int8 / int4 tensors below b200q_tc_min_s() take the
+ * f32-accurate tensor-core path (B200Q_PATH_TCX) instead of the SIMT decode
+ * kernels; the environment variable B200Q_TCX_MIN_S (>= 1) overrides the
+ * default, read at the first call.  A value >= b200q_tc_min_s() disables it.
+ */
+int b200q_tcx_min_s(void);
 
 /*
  * Fused gate/up pair: yg = matmul(tg, x) and yu = matmul(tu, x) in one pass

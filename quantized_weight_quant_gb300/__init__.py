@@ -17,7 +17,7 @@ import numpy as np
 
 F32, I8, I4, I2 = 0, 1, 2, 3
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4
-PATH_AUTO, PATH_F32, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_F32, PATH_TC, PATH_TCX = 0, 1, 2, 3
 GROUP_MAX = 16
 FORMATS = {"f32": F32, "i8": I8, "i4": I4, "i2": I2}
 
@@ -49,6 +49,8 @@ def _load():
     L.b200q_matmul_path.restype = ci
     L.b200q_tc_min_s.argtypes = []
     L.b200q_tc_min_s.restype = ci
+    L.b200q_tcx_min_s.argtypes = []
+    L.b200q_tcx_min_s.restype = ci
     L.b200q_matmul_gate_up.argtypes = [vp, vp, vp, vp, vp, ci, vp]
     L.b200q_matmul_gate_up.restype = ci
     L.b200q_matmul_grouped.argtypes = [vp, ci, vp, vp, ci, vp]
@@ -94,6 +96,10 @@ def device_status() -> int:
 
 def tc_min_s() -> int:
     return int(lib.b200q_tc_min_s())
+
+
+def tcx_min_s() -> int:
+    return int(lib.b200q_tcx_min_s())
 
 
 def _check(rc: int) -> int:

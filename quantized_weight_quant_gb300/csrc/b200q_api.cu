@@ -19,6 +19,8 @@ namespace qwq {
 // Kernels of the other translation units.
 cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
                           cudaStream_t st, bool *handled);
+cudaError_t launch_tcx(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
+                       cudaStream_t st, bool *handled);
 cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu,
                               int S, cudaStream_t st, bool *handled);
 cudaError_t decode_take_error(unsigned int *code);
@@ -80,7 +82,7 @@ int check_io(const Tensor &t, const float *x, const float *y, int S, const char 
 
 std::atomic<long long> g_launches{0};
 
-int g_tc_min_s = 0;
+int g_tc_min_s = 0, g_tcx_min_s = 0;
 std::once_flag g_tc_once;
 
 struct Staging {
@@ -94,22 +96,39 @@ Staging g_staging[64];
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
-int tc_min_s() {
+void read_thresholds() {
     std::call_once(g_tc_once, [] {
-        int v = 16;
-        if (const char *s = std::getenv("B200Q_TC_MIN_S")) {
-            int p = std::atoi(s);
-            if (p >= 1) v = p;
-        }
-        g_tc_min_s = v;
+        auto env_int = [](const char *name, int dflt) {
+            if (const char *s = std::getenv(name)) {
+                int p = std::atoi(s);
+                if (p >= 1) return p;
+            }
+            return dflt;
+        };
+        g_tc_min_s = env_int("B200Q_TC_MIN_S", 16);
+        g_tcx_min_s = env_int("B200Q_TCX_MIN_S", kTcxMinS);
     });
+}
+
+int tc_min_s() {
+    read_thresholds();
     return g_tc_min_s;
 }
 
+int tcx_min_s() {
+    read_thresholds();
+    return g_tcx_min_s;
+}
+
+// AUTO: int8 / int4 take the bf16 tensor-core path from tc_min_s() rows, the
+// f32-accurate tensor-core path (x in three bf16 pieces) from tcx_min_s()
+// rows, the SIMT f32 path below; f32 and int2 tensors always the SIMT path.
 int select_path(const Tensor &t, int S, int path) {
-    if (path == B200Q_PATH_AUTO)
-        return ((t.fmt == B200Q_I4 || t.fmt == B200Q_I8) && S >= tc_min_s()) ? B200Q_PATH_TC : B200Q_PATH_F32;
-    return path;
+    if (path != B200Q_PATH_AUTO) return path;
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return B200Q_PATH_F32;
+    if (S >= tc_min_s()) return B200Q_PATH_TC;
+    if (S >= tcx_min_s()) return B200Q_PATH_TCX;
+    return B200Q_PATH_F32;
 }
 
 int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S, int path,
@@ -118,10 +137,11 @@ int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, floa
     path = select_path(t, S, path);
     cudaError_t e = cudaSuccess;
     bool handled = false;
-    if (path == B200Q_PATH_TC) {
+    if (path == B200Q_PATH_TC || path == B200Q_PATH_TCX) {
         if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
-            return fail(B200Q_EINVAL, "%s: the tensor-core path takes int8 and int4 tensors only", who);
-        e = launch_prefill_tc(t, tu, x, y, yu, S, st, &handled);
+            return fail(B200Q_EINVAL, "%s: the tensor-core paths take int8 and int4 tensors only", who);
+        e = path == B200Q_PATH_TC ? launch_prefill_tc(t, tu, x, y, yu, S, st, &handled)
+                                  : launch_tcx(t, tu, x, y, yu, S, st, &handled);
         if (e == cudaSuccess && !handled)
             return fail(B200Q_ECUDA, "%s: no tensor-core kernel for this shape", who);
     } else {
@@ -154,6 +174,8 @@ int b200q_device_status(void) {
 }
 
 int b200q_tc_min_s(void) { return tc_min_s(); }
+
+int b200q_tcx_min_s(void) { return tcx_min_s(); }
 
 b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, const float *scales) {
     g_err.clear();
@@ -287,7 +309,7 @@ int b200q_matmul_ex(const b200q_tensor *h, const float *x, float *y, int S, int 
     if (rc) return rc;
     const Tensor &t = *reinterpret_cast<const Tensor *>(h);
     if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul: S must be >= 0 (got %d)", S);
-    if (path != B200Q_PATH_AUTO && path != B200Q_PATH_F32 && path != B200Q_PATH_TC)
+    if (path != B200Q_PATH_AUTO && path != B200Q_PATH_F32 && path != B200Q_PATH_TC && path != B200Q_PATH_TCX)
         return fail(B200Q_EINVAL, "b200q_matmul: unknown path %d", path);
     if (S == 0) return B200Q_OK;
     rc = check_io(t, x, y, S, "b200q_matmul");
@@ -362,7 +384,9 @@ int run_group(const b200q_tensor *const *hs, int n, const float *const *xa, cons
     int rc = check_group(hs, n, xa, xb, ys, S, ts, who);
     if (rc || S == 0) return rc;
     const bool silu = xb != nullptr;
-    if (select_path(*ts[0], S, B200Q_PATH_AUTO) == B200Q_PATH_F32) {
+    // below the bf16 tensor-core threshold the whole group is one decode launch
+    // per two rows; from it, each tensor runs its own tensor-core call
+    if (select_path(*ts[0], S, B200Q_PATH_AUTO) != B200Q_PATH_TC) {
         bool handled = false;
         cudaError_t e = launch_decode_group(ts, n, xa, xb, ys, silu, S, st, &handled);
         if (e != cudaSuccess) return cuda_fail(e, who);

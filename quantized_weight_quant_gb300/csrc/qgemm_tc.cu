@@ -46,11 +46,15 @@ namespace qwq {
 namespace {
 
 constexpr int BM = 128, BN = 176, BK = 64;
-// Pipeline stages (code tile + x tile + dequantized A tile, 42.5 KB for int4,
-// 46.5 KB for int8): as many as fit in 227 KB of shared memory, since the
-// stage ring has to cover a TMA round trip plus dequantization.
-template <int FMT>
-constexpr int kStagesFor = FMT == B200Q_I4 ? 5 : 4;
+// Pipeline stages (code tile + x tile + dequantized A tile; 42.5 KB for int4
+// at 176 tokens): as many as fit in 227 KB of shared memory, at most 8, since
+// the stage ring has to cover a TMA round trip plus dequantization.
+template <int FMT, int BNT>
+constexpr int stages_for() {
+    constexpr int per = BM * BK * 2 + BNT * BK * 2 + BM * (FMT == B200Q_I4 ? 32 : 64);
+    constexpr int n = (232448 - 1024 - 512) / per;
+    return n > 8 ? 8 : n;
+}
 constexpr int kThreads = 448;        // 14 warps
 constexpr int kDeqWarps = 8;
 constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
@@ -124,15 +128,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
+// M = 128, N = bnt.
+constexpr uint32_t idesc_for(int bnt) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bnt >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -196,22 +203,28 @@ __device__ __forceinline__ uint2 deq_i8_word(uint32_t w) {
 
 struct GemmParams {
     const float *scales;
+    const float2 *unscale;   // x pieces: per token, 2^-k as two exact factors
     float *y;
     int O, S;
     int m_tiles, n_tiles, nk;
     int code_bytes;      // bytes of one code tile row per k-block (32 int4, 64 int8)
 };
 
-template <int FMT>
+// BNT: columns of the B tile (tokens, or x pieces).  PIECES: B holds three
+// bf16 pieces per token (rows 3s, 3s+1, 3s+2, summing to x exactly) and the
+// epilogue adds each token's three columns.
+template <int FMT, int BNT, bool PIECES>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const GemmParams p) {
-    constexpr int kStages = kStagesFor<FMT>;
+    constexpr int kStages = stages_for<FMT, BNT>();
+    constexpr uint32_t kIdesc = idesc_for(BNT);
+    static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 256 && (!PIECES || BNT <= 48), "token tile");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     constexpr int A_BYTES = BM * BK * 2;               // 16384
-    constexpr int B_BYTES = BN * BK * 2;               // 22528
+    constexpr int B_BYTES = BNT * BK * 2;
     constexpr int C_BYTES = BM * (FMT == B200Q_I4 ? 32 : 64);
     uint8_t *a_s = smem;                                 // [kStages][A_BYTES]
     uint8_t *b_s = a_s + kStages * A_BYTES;              // [kStages][B_BYTES]
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
-                const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BN;
+                const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BNT;
                 for (int kb = 0; kb < p.nk; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1)) {
                         ok = false;
@@ -300,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_addr = smem_u32(b_s + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        mma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k),
+                        mma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), kIdesc,
                                  (kb > 0 || k > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty[stage]));
                     if (++stage == kStages) {
@@ -365,19 +378,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ab = t & 1;
             if (!mbar_wait(smem_u32(&acc_full[ab]), (t >> 1) & 1)) break;
             tc_fence_after();
-            const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BN;
+            const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BNT;
             const int o = m0 + quarter * 32 + lane;
             const float sc = o < p.O ? p.scales[o] : 0.f;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kAccStride;
-#pragma unroll 1
-            for (int c = 0; c < BN / 16; ++c) {
-                float v[16];
-                tmem_ld16(taddr + c * 16, v);
-                const int s0 = n0 + c * 16;
+            if constexpr (PIECES) {
+                float v[BNT];
+#pragma unroll
+                for (int c = 0; c < BNT / 16; ++c) {
+                    float w16[16];
+                    tmem_ld16(taddr + c * 16, w16);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[c * 16 + j] = w16[j];
+                }
                 if (o < p.O) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (s0 + j < p.S) p.y[(long long)(s0 + j) * p.O + o] = v[j] * sc;
+                    for (int s3 = 0; s3 < BNT / 3; ++s3)
+                        if (s3 < p.S) {
+                            const float2 u = p.unscale[s3];
+                            const float dot = (((v[3 * s3] + v[3 * s3 + 1]) + v[3 * s3 + 2]) * u.x) * u.y;   // exact scaling
+                            p.y[(long long)s3 * p.O + o] = dot * sc;
+                        }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BNT / 16; ++c) {
+                    float v[16];
+                    tmem_ld16(taddr + c * 16, v);
+                    const int s0 = n0 + c * 16;
+                    if (o < p.O) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (s0 + j < p.S) p.y[(long long)(s0 + j) * p.O + o] = v[j] * sc;
+                    }
                 }
             }
             tc_fence_before();
@@ -423,6 +456,112 @@ __global__ void x_to_bf16_kernel(const float *__restrict__ x, __nv_bfloat16 *__r
     }
 }
 
+// 2^k exactly for -149 <= k <= 127 (from the bits).
+__device__ __forceinline__ float pow2_bits(int k) {
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+// x f32 [S, I] -> exact three-piece bf16 split, one block per token.  The
+// row is first scaled by 2^k (k from its largest |x|, so the scaled row lies
+// below 2 in magnitude; two factors when k > 127): with v = x 2^k,
+// p0 = RN(v), p1 = RN(v - p0), p2 = v - p0 - p1, where both subtractions are
+// exact (operands within a factor of two) and p2 has at most 8 significant
+// bits, so p0 + p1 + p2 = v exactly.  Rows 3s, 3s+1, 3s+2 of xb [rows, k_pad]
+// receive the pieces (int4 tensors: each 8-group in the order
+// 0,4,1,5,2,6,3,7), unscale[s] = 2^-k as two factors; block S zeroes rows
+// 3S .. rows-1.
+constexpr int kPieceThreads = 512;
+constexpr int kPieceGroups = 2;          // 8-groups per thread kept in registers
+
+__global__ void __launch_bounds__(kPieceThreads)
+    x_to_pieces_kernel(const float *__restrict__ x, __nv_bfloat16 *__restrict__ xb, float2 *__restrict__ unscale,
+                       int S, int I, int k_pad, int rows, int permute8) {
+    const int groups = k_pad / 8;
+    const int tid = threadIdx.x;
+    if ((int)blockIdx.x == S) {
+        for (long long g = tid; g < (long long)(rows - 3 * S) * groups; g += kPieceThreads)
+            reinterpret_cast<uint4 *>(xb + (long long)3 * S * k_pad)[g] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    const int s = blockIdx.x;
+    const float *xr = x + (long long)s * I;
+    auto load8 = [&](int g, float (&v)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = g * 8 + i < I ? xr[g * 8 + i] : 0.f;
+    };
+    float held[kPieceGroups][8];
+    float m = 0.f;
+    for (int base = 0; base < groups; base += kPieceGroups * kPieceThreads) {
+#pragma unroll
+        for (int j = 0; j < kPieceGroups; ++j) {
+            const int g = base + j * kPieceThreads + tid;
+            if (g < groups) load8(g, held[j]);
+            else
+#pragma unroll
+                for (int i = 0; i < 8; ++i) held[j][i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(held[j][i]));
+        }
+    }
+    __shared__ float red[kPieceThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    m = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPieceThreads / 32; ++w) m = fmaxf(m, red[w]);
+    // k = -floor(log2 m) from the bits (subnormal m included); 0 for a zero row
+    int k = 0;
+    if (m > 0.f) {
+        const int b = __float_as_int(m), e = (b >> 23) & 0xFF;
+        k = -(e ? e - 127 : -118 - __clz(b));
+    }
+    const float s1 = k > 127 ? pow2_bits(64) : 1.f, s2 = pow2_bits(k > 127 ? k - 64 : k);
+    const int ku = -k;                                         // 2^-k as u1 * u2
+    const float u1 = ku > 127 ? pow2_bits(64) : 1.f, u2 = pow2_bits(ku > 127 ? ku - 64 : ku);
+    if (tid == 0) unscale[s] = make_float2(u1, u2);
+    __nv_bfloat16 *r0 = xb + (long long)3 * s * k_pad;
+    auto emit = [&](int g, const float (&v)[8]) {
+        float pc[3][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float a = (v[i] * s1) * s2;
+            const float p0 = __bfloat162float(__float2bfloat16_rn(a));
+            const float r1 = a - p0;
+            const float p1 = __bfloat162float(__float2bfloat16_rn(r1));
+            pc[0][i] = p0;
+            pc[1][i] = p1;
+            pc[2][i] = r1 - p1;
+        }
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            uint4 o;
+            if (permute8) {
+                o = make_uint4(pack_bf16(pc[j][0], pc[j][4]), pack_bf16(pc[j][1], pc[j][5]),
+                               pack_bf16(pc[j][2], pc[j][6]), pack_bf16(pc[j][3], pc[j][7]));
+            } else {
+                o = make_uint4(pack_bf16(pc[j][0], pc[j][1]), pack_bf16(pc[j][2], pc[j][3]),
+                               pack_bf16(pc[j][4], pc[j][5]), pack_bf16(pc[j][6], pc[j][7]));
+            }
+            reinterpret_cast<uint4 *>(r0 + (long long)j * k_pad)[g] = o;
+        }
+    };
+    if (groups <= kPieceGroups * kPieceThreads) {
+#pragma unroll
+        for (int j = 0; j < kPieceGroups; ++j) {
+            const int g = j * kPieceThreads + tid;
+            if (g < groups) emit(g, held[j]);
+        }
+    } else {
+        for (int g = tid; g < groups; g += kPieceThreads) {
+            float v[8];
+            load8(g, v);
+            emit(g, v);
+        }
+    }
+}
+
 cudaMemPool_t g_pool[64] = {};
 std::mutex g_pool_mu;
 int g_sms = 0;
@@ -443,40 +582,52 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out) {
     return cudaSuccess;
 }
 
-template <int FMT>
-cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, cudaStream_t st) {
+// b_rows: rows of the bf16 B operand (tokens, or the padded pieces rows).
+template <int FMT, int BNT, bool PIECES>
+cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const float2 *unscale, float *y, int S,
+                     cudaStream_t st) {
     constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
     CUtensorMap map_codes, map_x;
     if (!tmap_encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
                    (uint64_t)t.ld, code_bytes, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (!tmap_encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)xb, (uint64_t)t.k_pad, (uint64_t)S,
-                   (uint64_t)t.k_pad * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tmap_encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)xb, (uint64_t)t.k_pad, (uint64_t)b_rows,
+                   (uint64_t)t.k_pad * 2, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     GemmParams p{};
     p.scales = t.scales;
+    p.unscale = unscale;
     p.y = y;
     p.O = t.O;
     p.S = S;
     p.m_tiles = t.o_pad / BM;
-    p.n_tiles = (S + BN - 1) / BN;
+    p.n_tiles = PIECES ? 1 : (S + BNT - 1) / BNT;
     p.nk = (int)(t.k_pad / BK);
     p.code_bytes = code_bytes;
     constexpr int C_BYTES = BM * code_bytes;
-    constexpr int kStages = kStagesFor<FMT>;
-    const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BN * BK * 2 + C_BYTES) + (3 * kStages + 4) * 8 + 16;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    constexpr int kStages = stages_for<FMT, BNT>();
+    const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BNT * BK * 2 + C_BYTES) + (3 * kStages + 4) * 8 + 16;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static bool attr[64] = {};
+    if (!attr[dev]) {
+        e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT, BNT, PIECES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr[dev] = true;
     }
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < g_sms ? tiles : g_sms;
-    qgemm_tc_kernel<FMT><<<grid, kThreads, smem, st>>>(map_codes, map_x, p);
+    qgemm_tc_kernel<FMT, BNT, PIECES><<<grid, kThreads, smem, st>>>(map_codes, map_x, p);
     count_launch();
     return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t run_gemm_x(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, cudaStream_t st) {
+    return run_gemm<FMT, BN, false>(t, xb, S, nullptr, y, S, st);
 }
 
 }  // namespace
@@ -503,13 +654,66 @@ cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x,
     count_launch();
     e = cudaGetLastError();
     if (e == cudaSuccess)
-        e = t.fmt == B200Q_I4 ? run_gemm<B200Q_I4>(t, (__nv_bfloat16 *)ws, y, S, st)
-                              : run_gemm<B200Q_I8>(t, (__nv_bfloat16 *)ws, y, S, st);
+        e = t.fmt == B200Q_I4 ? run_gemm_x<B200Q_I4>(t, (__nv_bfloat16 *)ws, y, S, st)
+                              : run_gemm_x<B200Q_I8>(t, (__nv_bfloat16 *)ws, y, S, st);
     if (e == cudaSuccess && tu)
-        e = t.fmt == B200Q_I4 ? run_gemm<B200Q_I4>(*tu, (__nv_bfloat16 *)ws, yu, S, st)
-                              : run_gemm<B200Q_I8>(*tu, (__nv_bfloat16 *)ws, yu, S, st);
+        e = t.fmt == B200Q_I4 ? run_gemm_x<B200Q_I4>(*tu, (__nv_bfloat16 *)ws, yu, S, st)
+                              : run_gemm_x<B200Q_I8>(*tu, (__nv_bfloat16 *)ws, yu, S, st);
     cudaError_t ef = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = ef;
+    *handled = (e == cudaSuccess);
+    return e;
+}
+
+cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st);
+cudaError_t workspace_free(void *ptr, cudaStream_t st);
+
+// f32-accurate tensor-core path (B200Q_PATH_TCX): x split into three exact
+// bf16 pieces, at most 15 tokens (45 piece columns) per GEMM launch.  With tu
+// the same pieces serve the second tensor.
+template <int FMT>
+cudaError_t run_tcx_chunk(const Tensor &t, const Tensor *tu, const __nv_bfloat16 *pc, int bnt,
+                          const float2 *unscale, float *y, float *yu, int ns, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < (tu ? 2 : 1) && e == cudaSuccess; ++k) {
+        const Tensor &tt = k ? *tu : t;
+        float *yy = k ? yu : y;
+        e = bnt == 16   ? run_gemm<FMT, 16, true>(tt, pc, bnt, unscale, yy, ns, st)
+            : bnt == 32 ? run_gemm<FMT, 32, true>(tt, pc, bnt, unscale, yy, ns, st)
+                        : run_gemm<FMT, 48, true>(tt, pc, bnt, unscale, yy, ns, st);
+    }
+    return e;
+}
+
+cudaError_t launch_tcx(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
+                       cudaStream_t st, bool *handled) {
+    *handled = false;
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int s0 = 0; s0 < S && e == cudaSuccess;) {
+        const int ns = S - s0 < 15 ? S - s0 : 15;
+        const int bnt = 3 * ns <= 16 ? 16 : 3 * ns <= 32 ? 32 : 48;
+        void *ws = nullptr;
+        e = workspace_alloc(&ws, 1024 + (size_t)bnt * t.k_pad * 2, st);
+        if (e != cudaSuccess) return e;
+        float2 *unscale = (float2 *)ws;
+        __nv_bfloat16 *pc = (__nv_bfloat16 *)((uint8_t *)ws + 1024);
+        x_to_pieces_kernel<<<ns + 1, kPieceThreads, 0, st>>>(x + (long long)s0 * t.I, pc, unscale, ns, t.I,
+                                                             (int)t.k_pad, bnt, t.fmt == B200Q_I4 ? 1 : 0);
+        count_launch();
+        e = cudaGetLastError();
+        if (e == cudaSuccess) {
+            float *yc = y + (long long)s0 * t.O, *yuc = tu ? yu + (long long)s0 * tu->O : nullptr;
+            e = t.fmt == B200Q_I4 ? run_tcx_chunk<B200Q_I4>(t, tu, pc, bnt, unscale, yc, yuc, ns, st)
+                                  : run_tcx_chunk<B200Q_I8>(t, tu, pc, bnt, unscale, yc, yuc, ns, st);
+        }
+        cudaError_t ef = workspace_free(ws, st);
+        if (e == cudaSuccess) e = ef;
+        s0 += ns;
+    }
     *handled = (e == cudaSuccess);
     return e;
 }
@@ -585,8 +789,8 @@ cudaError_t launch_prefill_tc_noalloc(const Tensor &t, const float *x, float *y,
     count_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return t.fmt == B200Q_I4 ? run_gemm<B200Q_I4>(t, (__nv_bfloat16 *)ws, y, S, st)
-                             : run_gemm<B200Q_I8>(t, (__nv_bfloat16 *)ws, y, S, st);
+    return t.fmt == B200Q_I4 ? run_gemm_x<B200Q_I4>(t, (__nv_bfloat16 *)ws, y, S, st)
+                             : run_gemm_x<B200Q_I8>(t, (__nv_bfloat16 *)ws, y, S, st);
 }
 
 cudaError_t prefill_take_error(unsigned int *code) {

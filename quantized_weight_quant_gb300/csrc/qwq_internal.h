@@ -32,6 +32,7 @@ struct Tensor {
 
 constexpr int kRowAlign = 128;  // bytes; rows start on 128-byte boundaries
 constexpr int kRowTile = 128;   // O is padded to a multiple of this
+constexpr int kTcxMinS = 5;     // default first S of the three-piece tensor-core path (int8 / int4)
 
 inline int fmt_bits(int fmt) {
     return fmt == B200Q_F32 ? 32 : fmt == B200Q_I8 ? 8 : fmt == B200Q_I4 ? 4 : fmt == B200Q_I2 ? 2 : 0;

@@ -98,9 +98,10 @@ def test_grouped_one_launch_per_token_pair(q):
 
 
 def test_grouped_pair_equals_gate_up(q):
-    """[tg, tu] on one x is the fused gate/up call: the same launch, bit for bit."""
+    """[tg, tu] on one x is the fused gate/up call: the same launch, bit for bit
+    (at S = 1, where both run the SIMT decode kernel)."""
     import torch
-    fmt, O, I, S = 2, 2048, 6144, 2
+    fmt, O, I, S = 2, 2048, 6144, 1
     (cg, sg), (cu, su) = _tensors(fmt, [O, O], I, 5)
     x = to_dev(synth.activations(S, I, 5, 9))
     with q.tensor_upload(fmt, O, I, cg, sg) as tg, q.tensor_upload(fmt, O, I, cu, su) as tu:

@@ -147,11 +147,13 @@ def test_bad_pointers_rejected(q):
 
 
 def test_path_selection(q):
-    thr = q.tc_min_s()
+    thr, thx = q.tc_min_s(), q.tcx_min_s()
     for fmt in (0, 1, 2, 3):
         codes, scales, _ = inputs(fmt, 8, 32, 1)
         with q.tensor_upload(fmt, 8, 32, codes, scales) as t:
-            assert q.matmul_path(t, thr - 1) == q.PATH_F32
+            tcx = fmt in (1, 2) and thx < thr
+            assert q.matmul_path(t, thr - 1) == (q.PATH_TCX if tcx else q.PATH_F32)
+            assert q.matmul_path(t, 1) == (q.PATH_TCX if tcx and thx <= 1 else q.PATH_F32)
             want = q.PATH_TC if fmt in (1, 2) else q.PATH_F32
             assert q.matmul_path(t, thr) == want
 

@@ -43,12 +43,12 @@ def test_tc_ragged(q, fmt, O, I, S):
 
 @pytest.mark.parametrize("fmt", [1, 2], ids=["i8", "i4"])
 def test_threshold_15_16(q, fmt):
-    """S = 15 takes the f32 path (1e-5), S = 16 the tensor-core path."""
+    """S = 15 takes an f32-accurate path (1e-5), S = 16 the bf16 tensor-core path."""
     O, I = 200, 300
     thr = q.tc_min_s()
     codes, scales, x = inputs(fmt, O, I, thr, seed=5)
     with q.tensor_upload(fmt, O, I, codes, scales) as t:
-        assert q.matmul_path(t, thr - 1) == q.PATH_F32
+        assert q.matmul_path(t, thr - 1) in (q.PATH_F32, q.PATH_TCX)
         assert q.matmul_path(t, thr) == q.PATH_TC
         y15 = gpu_matmul(q, t, x[:thr - 1], thr - 1, O)
         y16 = gpu_matmul(q, t, x, thr, O)
@@ -83,8 +83,9 @@ def test_f32_and_int2_reject_tc(q):
         codes, scales, x = inputs(fmt, 16, 64, 20)
         with q.tensor_upload(fmt, 16, 64, codes, scales) as t:
             assert q.matmul_path(t, 100) == q.PATH_F32
-            with pytest.raises(q.B200QError):
-                q.matmul_ex(t, to_dev(x), empty(20, 16), 20, q.PATH_TC)
+            for path in (q.PATH_TC, q.PATH_TCX):
+                with pytest.raises(q.B200QError):
+                    q.matmul_ex(t, to_dev(x), empty(20, 16), 20, path)
 
 
 def _sample_idx(n, k, seed, must):
