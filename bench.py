@@ -423,6 +423,7 @@ def run_ours(args):
     # MoE expert layer at S=1 (8 of 256 resident experts), grouped and per expert
     if not args.no_moe:
         line["moe_layer"] = moe_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
+    line["layer_glue"] = glue_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
     # end to end through the host-buffer C-ABI call
     e2e_steps = max(3, min(args.steps, 20))
     e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 2)
@@ -466,6 +467,7 @@ def run_sweep(args):
         wl.close()
     moe = moe_measure(q, args.steps, args.warmup, stream)
     print(json.dumps(moe), flush=True)
+    print(json.dumps(glue_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)), flush=True)
     pf = prefill_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
     print(json.dumps({"workload": "prefill W4A16 12288x6144 S=1571", "result": pf}), flush=True)
 
@@ -588,6 +590,66 @@ def moe_measure(q, steps, warmup, stream):
             "per_expert_graph": rate(ms_graph),
             "per_expert_plain": rate(ms),
             "bytes_per_layer": layer_bytes}
+
+
+def glue_measure(q, steps, warmup, stream):
+    """Layer glue: RMSNorm with a residual (h = x + r written back, y = norm(h) * w),
+    D = 6144, at S = 1 (a chain of dependent calls as one CUDA graph) and
+    S = 1571 (L2 flushed before each call, on the timed stream)."""
+    import torch
+    import synth
+    D = 6144
+    out = {"workload": "RMSNorm + residual, D=6144"}
+    w = torch.from_numpy(synth.uniform_f32((D,), 0.5, 1.5, 0, 3)).cuda()
+    for S in (1, 1571):
+        x = torch.from_numpy(synth.normal_f32((S, D), 0, 1)).cuda()
+        r = torch.from_numpy(synth.normal_f32((S, D), 0, 2)).cuda()
+        h = torch.empty_like(x)
+        y = torch.empty_like(x)
+        nbytes = 4 * S * D * 4 + 4 * D
+        if S == 1:
+            n = 64
+            with torch.cuda.stream(stream):
+                for _ in range(warmup):
+                    q.rmsnorm(x, w, y, S, D, 1e-6, r=r, h=h, stream=stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    q.rmsnorm(x, w, y, S, D, 1e-6, r=r, h=h, stream=stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(steps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (steps * n)
+            out["S1_us_per_call"] = round(us, 3)
+        else:
+            flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+            with torch.cuda.stream(stream):
+                for _ in range(warmup):
+                    q.rmsnorm(x, w, y, S, D, 1e-6, r=r, h=h, stream=stream)
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(steps):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                q.rmsnorm(x, w, y, S, D, 1e-6, r=r, h=h, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out["S1571"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                            "frac_hbm": round(gbs / peaks()["hbm_gbs"], 4), "bytes": nbytes}
+    return out
 
 
 def run_reference(args):

@@ -219,6 +219,25 @@ int b200q_matmul_grouped_silu(const b200q_tensor *const *ts, int n, const float 
 int b200q_silu_mul(const float *g, const float *u, float *h, long n, void *stream);
 
 /*
+ * Layer glue kept on the device ("The GPU-resident pipeline" section of the
+ * colibri CUDA docs: norms and residual adds run on the GPU while the expert
+ * loop runs).  The norm is not printed on the pages; this is the textbook
+ * RMSNorm with an optional residual, per row s of S rows of D floats:
+ *     h = x + r (r NULL: h = x),  y = h * w / sqrt(mean_d h^2 + eps)
+ *   x, r, y   DEVICE pointers, [S, D] f32, 16-byte aligned
+ *   h         DEVICE pointer [S, D] receiving h, or NULL; it may be x or r
+ *             itself (the residual stream updated in place) but must not
+ *             partially overlap them
+ *   w         DEVICE pointer, D floats
+ *   eps       >= 0 and finite
+ * y must not overlap x, r, h or w.  f32 arithmetic (sum of squares, correctly
+ * rounded square root and division): |y - y_exact| <= 1e-5 * |y_exact| on
+ * rows whose h is not all zero.  S = 0 is a no-op.  One kernel launch.
+ */
+int b200q_rmsnorm(const float *x, const float *r, float *h, const float *w, float *y, int S, int D, float eps,
+                  void *stream);
+
+/*
  * Host-buffer call in the style of the reference backend ("CUDA 后端",
  * section 1: each matmul copies its input to the GPU, runs the kernel and
  * copies the result back, blocking): copies x_host ([S, I] f32) to a

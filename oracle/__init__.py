@@ -62,6 +62,8 @@ def _bind(path: str):
     L.qref_matmul_gate_up.restype = c_int
     L.qref_silu_mul.argtypes = [vp, vp, c_long, vp, vp]
     L.qref_silu_mul.restype = None
+    L.qref_rmsnorm.argtypes = [vp, vp, vp, c_long, c_long, ctypes.c_double, vp, vp, vp]
+    L.qref_rmsnorm.restype = c_int
     L.qref_round_bf16.argtypes = [ctypes.c_float]
     L.qref_round_bf16.restype = ctypes.c_float
     L.qref_matmul_bf16x.argtypes = [c_int, c_long, c_long, vp, vp, vp, c_long, vp,
@@ -190,6 +192,24 @@ def silu_mul(g, u):
     hd = np.empty(g.shape, np.float64)
     _L().qref_silu_mul(_ptr(g), _ptr(u), g.size, _ptr(h), _ptr(hd))
     return h, hd
+
+
+def rmsnorm(x, w, eps: float, r=None):
+    """h = x + r (f32, or x when r is None); y = h * w / sqrt(mean(h^2) + eps)
+    per row, in double.  Returns (h f32, y f32, y f64)."""
+    x = _f32(x)
+    S, D = x.shape
+    w = _f32(w).reshape(D)
+    if r is not None:
+        r = _f32(r).reshape(S, D)
+    h = np.empty((S, D), np.float32)
+    y = np.empty((S, D), np.float32)
+    yd = np.empty((S, D), np.float64)
+    rc = _L().qref_rmsnorm(_ptr(x), _ptr(r) if r is not None else None, _ptr(w), S, D, float(eps),
+                           _ptr(h), _ptr(y), _ptr(yd))
+    if rc:
+        raise ValueError("qref_rmsnorm: bad argument")
+    return h, y, yd
 
 
 def round_bf16(v) -> np.ndarray:

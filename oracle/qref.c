@@ -180,6 +180,39 @@ void qref_silu_mul(const float *g, const float *u, long n, float *h, double *hdb
 }
 
 /*
+ * Layer glue kept on the device (colibri CUDA docs, "The GPU-resident
+ * pipeline": rmsnorms and residual adds run on the GPU between the expert
+ * loops).  The pages name the operation but do not print it; this is the
+ * textbook RMSNorm, in double:
+ *     h[s,d] = x[s,d] + r[s,d]           (r may be NULL: h = x)
+ *     y[s,d] = h[s,d] * w[d] / sqrt(mean_d h[s,d]^2 + eps)
+ * h is formed as an f32 sum (one rounding of the exact sum, which is what an
+ * f32 addition gives) and normalized as stored; y is returned rounded to f32
+ * and unrounded.  Returns 0, or -1 for a bad argument.
+ */
+int qref_rmsnorm(const float *x, const float *r, const float *w, long S, long D, double eps, float *h,
+                 float *y, double *ydbl)
+{
+    if (S < 0 || D <= 0 || !x || !w || eps < 0) return -1;
+    for (long s = 0; s < S; ++s) {
+        double ss = 0.0;
+        for (long d = 0; d < D; ++d) {
+            float hv = r ? (float)((double)x[s * D + d] + (double)r[s * D + d]) : x[s * D + d];
+            if (h) h[s * D + d] = hv;
+            ss += (double)hv * (double)hv;
+        }
+        double inv = 1.0 / sqrt(ss / (double)D + eps);
+        for (long d = 0; d < D; ++d) {
+            float hv = r ? (float)((double)x[s * D + d] + (double)r[s * D + d]) : x[s * D + d];
+            double v = (double)hv * (double)w[d] * inv;
+            if (y) y[s * D + d] = (float)v;
+            if (ydbl) ydbl[s * D + d] = v;
+        }
+    }
+    return 0;
+}
+
+/*
  * Round an f32 to the nearest bfloat16 (8 significant bits, f32's exponent
  * range), ties to the even significand, returned as an f32.  Written from the
  * definition: take the two bf16 neighbours of v (truncation toward zero and

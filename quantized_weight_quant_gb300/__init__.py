@@ -57,6 +57,8 @@ def _load():
     L.b200q_matmul_grouped.restype = ci
     L.b200q_matmul_grouped_silu.argtypes = [vp, ci, vp, vp, vp, ci, vp]
     L.b200q_matmul_grouped_silu.restype = ci
+    L.b200q_rmsnorm.argtypes = [vp, vp, vp, vp, vp, ci, ci, cf, vp]
+    L.b200q_rmsnorm.restype = ci
     L.b200q_silu_mul.argtypes = [vp, vp, vp, cl, vp]
     L.b200q_silu_mul.restype = ci
     L.b200q_matmul_host.argtypes = [vp, vp, vp, ci, vp]
@@ -253,6 +255,12 @@ def tc_noalloc_capacity() -> int:
 
 def silu_mul(g, u, h, n: int, stream=None) -> None:
     _check(lib.b200q_silu_mul(_dptr(g), _dptr(u), _dptr(h), n, _stream(stream)))
+
+
+def rmsnorm(x, w, y, S: int, D: int, eps: float, r=None, h=None, stream=None) -> None:
+    """y = (x + r) * w / sqrt(mean((x + r)^2) + eps) per row; h receives x + r
+    when given (b200q_rmsnorm)."""
+    _check(lib.b200q_rmsnorm(_dptr(x), _dptr(r), _dptr(h), _dptr(w), _dptr(y), S, D, eps, _stream(stream)))
 
 
 def matmul_host(t, x_host, y_host, S: int, stream=None) -> None:

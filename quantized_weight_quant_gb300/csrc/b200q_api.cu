@@ -467,6 +467,25 @@ int b200q_silu_mul(const float *g, const float *u, float *h, long n, void *strea
     return B200Q_OK;
 }
 
+int b200q_rmsnorm(const float *x, const float *r, float *h, const float *w, float *y, int S, int D, float eps,
+                  void *stream) {
+    if (S < 0 || D < 1) return fail(B200Q_EINVAL, "b200q_rmsnorm: need S >= 0 and D >= 1 (got S=%d, D=%d)", S, D);
+    if (!(eps >= 0.f) || eps > 3.0e38f) return fail(B200Q_EINVAL, "b200q_rmsnorm: eps must be finite and >= 0");
+    if (S == 0) return B200Q_OK;
+    if (!x || !w || !y) return fail(B200Q_EINVAL, "b200q_rmsnorm: x, w and y must not be NULL");
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (r && !aligned16(r)) || (h && !aligned16(h)))
+        return fail(B200Q_EINVAL, "b200q_rmsnorm: pointers must be 16-byte aligned");
+    const size_t nb = (size_t)S * D * 4;
+    if (overlap(y, nb, x, nb) || (r && overlap(y, nb, r, nb)) || (h && overlap(y, nb, h, nb)) ||
+        overlap(y, nb, w, (size_t)D * 4))
+        return fail(B200Q_EINVAL, "b200q_rmsnorm: y must not overlap x, r, h or w");
+    if (h && ((h != x && overlap(h, nb, x, nb)) || (r && h != r && overlap(h, nb, r, nb))))
+        return fail(B200Q_EINVAL, "b200q_rmsnorm: h may equal x or r but must not partially overlap them");
+    cudaError_t e = launch_rmsnorm(x, r, h, w, y, S, D, eps, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_rmsnorm");
+    return B200Q_OK;
+}
+
 int b200q_matmul_host(const b200q_tensor *h, const float *x_host, float *y_host, int S, void *stream) {
     int rc = check_tensor(h, "b200q_matmul_host");
     if (rc) return rc;

@@ -164,6 +164,101 @@ __global__ void silu_mul_kernel(const float *__restrict__ g, const float *__rest
         h[i] = g[i] / (1.f + expf(-g[i])) * u[i];
 }
 
+// Layer glue kept on the device (colibri CUDA docs, "The GPU-resident
+// pipeline": the norms and residual adds run on the GPU).  Textbook RMSNorm
+// with an optional residual, one block per row:
+//     h = x + r (r may be NULL: h = x),  y = h * w / sqrt(mean(h^2) + eps)
+// h is stored when h_out is given (it may be x or r itself: the residual
+// stream updated in place).  Rows of up to kRmsHeld float4 per thread stay in
+// registers between the two passes; longer rows are read again (from h_out
+// when given).  1 / sqrt uses the correctly rounded square root and division.
+constexpr int kRmsThreads = 256;
+constexpr int kRmsHeld = 8;
+
+__global__ void __launch_bounds__(kRmsThreads)
+    rmsnorm_kernel(const float *x, const float *r, float *h_out, const float *__restrict__ w, float *y, int D,
+                   float eps) {
+    const long long off = (long long)blockIdx.x * D;
+    const int tid = threadIdx.x;
+    __shared__ float red[kRmsThreads / 32];
+    float ss = 0.f;
+    if ((D & 3) == 0) {
+        const int D4 = D / 4;
+        const float4 *x4 = reinterpret_cast<const float4 *>(x + off);
+        const float4 *r4 = r ? reinterpret_cast<const float4 *>(r + off) : nullptr;
+        float4 *h4 = h_out ? reinterpret_cast<float4 *>(h_out + off) : nullptr;
+        auto hval = [&](int k) {
+            float4 v = x4[k];
+            if (r4) {
+                const float4 b = r4[k];
+                v = make_float4(v.x + b.x, v.y + b.y, v.z + b.z, v.w + b.w);
+            }
+            return v;
+        };
+        float4 held[kRmsHeld];
+#pragma unroll
+        for (int i = 0; i < kRmsHeld; ++i) {
+            const int k = i * kRmsThreads + tid;
+            held[i] = k < D4 ? hval(k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kRmsHeld; ++i) {
+            const int k = i * kRmsThreads + tid;
+            if (k < D4 && h4) h4[k] = held[i];
+            ss += held[i].x * held[i].x + held[i].y * held[i].y + held[i].z * held[i].z + held[i].w * held[i].w;
+        }
+        for (int k = kRmsHeld * kRmsThreads + tid; k < D4; k += kRmsThreads) {
+            const float4 v = hval(k);
+            if (h4) h4[k] = v;
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRmsThreads / 32; ++i) ss += red[i];
+        const float inv = 1.f / sqrtf(ss / (float)D + eps);
+        const float4 *w4 = reinterpret_cast<const float4 *>(w);
+        float4 *y4 = reinterpret_cast<float4 *>(y + off);
+#pragma unroll
+        for (int i = 0; i < kRmsHeld; ++i) {
+            const int k = i * kRmsThreads + tid;
+            if (k < D4) {
+                const float4 g = w4[k];
+                const float4 v = held[i];
+                y4[k] = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+            }
+        }
+        for (int k = kRmsHeld * kRmsThreads + tid; k < D4; k += kRmsThreads) {
+            const float4 v = h4 ? h4[k] : hval(k);
+            const float4 g = w4[k];
+            y4[k] = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+        }
+    } else {
+        const float *xr = x + off, *rr = r ? r + off : nullptr;
+        float *hr = h_out ? h_out + off : nullptr;
+        for (int k = tid; k < D; k += kRmsThreads) {
+            const float v = rr ? xr[k] + rr[k] : xr[k];
+            if (hr) hr[k] = v;
+            ss += v * v;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRmsThreads / 32; ++i) ss += red[i];
+        const float inv = 1.f / sqrtf(ss / (float)D + eps);
+        for (int k = tid; k < D; k += kRmsThreads) {
+            const float v = hr ? hr[k] : (rr ? xr[k] + rr[k] : xr[k]);
+            y[off + k] = v * inv * w[k];
+        }
+    }
+}
+
 int sm_count() {
     static int n = 0;
     if (!n) {
@@ -216,6 +311,13 @@ cudaError_t launch_silu_mul(const float *g, const float *u, float *h, long n, cu
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     silu_mul_kernel<<<(int)blocks, 256, 0, st>>>(g, u, h, n);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float *x, const float *r, float *h, const float *w, float *y, int S, int D,
+                           float eps, cudaStream_t st) {
+    rmsnorm_kernel<<<S, kRmsThreads, 0, st>>>(x, r, h, w, y, D, eps);
     count_launch();
     return cudaGetLastError();
 }

@@ -65,4 +65,7 @@ cudaError_t launch_qmv_simt(const Tensor &t, const Tensor *tu, const float *x, f
 
 cudaError_t launch_silu_mul(const float *g, const float *u, float *h, long n, cudaStream_t st);
 
+cudaError_t launch_rmsnorm(const float *x, const float *r, float *h, const float *w, float *y, int S, int D,
+                           float eps, cudaStream_t st);
+
 }  // namespace qwq

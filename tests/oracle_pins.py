@@ -271,6 +271,41 @@ def check_silu():
     assert np.array_equal(h, hd.astype(np.float32))
 
 
+def check_rmsnorm():
+    """RMSNorm (textbook, the pages name it without printing it): a worked
+    example by hand, closed forms, the residual sum, the eps term, row
+    independence and scale invariance."""
+    one = np.ones(2, np.float32)
+    # [3, 4]: mean square 12.5, y = [3, 4] / sqrt(12.5)
+    _, y, yd = Q.rmsnorm(np.array([[3.0, 4.0]], np.float32), one, 0.0)
+    assert np.allclose(yd, [[0.848528137423857, 1.131370849898476]], rtol=1e-14, atol=0)
+    # the weight multiplies per element
+    _, _, yd = Q.rmsnorm(np.array([[3.0, 4.0]], np.float32), np.array([2.0, -1.0], np.float32), 0.0)
+    assert np.allclose(yd, [[1.697056274847714, -1.131370849898476]], rtol=1e-14, atol=0)
+    # a constant row c: h / |c| = sign(c), so y = -w exactly for c = -2
+    w5 = np.array([1.0, 0.5, -3.0, 2.0, 0.25], np.float32)
+    _, y, yd = Q.rmsnorm(np.full((1, 5), -2.0, np.float32), w5, 0.0)
+    assert np.array_equal(yd[0], -w5.astype(np.float64)) and np.array_equal(y[0], -w5)
+    # eps enters under the root: [1, 1] with eps 3 -> 1 / sqrt(1 + 3) = 0.5
+    _, _, yd = Q.rmsnorm(np.array([[1.0, 1.0]], np.float32), one, 3.0)
+    assert np.array_equal(yd, [[0.5, 0.5]])
+    # residual: h = x + r = [4, 0], mean square 8, y = [sqrt 2, 0]
+    h, _, yd = Q.rmsnorm(np.array([[1.0, 2.0]], np.float32), one, 0.0, r=np.array([[3.0, -2.0]], np.float32))
+    assert np.array_equal(h, [[4.0, 0.0]])
+    assert abs(yd[0, 0] - np.sqrt(2.0)) < 1e-15 and yd[0, 1] == 0.0
+    # rows are normalized independently; a power-of-two scale of a row cancels exactly
+    g = synth.rng(5, 0)
+    x = g.standard_normal((2, 7)).astype(np.float32)
+    w7 = g.uniform(0.5, 2.0, 7).astype(np.float32)
+    _, y, yd = Q.rmsnorm(x, w7, 0.0)
+    _, y4, yd4 = Q.rmsnorm(np.stack([x[0] * 4.0, x[1]]).astype(np.float32), w7, 0.0)
+    assert np.array_equal(y4, y) and np.allclose(yd4, yd, rtol=1e-15)
+    _, y1, _ = Q.rmsnorm(x[1:], w7, 0.0)
+    assert np.array_equal(y1[0], y[1])
+    # mean of squares: sum of y^2 / w^2 equals D (eps = 0)
+    assert abs(np.sum((yd[0] / w7) ** 2) - 7.0) < 1e-12
+
+
 def check_round_bf16():
     import torch
     one = 1.0

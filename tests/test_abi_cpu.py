@@ -112,3 +112,15 @@ def test_grouped_argument_errors_without_gpu(built_lib):
     assert q.GROUP_MAX == 16
     with pytest.raises(ValueError):
         q.matmul_grouped([1, 2], [3], [4, 5], 1)
+
+
+def test_rmsnorm_argument_errors_without_gpu(built_lib):
+    import quantized_weight_quant_gb300 as q
+    L = q.lib
+    assert L.b200q_rmsnorm(None, None, None, None, None, 0, 8, 1e-6, None) == q.OK      # S == 0
+    assert L.b200q_rmsnorm(None, None, None, None, None, 1, 0, 1e-6, None) == q.EINVAL  # D == 0
+    assert L.b200q_rmsnorm(None, None, None, None, None, 1, 8, -1.0, None) == q.EINVAL  # eps < 0
+    assert L.b200q_rmsnorm(None, None, None, None, None, 1, 8, 1e-6, None) == q.EINVAL  # NULL x
+    assert L.b200q_rmsnorm(16, None, None, 32, 48 + 4, 1, 8, 1e-6, None) == q.EINVAL    # misaligned y
+    assert L.b200q_rmsnorm(4096, None, None, 0x10000, 4096 + 16, 1, 8, 1e-6, None) == q.EINVAL   # y overlaps x
+    assert "overlap" in q.last_error()

@@ -45,6 +45,14 @@ MUTANTS = {
     "gate_up_same_tensor": ("return qref_matmul(fmt, O, I, codes_u, scales_u, x, S, yu, NULL, bound_u);",
                             "return qref_matmul(fmt, O, I, codes_g, scales_g, x, S, yu, NULL, bound_u);"),
     "y_rounded_before_scale": ("y[so] = (float)(sc * acc);", "y[so] = (float)(sc * (float)acc);"),
+    "rms_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)D + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
+    "rms_no_root": ("double inv = 1.0 / sqrt(ss / (double)D + eps);", "double inv = 1.0 / (ss / (double)D + eps);"),
+    "rms_eps_outside_root": ("double inv = 1.0 / sqrt(ss / (double)D + eps);",
+                             "double inv = 1.0 / (sqrt(ss / (double)D) + eps);"),
+    "rms_abs_not_square": ("ss += (double)hv * (double)hv;", "ss += fabs((double)hv);"),
+    "rms_weight_dropped": ("double v = (double)hv * (double)w[d] * inv;", "double v = (double)hv * inv;"),
+    "rms_residual_dropped": ("float hv = r ? (float)((double)x[s * D + d] + (double)r[s * D + d]) : x[s * D + d];\n            if (h)",
+                             "float hv = x[s * D + d];\n            if (h)"),
 }
 
 
