@@ -62,6 +62,8 @@ def _bind(path: str):
     L.qref_matmul_gate_up.restype = c_int
     L.qref_silu_mul.argtypes = [vp, vp, c_long, vp, vp]
     L.qref_silu_mul.restype = None
+    L.qref_matmul_gs.argtypes = [c_int, c_long, c_long, c_long, vp, vp, vp, c_long, vp, vp, vp]
+    L.qref_matmul_gs.restype = c_int
     L.qref_rmsnorm.argtypes = [vp, vp, vp, c_long, c_long, ctypes.c_double, vp, vp, vp]
     L.qref_rmsnorm.restype = c_int
     L.qref_round_bf16.argtypes = [ctypes.c_float]
@@ -162,6 +164,24 @@ def matmul(fmt: int, O: int, I: int, codes, scales, x, *, want_dbl: bool = False
                            _ptr(ydbl), _ptr(bound))
     if rc:
         raise ValueError("qref_matmul: bad argument")
+    return (y, bound, ydbl) if want_dbl else (y, bound)
+
+
+def matmul_gs(fmt: int, O: int, I: int, gs: int, codes, gscales, x, *, want_dbl: bool = False):
+    """Group-wise scales gscales [O, ceil(I / gs)]: returns (y f32 [S,O], bound
+    f64 [S,O]) or (y, bound, ydbl) with want_dbl."""
+    codes = _check_codes(fmt, O, I, codes)
+    G = -(-I // gs)
+    gscales = _f32(gscales).reshape(O, G)
+    x = _f32(x).reshape(-1, I)
+    S = x.shape[0]
+    y = np.empty((S, O), np.float32)
+    bound = np.empty((S, O), np.float64)
+    ydbl = np.empty((S, O), np.float64) if want_dbl else None
+    rc = _L().qref_matmul_gs(fmt, O, I, gs, _ptr(codes), _ptr(gscales), _ptr(x), S, _ptr(y),
+                             _ptr(ydbl), _ptr(bound))
+    if rc:
+        raise ValueError("qref_matmul_gs: bad argument")
     return (y, bound, ydbl) if want_dbl else (y, bound)
 
 

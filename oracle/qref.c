@@ -148,6 +148,52 @@ int qref_matmul(int fmt, long O, long I, const uint8_t *codes, const float *scal
 }
 
 /*
+ * Group-wise scales.  The Vulkan tensor of the three-backends chapter (section
+ * 三) carries a group size gs next to fmt; the pages say nothing more, so the
+ * plain reading is one scale per row and group of gs consecutive columns:
+ *     y[s,o] = sum_g gscales[o, g] * sum_{i in group g} deq(W[o,i]) * x[s,i]
+ * groups g = 0 .. G-1, G = ceil(I / gs), the last one possibly short;
+ * gscales is [O, G] row-major.  In double, one rounding at the end;
+ * bound[s,o] = sum_i |gscales[o, i / gs] * deq * x|.  Returns 0 or -1.
+ */
+int qref_matmul_gs(int fmt, long O, long I, long gs, const uint8_t *codes, const float *gscales,
+                   const float *x, long S, float *y, double *ydbl, double *bound)
+{
+    long rb = qref_row_bytes(fmt, I);
+    if (rb < 0 || O < 0 || S < 0 || gs < 1) return -1;
+    if (O == 0 || S == 0) return 0;
+    if (!codes || !gscales || !x || !y) return -1;
+    long G = (I + gs - 1) / gs;
+    long n = S * O;
+#ifdef _OPENMP
+    int nt = qref_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nt)
+#endif
+    for (long so = 0; so < n; ++so) {
+        long s = so / O, o = so % O;
+        const uint8_t *wrow = codes + o * rb;
+        const float *xrow = x + s * I;
+        double total = 0.0, bnd = 0.0;
+        for (long g = 0; g < G; ++g) {
+            double acc = 0.0, gb = 0.0;
+            long end = (g + 1) * gs < I ? (g + 1) * gs : I;
+            for (long i = g * gs; i < end; ++i) {
+                double p = qref_weight(fmt, wrow, i) * (double)xrow[i];
+                acc += p;
+                gb += fabs(p);
+            }
+            double sc = (double)gscales[o * G + g];
+            total += sc * acc;
+            bnd += fabs(sc) * gb;
+        }
+        y[so] = (float)total;
+        if (ydbl) ydbl[so] = total;
+        if (bound) bound[so] = bnd;
+    }
+    return 0;
+}
+
+/*
  * The fused gate/up pair (qmatmul_gate_up.comp in the three-backends chapter):
  * two matmuls of equal shape on the same input x.
  */

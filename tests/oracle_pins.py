@@ -271,6 +271,52 @@ def check_silu():
     assert np.array_equal(h, hd.astype(np.float32))
 
 
+def check_group_scales():
+    """Group-wise scales: one group is the per-row scale exactly; a hand-worked
+    group size 1; a short last group; per-group linearity; the bound."""
+    # gs = I: bit for bit the per-row matmul
+    c, sc = synth.quant_tensor(2, 5, 40, 0, 1, 5e-3, 2e-2)
+    x = synth.activations(3, 40, 0, 2)
+    y1, b1 = Q.matmul(2, 5, 40, c, sc, x)
+    y2, b2 = Q.matmul_gs(2, 5, 40, 40, c, sc.reshape(5, 1), x)
+    assert np.array_equal(y1, y2) and np.allclose(b1, b2, rtol=1e-15, atol=0)
+    # gs = 1, int8 codes [1, -2, 3], scales [0.5, 2, -1], x [2, 1, 4]:
+    # 0.5*1*2 + 2*(-2)*1 + (-1)*3*4 = -15, bound 1 + 4 + 12 = 17
+    codes = np.array([[1, 0xFE, 3]], np.uint8)
+    y, b, yd = Q.matmul_gs(1, 1, 3, 1, codes, np.array([[0.5, 2.0, -1.0]], np.float32),
+                           np.array([[2.0, 1.0, 4.0]], np.float32), want_dbl=True)
+    assert yd[0, 0] == -15.0 and b[0, 0] == 17.0
+    # int4, I = 5, gs = 2: groups {0, 1}, {2, 3}, {4}; codes 9, 10, 6, 8, 15 -> 1, 2, -2, 0, 7
+    codes = np.array([[0xA9, 0x86, 0x0F]], np.uint8)
+    gsc = np.array([[1.0, 0.25, -0.5]], np.float32)
+    xx = np.array([[1.0, 2.0, 3.0, 4.0, 2.0]], np.float32)
+    _, b, yd = Q.matmul_gs(2, 1, 5, 2, codes, gsc, xx, want_dbl=True)
+    # 1*(1*1 + 2*2) + 0.25*(-2*3 + 0*4) + (-0.5)*(7*2) = 5 - 1.5 - 7 = -3.5; bound 5 + 1.5 + 7
+    assert yd[0, 0] == -3.5 and b[0, 0] == 13.5
+    # doubling one group's scale adds exactly that group's contribution again
+    gs, I = 16, 70
+    c, _ = synth.quant_tensor(2, 3, I, 0, 3, 5e-3, 2e-2)
+    G = -(-I // gs)
+    gsc = synth.uniform_f32((3, G), 5e-3, 2e-2, 0, 4)
+    x = synth.activations(2, I, 0, 5)
+    _, _, y0 = Q.matmul_gs(2, 3, I, gs, c, gsc, x, want_dbl=True)
+    g2 = gsc.copy()
+    g2[:, 2] *= 2.0
+    _, _, y2 = Q.matmul_gs(2, 3, I, gs, c, g2, x, want_dbl=True)
+    only = np.zeros_like(gsc)
+    only[:, 2] = gsc[:, 2]
+    _, _, yg = Q.matmul_gs(2, 3, I, gs, c, only, x, want_dbl=True)
+    assert np.allclose(y2 - y0, yg, rtol=1e-12, atol=1e-18)
+    # the last (short) group matters: zeroing its scale removes element 64..69
+    z = gsc.copy()
+    z[:, G - 1] = 0.0
+    _, _, yz = Q.matmul_gs(2, 3, I, gs, c, z, x, want_dbl=True)
+    lastonly = np.zeros_like(gsc)
+    lastonly[:, G - 1] = gsc[:, G - 1]
+    _, _, yl = Q.matmul_gs(2, 3, I, gs, c, lastonly, x, want_dbl=True)
+    assert np.allclose(y0 - yz, yl, rtol=1e-12, atol=1e-18) and np.any(yl != 0)
+
+
 def check_rmsnorm():
     """RMSNorm (textbook, the pages name it without printing it): a worked
     example by hand, closed forms, the residual sum, the eps term, row

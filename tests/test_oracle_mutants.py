@@ -45,6 +45,9 @@ MUTANTS = {
     "gate_up_same_tensor": ("return qref_matmul(fmt, O, I, codes_u, scales_u, x, S, yu, NULL, bound_u);",
                             "return qref_matmul(fmt, O, I, codes_g, scales_g, x, S, yu, NULL, bound_u);"),
     "y_rounded_before_scale": ("y[so] = (float)(sc * acc);", "y[so] = (float)(sc * (float)acc);"),
+    "gs_first_scale_only": ("double sc = (double)gscales[o * G + g];", "double sc = (double)gscales[o * G];"),
+    "gs_bound_unscaled": ("bnd += fabs(sc) * gb;", "bnd += gb;"),
+    "gs_short_group_dropped": ("long G = (I + gs - 1) / gs;", "long G = I / gs;"),
     "rms_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)D + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
     "rms_no_root": ("double inv = 1.0 / sqrt(ss / (double)D + eps);", "double inv = 1.0 / (ss / (double)D + eps);"),
     "rms_eps_outside_root": ("double inv = 1.0 / sqrt(ss / (double)D + eps);",
