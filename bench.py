@@ -204,7 +204,7 @@ def job_throughput(bytes_per_rank_step, steps, world, ms_max):
 class Decode:
     """R distinct resident [O, I] tensors, S tokens: one step = R matmul calls."""
 
-    def __init__(self, q, fmt, O, I, S, R, seed=0):
+    def __init__(self, q, fmt, O, I, S, R, seed=0, gs=0):
         import torch
         import synth
         self.q, self.fmt, self.O, self.I, self.S, self.R = q, fmt, O, I, S, R
@@ -212,12 +212,14 @@ class Decode:
         lo, hi = {0: (1e-3, 2e-2), 1: (1e-3, 1e-2), 2: (5e-3, 2e-2), 3: (1e-3, 2e-2)}[fmt]
         for r in range(R):
             codes, scales = synth.quant_tensor(fmt, O, I, seed, 1 + r, lo, hi)
-            self.tensors.append(q.tensor_upload(fmt, O, I, codes, scales))
+            if gs:                      # group-wise scales, [O, ceil(I / gs)]
+                scales = synth.uniform_f32((O, -(-I // gs)), lo, hi, seed, 500 + r)
+            self.tensors.append(q.tensor_upload(fmt, O, I, codes, scales, gs=gs))
         x = synth.activations(S, I, seed, 9999)
         self.x = torch.from_numpy(x).cuda()
         self.y = torch.empty((R, S, O), dtype=torch.float32, device="cuda")
         bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
-        self.bytes_per_call = algorithmic_bytes(bits, O, I, S)
+        self.bytes_per_call = algorithmic_bytes(bits, O, I, S) + (4 * O * (-(-I // gs) - 1) if gs else 0)
         self.bytes_per_step = self.bytes_per_call * R
         self.flops_per_step = 2.0 * O * I * S * R
         self.launches_per_step = None
@@ -453,11 +455,13 @@ def run_sweep(args):
     cases += [("int4 12288x6144", I4, 12288, 6144, s) for s in (1, 4)]
     cases += [("%s 8192x8192" % n, f, 8192, 8192, s) for n, f in (("f32", 0), ("int8", 1), ("int4", 2), ("int2", 3))
               for s in (1, 2, 8)]
-    for name, fmt, O, I, S in cases:
+    cases = [c + (0,) for c in cases] + [("int4 12288x6144 gs=128", I4, 12288, 6144, 1, 128),
+                                         ("int4 12288x6144 gs=128", I4, 12288, 6144, 4, 128)]
+    for name, fmt, O, I, S, gs in cases:
         bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
         per = algorithmic_bytes(bits, O, I, S)
         R = max(2, min(64, -(-3 * L2_BYTES // per)))
-        wl = Decode(q, fmt, O, I, S, R)
+        wl = Decode(q, fmt, O, I, S, R, gs=gs)
         ms, launches = time_steps(wl, args.steps, args.warmup, stream)
         gbs = wl.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
         print(json.dumps({"workload": "%s S=%d" % (name, S), "GB/s": round(gbs, 1),

@@ -96,6 +96,26 @@ enum { B200Q_PATH_AUTO = 0, B200Q_PATH_F32 = 1, B200Q_PATH_TC = 2, B200Q_PATH_TC
 b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, const float *scales);
 
 /*
+ * As b200q_tensor_upload with group-wise scales: one scale per row and group
+ * of gs consecutive columns, the group size the Vulkan tensor carries next to
+ * fmt (three-backends chapter, section 三; the pages say nothing more, so this
+ * is the plain reading):
+ *     y[s,o] = sum_g scales[o, g] * sum_{i in group g} deq(W[o,i]) * x[s,i]
+ *   gs      group size: a multiple of a 16-byte chunk's element count (4 f32,
+ *           16 int8, 32 int4, 64 int2), or 16 or 32 where that divides it;
+ *           B200Q_EINVAL otherwise
+ *   scales  HOST pointer to [O, ceil(I / gs)] floats, row-major; the last
+ *           group of a row may be short
+ * Such tensors run on the f32 path's SIMT kernel at every S (the bound is
+ * taken with the group scales); the tensor-core paths and
+ * b200q_matmul_tc_noalloc refuse them (B200Q_EINVAL).
+ */
+b200q_tensor *b200q_tensor_upload_grouped(int fmt, int O, int I, int gs, const void *codes, const float *scales);
+
+/* Group size of a tensor's scales (0: one scale per row), or a negative status. */
+int b200q_tensor_group_size(const b200q_tensor *t);
+
+/*
  * Free a tensor (counterpart of coli_cuda_tensor_free).  NULL is a no-op.
  * The caller must make sure no queued kernel still reads the tensor.
  */

@@ -39,6 +39,10 @@ def _load():
     vp, ci, cl, cll, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_longlong, ctypes.c_float
     L.b200q_tensor_upload.argtypes = [ci, ci, ci, vp, vp]
     L.b200q_tensor_upload.restype = vp
+    L.b200q_tensor_upload_grouped.argtypes = [ci, ci, ci, ci, vp, vp]
+    L.b200q_tensor_upload_grouped.restype = vp
+    L.b200q_tensor_group_size.argtypes = [vp]
+    L.b200q_tensor_group_size.restype = ci
     L.b200q_tensor_free.argtypes = [vp]
     L.b200q_tensor_free.restype = None
     L.b200q_matmul.argtypes = [vp, vp, vp, ci, vp]
@@ -161,26 +165,40 @@ def _h(t) -> int:
     return t.handle if isinstance(t, QTensor) else t
 
 
-def tensor_upload(fmt: int, O: int, I: int, codes, scales) -> QTensor:
+def tensor_upload(fmt: int, O: int, I: int, codes, scales, gs: int = 0) -> QTensor:
     """Upload host codes ([O, row_bytes] uint8, or f32 [O, I] for fmt F32) and
-    host scales (f32 [O], or None for F32) to the current device."""
+    host scales (f32 [O], or None for F32; with gs >= 1 group-wise scales
+    [O, ceil(I / gs)]) to the current device."""
     codes = np.ascontiguousarray(codes)
     if codes.dtype != np.uint8:
         codes = codes.view(np.uint8)
+    n_scales = O * (-(-I // gs) if gs else 1)
     if scales is not None:
         scales = np.ascontiguousarray(scales, dtype=np.float32)
-        if scales.size != O:
-            raise ValueError("scales must hold O floats")
+        if scales.size != n_scales:
+            raise ValueError("scales must hold %d floats" % n_scales)
     bits = {F32: 32, I8: 8, I4: 4, I2: 2}.get(fmt)
     if bits is not None and codes.size != O * ((I * bits + 7) // 8):
         raise ValueError("codes hold %d bytes, expected O * row_bytes = %d"
                          % (codes.size, O * ((I * bits + 7) // 8)))
-    h = lib.b200q_tensor_upload(fmt, O, I, codes.ctypes.data,
-                                None if scales is None else scales.ctypes.data)
+    sp = None if scales is None else scales.ctypes.data
+    if gs:
+        h = lib.b200q_tensor_upload_grouped(fmt, O, I, gs, codes.ctypes.data, sp)
+    else:
+        h = lib.b200q_tensor_upload(fmt, O, I, codes.ctypes.data, sp)
     if not h:
         msg = last_error()
         raise B200QError(ENOMEM if "memory" in msg else EINVAL, msg)
     return QTensor(h, fmt, O, I)
+
+
+def tensor_upload_grouped(fmt: int, O: int, I: int, gs: int, codes, scales) -> QTensor:
+    """tensor_upload with group-wise scales (b200q_tensor_upload_grouped)."""
+    return tensor_upload(fmt, O, I, codes, scales, gs=gs)
+
+
+def tensor_group_size(t) -> int:
+    return _check(lib.b200q_tensor_group_size(_h(t)))
 
 
 def tensor_free(t) -> None:

@@ -125,7 +125,7 @@ int tcx_min_s() {
 // rows, the SIMT f32 path below; f32 and int2 tensors always the SIMT path.
 int select_path(const Tensor &t, int S, int path) {
     if (path != B200Q_PATH_AUTO) return path;
-    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return B200Q_PATH_F32;
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8 || t.gs) return B200Q_PATH_F32;
     if (S >= tc_min_s()) return B200Q_PATH_TC;
     if (S >= tcx_min_s()) return B200Q_PATH_TCX;
     return B200Q_PATH_F32;
@@ -140,12 +140,15 @@ int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, floa
     if (path == B200Q_PATH_TC || path == B200Q_PATH_TCX) {
         if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
             return fail(B200Q_EINVAL, "%s: the tensor-core paths take int8 and int4 tensors only", who);
+        if (t.gs || (tu && tu->gs))
+            return fail(B200Q_EINVAL, "%s: tensors with group-wise scales run on the f32 path only", who);
         e = path == B200Q_PATH_TC ? launch_prefill_tc(t, tu, x, y, yu, S, st, &handled)
                                   : launch_tcx(t, tu, x, y, yu, S, st, &handled);
         if (e == cudaSuccess && !handled)
             return fail(B200Q_ECUDA, "%s: no tensor-core kernel for this shape", who);
     } else {
-        e = launch_decode(t, tu, x, y, yu, S, st, &handled);
+        // group-wise scales: the general SIMT kernel
+        if (!t.gs && !(tu && tu->gs)) e = launch_decode(t, tu, x, y, yu, S, st, &handled);
         if (e == cudaSuccess && !handled) e = launch_qmv_simt(t, tu, x, y, yu, S, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, who);
@@ -177,39 +180,51 @@ int b200q_tc_min_s(void) { return tc_min_s(); }
 
 int b200q_tcx_min_s(void) { return tcx_min_s(); }
 
-b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, const float *scales) {
+}  // extern "C"
+
+namespace {
+
+// One upload for both scale layouts: gs = 0, one scale per row; gs >= 1, one
+// per row and group of gs columns ([O, ceil(I / gs)] host floats).
+b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, const float *scales, const char *who) {
     g_err.clear();
     if (fmt_bits(fmt) == 0) {
-        fail(B200Q_EINVAL, "b200q_tensor_upload: unknown format %d", fmt);
+        fail(B200Q_EINVAL, "%s: unknown format %d", who, fmt);
         return nullptr;
     }
     if (O <= 0 || I <= 0) {
-        fail(B200Q_EINVAL, "b200q_tensor_upload: O and I must be > 0 (got O=%d, I=%d)", O, I);
+        fail(B200Q_EINVAL, "%s: O and I must be > 0 (got O=%d, I=%d)", who, O, I);
         return nullptr;
     }
     if (!codes) {
-        fail(B200Q_EINVAL, "b200q_tensor_upload: codes is NULL");
+        fail(B200Q_EINVAL, "%s: codes is NULL", who);
         return nullptr;
     }
-    if (!scales && fmt != B200Q_F32) {
-        fail(B200Q_EINVAL, "b200q_tensor_upload: scales are required for quantized formats");
+    if (!scales && (fmt != B200Q_F32 || gs)) {
+        fail(B200Q_EINVAL, "%s: scales are required for quantized formats and group-wise scales", who);
+        return nullptr;
+    }
+    if (gs && !group_size_ok(fmt, gs)) {
+        fail(B200Q_EINVAL,
+             "%s: group size %d not supported for this format (a multiple of %d elements, or 16 / 32 dividing it)",
+             who, gs, fmt == B200Q_F32 ? 4 : fmt == B200Q_I8 ? 16 : fmt == B200Q_I4 ? 32 : 64);
         return nullptr;
     }
     if (const char *fi = std::getenv("B200Q_FAULT_INJECT")) {
         if (std::strcmp(fi, "alloc") == 0) {
-            fail(B200Q_ENOMEM, "b200q_tensor_upload: out of device memory (injected by B200Q_FAULT_INJECT)");
+            fail(B200Q_ENOMEM, "%s: out of device memory (injected by B200Q_FAULT_INJECT)", who);
             return nullptr;
         }
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
-        cuda_fail(e, "b200q_tensor_upload: cudaGetDevice");
+        cuda_fail(e, who);
         return nullptr;
     }
     Tensor *t = new (std::nothrow) Tensor();
     if (!t) {
-        fail(B200Q_ENOMEM, "b200q_tensor_upload: out of host memory");
+        fail(B200Q_ENOMEM, "%s: out of host memory", who);
         return nullptr;
     }
     const long long rb = host_row_bytes(fmt, I);
@@ -220,12 +235,14 @@ b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, cons
     t->o_pad = (O + kRowTile - 1) / kRowTile * kRowTile;
     t->ld = (rb + kRowAlign - 1) / kRowAlign * kRowAlign;
     t->k_pad = t->ld * 8 / fmt_bits(fmt);
+    t->gs = gs;
+    t->G = gs ? (I + gs - 1) / gs : 1;
     const size_t code_bytes = (size_t)t->o_pad * t->ld;
-    t->bytes = code_bytes + (size_t)t->o_pad * sizeof(float);
+    t->bytes = code_bytes + (size_t)t->o_pad * t->G * sizeof(float);
     void *mem = nullptr;
     e = cudaMalloc(&mem, t->bytes);
     if (e != cudaSuccess) {
-        cuda_fail(e, "b200q_tensor_upload: cudaMalloc");
+        cuda_fail(e, who);
         cudaGetLastError();
         delete t;
         return nullptr;
@@ -236,7 +253,7 @@ b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, cons
     cudaStream_t st = nullptr;
     e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaMemsetAsync(t->codes, zero_byte(fmt), code_bytes, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(t->scales, 0, (size_t)t->o_pad * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(t->scales, 0, (size_t)t->o_pad * t->G * sizeof(float), st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e == cudaSuccess)
         e = cudaMemcpy2DAsync(t->codes, (size_t)t->ld, codes, (size_t)rb, (size_t)rb, (size_t)O,
@@ -244,7 +261,7 @@ b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, cons
     if (e == cudaSuccess) e = launch_fix_row_tails(*t, rb, st);
     if (e == cudaSuccess) {
         if (scales) {
-            e = cudaMemcpyAsync(t->scales, scales, (size_t)O * sizeof(float), cudaMemcpyHostToDevice, st);
+            e = cudaMemcpyAsync(t->scales, scales, (size_t)O * t->G * sizeof(float), cudaMemcpyHostToDevice, st);
         } else {
             // f32 without scales: 1.0 for every real row (0x3f800000 as four bytes is not a
             // memset pattern, so copy from a host vector)
@@ -267,13 +284,35 @@ b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, cons
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         e = cudaErrorNotSupported;
     if (e != cudaSuccess) {
-        cuda_fail(e, "b200q_tensor_upload: copy");
+        cuda_fail(e, who);
         cudaGetLastError();
         cudaFree(mem);
         delete t;
         return nullptr;
     }
     return reinterpret_cast<b200q_tensor *>(t);
+}
+
+}  // namespace
+
+extern "C" {
+
+b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, const float *scales) {
+    return upload_impl(fmt, O, I, 0, codes, scales, "b200q_tensor_upload");
+}
+
+b200q_tensor *b200q_tensor_upload_grouped(int fmt, int O, int I, int gs, const void *codes, const float *scales) {
+    if (gs < 1) {
+        g_err.clear();
+        fail(B200Q_EINVAL, "b200q_tensor_upload_grouped: group size must be >= 1 (got %d)", gs);
+        return nullptr;
+    }
+    return upload_impl(fmt, O, I, gs, codes, scales, "b200q_tensor_upload_grouped");
+}
+
+int b200q_tensor_group_size(const b200q_tensor *h) {
+    if (!h) return fail(B200Q_EINVAL, "b200q_tensor_group_size: tensor is NULL");
+    return reinterpret_cast<const Tensor *>(h)->gs;
 }
 
 void b200q_tensor_free(b200q_tensor *h) {
@@ -329,8 +368,8 @@ int b200q_matmul_gate_up(const b200q_tensor *hg, const b200q_tensor *hu, const f
     if (rc) return rc;
     const Tensor &tg = *reinterpret_cast<const Tensor *>(hg);
     const Tensor &tu = *reinterpret_cast<const Tensor *>(hu);
-    if (tg.fmt != tu.fmt || tg.O != tu.O || tg.I != tu.I)
-        return fail(B200Q_EINVAL, "b200q_matmul_gate_up: gate and up differ in format or shape");
+    if (tg.fmt != tu.fmt || tg.O != tu.O || tg.I != tu.I || tg.gs != tu.gs)
+        return fail(B200Q_EINVAL, "b200q_matmul_gate_up: gate and up differ in format, shape or group size");
     if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_gate_up: S must be >= 0 (got %d)", S);
     if (S == 0) return B200Q_OK;
     rc = check_io(tg, x, yg, S, "b200q_matmul_gate_up");
@@ -386,7 +425,9 @@ int run_group(const b200q_tensor *const *hs, int n, const float *const *xa, cons
     const bool silu = xb != nullptr;
     // below the bf16 tensor-core threshold the whole group is one decode launch
     // per two rows; from it, each tensor runs its own tensor-core call
-    if (select_path(*ts[0], S, B200Q_PATH_AUTO) != B200Q_PATH_TC) {
+    bool any_gs = false;
+    for (int j = 0; j < n; ++j) any_gs |= ts[j]->gs != 0;
+    if (!any_gs && select_path(*ts[0], S, B200Q_PATH_AUTO) != B200Q_PATH_TC) {
         bool handled = false;
         cudaError_t e = launch_decode_group(ts, n, xa, xb, ys, silu, S, st, &handled);
         if (e != cudaSuccess) return cuda_fail(e, who);
@@ -434,8 +475,8 @@ int b200q_matmul_tc_noalloc(const b200q_tensor *h, const float *x, float *y, int
     int rc = check_tensor(h, "b200q_matmul_tc_noalloc");
     if (rc) return rc;
     const Tensor &t = *reinterpret_cast<const Tensor *>(h);
-    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
-        return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: takes int8 and int4 tensors only");
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8 || t.gs)
+        return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: takes int8 and int4 tensors with per-row scales only");
     if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: S must be >= 0 (got %d)", S);
     if (S == 0) return B200Q_OK;
     const size_t need = (size_t)S * (size_t)t.k_pad * 2;

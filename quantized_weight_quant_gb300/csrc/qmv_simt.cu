@@ -11,9 +11,15 @@
 // more than (elements per chunk + chunks per lane) terms.  The 32 lane sums
 // are combined with shuffles and the scale is applied once per row.
 //
-// This kernel is the general path (f32 weights, int2, every S); the int4 /
-// int8 decode kernels and the tensor-core prefill kernel are faster on
-// their shapes.
+// Group-wise scales (one scale per row and group of gs columns, the group
+// size of the Vulkan tensor in the three-backends chapter, section 三): the
+// chunk-local sum is scaled by its group's scale before it joins the lane's
+// sum (gs a multiple of the chunk's element count), or the chunk is split into
+// groups of 16 or 32 elements, each summed and scaled on its own.
+//
+// This kernel is the general path (f32 weights, int2, every S, group-wise
+// scales); the decode kernels and the tensor-core kernels are faster on their
+// shapes.
 #include "qwq_internal.h"
 
 namespace qwq {
@@ -78,15 +84,21 @@ struct Deq<B200Q_I2> {
 
 struct RowSet {
     const uint8_t *codes;
-    const float *scales;
+    const float *scales;   // [O] per row, or [O, G] per row and group
     float *y;
+    int gs;                // 0: per-row scales
+    int G;                 // groups per row
 };
 
-template <int FMT>
+// SUB = 0: per-row scales, or groups that are whole chunks (gs a multiple of
+// the chunk's element count); SUB = 16 or 32: groups of SUB elements inside
+// a chunk.
+template <int FMT, int SUB>
 __global__ void __launch_bounds__(kWarps * 32)
 qmv_simt_kernel(RowSet a, RowSet b, int n_sets, int O, int I, long long ld, const float *__restrict__ x,
                 int S) {
     using D = Deq<FMT>;
+    static_assert(SUB == 0 || D::kPerChunk % SUB == 0, "groups inside a chunk");
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int s0 = blockIdx.y * kTok;
@@ -110,18 +122,44 @@ qmv_simt_kernel(RowSet a, RowSet b, int n_sets, int O, int I, long long ld, cons
             float w[D::kPerChunk];
             D::run(raw, w);
             const int kn = (int)min((long long)D::kPerChunk, (long long)I - k0);
+            if constexpr (SUB == 0) {
+                // per-row scale (applied at the end), or the chunk's group scale
+                const float gsc = rs.gs ? rs.scales[(long long)o * rs.G + k0 / rs.gs] : 1.f;
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) {
-                if (t < ns) {
-                    const float *xs = x + (long long)(s0 + t) * I + k0;
-                    float part = 0.f;
-                    if (kn == D::kPerChunk) {
+                for (int t = 0; t < kTok; ++t) {
+                    if (t < ns) {
+                        const float *xs = x + (long long)(s0 + t) * I + k0;
+                        float part = 0.f;
+                        if (kn == D::kPerChunk) {
 #pragma unroll
-                        for (int j = 0; j < D::kPerChunk; ++j) part = fmaf(w[j], __ldg(xs + j), part);
-                    } else {
-                        for (int j = 0; j < kn; ++j) part = fmaf(w[j], __ldg(xs + j), part);
+                            for (int j = 0; j < D::kPerChunk; ++j) part = fmaf(w[j], __ldg(xs + j), part);
+                        } else {
+                            for (int j = 0; j < kn; ++j) part = fmaf(w[j], __ldg(xs + j), part);
+                        }
+                        acc[t] = rs.gs ? fmaf(part, gsc, acc[t]) : acc[t] + part;
                     }
-                    acc[t] += part;
+                }
+            } else {
+                // groups of SUB elements: each summed, scaled and added on its own
+                const float *gsc = rs.scales + (long long)o * rs.G + k0 / SUB;
+#pragma unroll
+                for (int t = 0; t < kTok; ++t) {
+                    if (t < ns) {
+                        const float *xs = x + (long long)(s0 + t) * I + k0;
+#pragma unroll
+                        for (int g = 0; g < D::kPerChunk / SUB; ++g) {
+                            float part = 0.f;
+                            if (kn == D::kPerChunk) {
+#pragma unroll
+                                for (int j = 0; j < SUB; ++j) part = fmaf(w[g * SUB + j], __ldg(xs + g * SUB + j), part);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < SUB; ++j)
+                                    if (g * SUB + j < kn) part = fmaf(w[g * SUB + j], __ldg(xs + g * SUB + j), part);
+                            }
+                            if (g * SUB < kn) acc[t] = fmaf(part, gsc[g], acc[t]);
+                        }
+                    }
                 }
             }
         }
@@ -131,10 +169,10 @@ qmv_simt_kernel(RowSet a, RowSet b, int n_sets, int O, int I, long long ld, cons
             for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
         }
         if (lane == 0) {
-            const float sc = rs.scales[o];
+            const float sc = rs.gs ? 1.f : rs.scales[o];
 #pragma unroll
             for (int t = 0; t < kTok; ++t)
-                if (t < ns) rs.y[(long long)(s0 + t) * O + o] = sc * acc[t];
+                if (t < ns) rs.y[(long long)(s0 + t) * O + o] = rs.gs ? acc[t] : sc * acc[t];
         }
     }
 }
@@ -283,8 +321,8 @@ cudaError_t launch_fix_row_tails(const Tensor &t, long long rb, cudaStream_t st)
 
 cudaError_t launch_qmv_simt(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
                             cudaStream_t st) {
-    RowSet a{t.codes, t.scales, y};
-    RowSet b = tu ? RowSet{tu->codes, tu->scales, yu} : a;
+    RowSet a{t.codes, t.scales, y, t.gs, t.G};
+    RowSet b = tu ? RowSet{tu->codes, tu->scales, yu, tu->gs, tu->G} : a;
     const int n_sets = tu ? 2 : 1;
     const long long rows = (long long)t.O * n_sets;
     const int tok_blocks = (S + kTok - 1) / kTok;
@@ -293,13 +331,26 @@ cudaError_t launch_qmv_simt(const Tensor &t, const Tensor *tu, const float *x, f
     const int gx = (int)(want < cap ? want : cap);
     if (tok_blocks > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(gx, tok_blocks);
+    // groups smaller than a chunk (16 or 32 elements) take the split variant
+    const int per_chunk = t.fmt == B200Q_F32 ? 4 : t.fmt == B200Q_I8 ? 16 : t.fmt == B200Q_I4 ? 32 : 64;
+    const int sub = (t.gs && t.gs < per_chunk) ? t.gs : 0;
+    if (sub != 0 && sub != 16 && sub != 32) return cudaErrorInvalidValue;
+#define QWQ_SIMT(F, SB) qmv_simt_kernel<F, SB><<<grid, kWarps * 32, 0, st>>>(a, b, n_sets, t.O, t.I, t.ld, x, S)
     switch (t.fmt) {
-    case B200Q_F32: qmv_simt_kernel<B200Q_F32><<<grid, kWarps * 32, 0, st>>>(a, b, n_sets, t.O, t.I, t.ld, x, S); break;
-    case B200Q_I8: qmv_simt_kernel<B200Q_I8><<<grid, kWarps * 32, 0, st>>>(a, b, n_sets, t.O, t.I, t.ld, x, S); break;
-    case B200Q_I4: qmv_simt_kernel<B200Q_I4><<<grid, kWarps * 32, 0, st>>>(a, b, n_sets, t.O, t.I, t.ld, x, S); break;
-    case B200Q_I2: qmv_simt_kernel<B200Q_I2><<<grid, kWarps * 32, 0, st>>>(a, b, n_sets, t.O, t.I, t.ld, x, S); break;
+    case B200Q_F32: QWQ_SIMT(B200Q_F32, 0); break;
+    case B200Q_I8: QWQ_SIMT(B200Q_I8, 0); break;
+    case B200Q_I4:
+        if (sub == 16) QWQ_SIMT(B200Q_I4, 16);
+        else QWQ_SIMT(B200Q_I4, 0);
+        break;
+    case B200Q_I2:
+        if (sub == 16) QWQ_SIMT(B200Q_I2, 16);
+        else if (sub == 32) QWQ_SIMT(B200Q_I2, 32);
+        else QWQ_SIMT(B200Q_I2, 0);
+        break;
     default: return cudaErrorInvalidValue;
     }
+#undef QWQ_SIMT
     count_launch();
     return cudaGetLastError();
 }

@@ -26,9 +26,19 @@ struct Tensor {
     long long ld;     // device row stride in bytes
     long long k_pad;  // elements per padded row = ld * 8 / bits
     uint8_t *codes;
-    float *scales;
+    float *scales;    // [o_pad] per row, or [o_pad, G] per row and group
     size_t bytes;     // one allocation: codes then scales
+    int gs;           // group size of the scales; 0: one scale per row
+    int G;            // scales per row (1, or ceil(I / gs))
 };
+
+// Group sizes the kernels take: a multiple of a 16-byte chunk's element
+// count (4 f32, 16 int8, 32 int4, 64 int2), or 16 or 32 dividing it.
+inline bool group_size_ok(int fmt, int gs) {
+    const int per = fmt == B200Q_F32 ? 4 : fmt == B200Q_I8 ? 16 : fmt == B200Q_I4 ? 32 : fmt == B200Q_I2 ? 64 : 0;
+    if (per == 0 || gs < 1) return false;
+    return gs % per == 0 || ((gs == 16 || gs == 32) && per % gs == 0);
+}
 
 constexpr int kRowAlign = 128;  // bytes; rows start on 128-byte boundaries
 constexpr int kRowTile = 128;   // O is padded to a multiple of this
