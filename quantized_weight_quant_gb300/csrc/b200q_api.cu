@@ -147,8 +147,7 @@ int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, floa
         if (e == cudaSuccess && !handled)
             return fail(B200Q_ECUDA, "%s: no tensor-core kernel for this shape", who);
     } else {
-        // group-wise scales: the general SIMT kernel
-        if (!t.gs && !(tu && tu->gs)) e = launch_decode(t, tu, x, y, yu, S, st, &handled);
+        e = launch_decode(t, tu, x, y, yu, S, st, &handled);
         if (e == cudaSuccess && !handled) e = launch_qmv_simt(t, tu, x, y, yu, S, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, who);
@@ -237,8 +236,28 @@ b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, cons
     t->k_pad = t->ld * 8 / fmt_bits(fmt);
     t->gs = gs;
     t->G = gs ? (I + gs - 1) / gs : 1;
+    t->G_ld = 1;
+    t->sc_box = 0;
+    if (gs) {
+        // a decode stage holds 32 chunks of a row (32 * per-chunk elements);
+        // its group scales are copied from the first group rounded down to a
+        // multiple of 4 (16 bytes), so take the widest such span over stages
+        const long long seg_elems = 32LL * (128 / fmt_bits(fmt));
+        const long long nseg = (t->ld + 511) / 512;
+        long long span = 1;
+        for (long long sg = 0; sg < nseg; ++sg) {
+            const long long lo = (sg * seg_elems / gs) & ~3LL;
+            const long long end = (sg + 1) * seg_elems < t->k_pad ? (sg + 1) * seg_elems : t->k_pad;
+            const long long hi = (end - 1) / gs;
+            if (hi - lo + 1 > span) span = hi - lo + 1;
+        }
+        t->sc_box = (int)((span + 3) & ~3LL);
+        t->G_ld = (t->G + 3) & ~3;
+        if (t->G_ld < t->sc_box) t->G_ld = t->sc_box;
+    }
     const size_t code_bytes = (size_t)t->o_pad * t->ld;
-    t->bytes = code_bytes + (size_t)t->o_pad * t->G * sizeof(float);
+    const size_t scale_bytes = (size_t)t->o_pad * t->G_ld * sizeof(float);
+    t->bytes = code_bytes + scale_bytes;
     void *mem = nullptr;
     e = cudaMalloc(&mem, t->bytes);
     if (e != cudaSuccess) {
@@ -253,7 +272,7 @@ b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, cons
     cudaStream_t st = nullptr;
     e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaMemsetAsync(t->codes, zero_byte(fmt), code_bytes, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(t->scales, 0, (size_t)t->o_pad * t->G * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(t->scales, 0, scale_bytes, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e == cudaSuccess)
         e = cudaMemcpy2DAsync(t->codes, (size_t)t->ld, codes, (size_t)rb, (size_t)rb, (size_t)O,
@@ -261,7 +280,8 @@ b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, cons
     if (e == cudaSuccess) e = launch_fix_row_tails(*t, rb, st);
     if (e == cudaSuccess) {
         if (scales) {
-            e = cudaMemcpyAsync(t->scales, scales, (size_t)O * t->G * sizeof(float), cudaMemcpyHostToDevice, st);
+            e = cudaMemcpy2DAsync(t->scales, (size_t)t->G_ld * sizeof(float), scales, (size_t)t->G * sizeof(float),
+                                  (size_t)t->G * sizeof(float), (size_t)O, cudaMemcpyHostToDevice, st);
         } else {
             // f32 without scales: 1.0 for every real row (0x3f800000 as four bytes is not a
             // memset pattern, so copy from a host vector)
@@ -281,6 +301,11 @@ b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, cons
     if (e == cudaSuccess &&
         !tmap_encode_2d(&t->dec_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, t->codes, (uint64_t)(t->ld / 4),
                         (uint64_t)t->o_pad, (uint64_t)t->ld, (uint32_t)(t->ld < 512 ? t->ld / 4 : 128), 8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        e = cudaErrorNotSupported;
+    if (e == cudaSuccess && gs &&
+        !tmap_encode_2d(&t->sc_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, t->scales, (uint64_t)t->G_ld,
+                        (uint64_t)t->o_pad, (uint64_t)t->G_ld * sizeof(float), (uint32_t)t->sc_box, 8,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         e = cudaErrorNotSupported;
     if (e != cudaSuccess) {
@@ -425,9 +450,7 @@ int run_group(const b200q_tensor *const *hs, int n, const float *const *xa, cons
     const bool silu = xb != nullptr;
     // below the bf16 tensor-core threshold the whole group is one decode launch
     // per two rows; from it, each tensor runs its own tensor-core call
-    bool any_gs = false;
-    for (int j = 0; j < n; ++j) any_gs |= ts[j]->gs != 0;
-    if (!any_gs && select_path(*ts[0], S, B200Q_PATH_AUTO) != B200Q_PATH_TC) {
+    if (select_path(*ts[0], S, B200Q_PATH_AUTO) != B200Q_PATH_TC) {
         bool handled = false;
         cudaError_t e = launch_decode_group(ts, n, xa, xb, ys, silu, S, st, &handled);
         if (e != cudaSuccess) return cuda_fail(e, who);

@@ -60,6 +60,10 @@ namespace qwq {
 namespace {
 
 constexpr int kMaxWarps = 15;
+// Consumer warps of a variant: two tokens with group-wise scales hold a
+// second set of sums, so those variants run fewer, larger threads (no spills).
+template <int NS, int GW>
+constexpr int max_warps() { return NS == 2 && GW ? 11 : kMaxWarps; }
 constexpr int kMaxSets = B200Q_GROUP_MAX;  // tensors per launch
 constexpr int kSeg = 512;            // bytes per row per stage: 32 lanes x 16 B
 constexpr int kStage = 8 * kSeg;     // one stage: 8 rows x 512 B (one TMA box)
@@ -289,6 +293,7 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv &f) {
 template <int MS>
 struct DecParams {
     CUtensorMap map[MS];      // decode tensor map of each set
+    CUtensorMap smap[MS];     // group-scale tensor map of each set (group-wise scales)
     const float *scales[MS];
     float *y[MS];             // [S, O[j]] per set, at this launch's first token
     const float *xa[MS];      // per x slot: x, or g when silu(g) * u is staged
@@ -306,15 +311,24 @@ struct DecParams {
     int depth;                // stages per warp
     int round_rgs;            // row groups combined per round (partials buffer rows)
     int nx_max;               // most x slots any CTA stages (shared-memory layout)
+    int gbox;                 // group scales per row in a stage (group-wise scales)
     FastDiv div_grid, div_nw, div_nseg;   // by gridDim.x, the consumer warps, the segments per row
+    FastDiv div_gs;           // by the group size (group-wise scales)
 };
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int FMT, int NS, int MS>
-__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
+// GW = 0: one scale per row, applied once per output.  GW > 0: group-wise
+// scales; a group spans GW 32-bit words of a 16-byte chunk (GW = 1 or 2), or
+// whole chunks (GW = 4).  Each lane then sums every group's products on their
+// own (zero point taken out as above), multiplies the group sum by the group's
+// scale and adds it to the row's sum; the producer copies each stage's
+// scales (8 rows x gbox, from a 4-aligned first group) next to its codes.
+template <int FMT, int NS, int MS, int GW>
+__global__ void __launch_bounds__((max_warps<NS, GW>() + 1) * 32, 1)
     qmv_decode_kernel(const __grid_constant__ DecParams<MS> p) {
     constexpr int E = F<FMT>::E;
+    constexpr int SEGE = (kSeg / 16) * E;            // elements of a row in one stage
     constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
     constexpr int EW = 32 / bits;                    // elements per 32-bit word
     constexpr int NV = 8 * NS;                       // partial sums per lane and row group
@@ -330,13 +344,15 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
     // addresses every lane slot of a segment), or k_pad for f32
     const int k_alloc = FMT == B200Q_F32 ? p.k_pad : nseg * (kSeg / 4) * EW;
     const int nxr = p.nx_max * NS;                    // staged x rows (slot-major)
+    const int scb = GW ? 32 * p.gbox : 0;             // group-scale bytes per stage (8 rows x gbox f32)
+    const int stg = kStage + scb;                     // bytes per ring stage
 
     // shared memory: x' [nx_max][NS][k_alloc] | rings [nw][depth] | full and
     // empty mbarriers [2][nw][depth] + x-staged | partials | per-row unscale
     // factors | max scratch | done counter | row scales
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * nxr * k_alloc;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * kStage);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stg);
     const int kR = p.round_rgs;
     float *part = reinterpret_cast<float *>(bars + 2 * nw * depth + 1);  // [kR][nw][NS][8]
     float *unscale = part + (size_t)kR * nw * NS * 8;                  // [nxr][2]: 2^-T as two factors
@@ -384,8 +400,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         }
     };
 
-    if (tid <= s_hi - s_lo)
+    if (tid <= s_hi - s_lo) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.map[s_lo + tid])) : "memory");
+        if (GW)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.smap[s_lo + tid])) : "memory");
+    }
     if (tid < nxr) reinterpret_cast<unsigned *>(red)[tid] = 0u;   // row maxima of x (atomicMax)
     if (warp == nw && lane < nw) {
         for (int b = 0; b < depth; ++b) {
@@ -421,9 +440,12 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
             const int rg = pc.round_base + pc.rgl;
             pset = set_of(rg, pset);
             const uint32_t bar = my_full + 8 * ps;
-            mbar_expect_tx(bar, (uint32_t)(8 * rb));
-            tma_load_2d(smem_u32(ring + ((size_t)lane * depth + ps) * kStage), &p.map[pset], pc.sg * (kSeg / 4),
-                        (rg - p.rg_start[pset]) * 8, bar, policy);
+            const uint32_t dst = smem_u32(ring + ((size_t)lane * depth + ps) * stg);
+            mbar_expect_tx(bar, (uint32_t)(8 * rb + scb));
+            tma_load_2d(dst, &p.map[pset], pc.sg * (kSeg / 4), (rg - p.rg_start[pset]) * 8, bar, policy);
+            if (GW)   // this stage's group scales, from the first group rounded down to 16 bytes
+                tma_load_2d(dst + kStage, &p.smap[pset], fdiv(pc.sg * SEGE, p.div_gs) & ~3,
+                            (rg - p.rg_start[pset]) * 8, bar, policy);
             advance(pc);
             if (++ps == depth) {
                 ps = 0;
@@ -489,7 +511,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 #pragma unroll
     for (int i = 0; i < kSc; ++i) {
         const int r = i * nct + tid;
-        sc_reg[i] = r < (rg1 - rg0) * 8 ? scale_early(r) : 0.f;
+        sc_reg[i] = !GW && r < (rg1 - rg0) * 8 ? scale_early(r) : 0.f;
     }
 
     // round-0 partials start at zero (warps that touch no unit of a row group
@@ -659,7 +681,8 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 #pragma unroll
     for (int i = 0; i < kSc; ++i)
         if (i * nct + tid < (rg1 - rg0) * 8) row_scale[i * nct + tid] = sc_reg[i];
-    for (int r = kSc * nct + tid; r < (rg1 - rg0) * 8; r += nct) row_scale[r] = scale_of(r);  // tall CTAs
+    if (!GW)
+        for (int r = kSc * nct + tid; r < (rg1 - rg0) * 8; r += nct) row_scale[r] = scale_of(r);  // tall CTAs
     consumers_sync(nct);
     if constexpr (FMT != B200Q_F32) {
         // rows outside the fixed exponent's range: staged again with their own
@@ -689,20 +712,43 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
 
     // ---- main loop
     const uint32_t my_full = full0 + 8 * warp * depth, my_empty = empty0 + 8 * warp * depth;
-    const uint8_t *my_ring = ring + (size_t)warp * depth * kStage;
+    const uint8_t *my_ring = ring + (size_t)warp * depth * stg;
     Cursor cc;
     int c_stage = 0, cset = s_lo;
     uint32_t c_phase = 0;
     bool ok = true;
     const float *xsb = xs;                            // x' rows of the current set's slot
+    // per-row scales: a2 / az run across the row group's units; group-wise
+    // scales: a2 / az hold one group, a1 the row group's scaled group sums
     float2 a2[8][NS], az[NS];
-    auto clear_acc = [&]() {
+    float a1[8][NS];
+    auto clear_group = [&]() {
 #pragma unroll
         for (int t = 0; t < NS; ++t) {
             az[t] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < 8; ++r) a2[r][t] = make_float2(0.f, 0.f);
         }
+    };
+    auto clear_acc = [&]() {
+        clear_group();
+#pragma unroll
+        for (int t = 0; t < NS; ++t)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) a1[r][t] = 0.f;
+    };
+    // a group's sums, times its scales (ssc: the stage's scales at the group's column)
+    auto fold_group = [&](const float *ssc) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const float g = ssc[r * p.gbox];
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+                a1[r][t] = fmaf(g, FMT == B200Q_F32 ? a2[r][t].x + a2[r][t].y
+                                                    : (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y),
+                                a1[r][t]);
+        }
+        clear_group();
     };
     // lane sums of the current row group -> part[rgl][warp]
     auto flush = [&](int rgl) {
@@ -711,8 +757,9 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
         for (int t = 0; t < NS; ++t)
 #pragma unroll
             for (int r = 0; r < 8; ++r)
-                v[t * 8 + r] = FMT == B200Q_F32 ? a2[r][t].x + a2[r][t].y
-                                                : (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y);
+                v[t * 8 + r] = GW ? a1[r][t]
+                                  : FMT == B200Q_F32 ? a2[r][t].x + a2[r][t].y
+                                                     : (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y);
         const float sum = reduce_scatter<NV>(v, lane);
         constexpr int sh = NS == 2 ? 1 : 2;         // this lane holds value index lane >> sh
         const int idx = lane >> sh;
@@ -745,7 +792,12 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
             }
             const int chunks = (p.ld - sg * kSeg < kSeg ? p.ld - sg * kSeg : kSeg) / 16;
             if (lane < chunks) {
-                const uint8_t *st = my_ring + (size_t)c_stage * kStage + lane * 16;
+                const uint8_t *st = my_ring + (size_t)c_stage * stg + lane * 16;
+                // group-wise scales: this lane's first group, as a column of the stage's scales
+                const float *ssc = nullptr;
+                if (GW)
+                    ssc = reinterpret_cast<const float *>(my_ring + (size_t)c_stage * stg + kStage) +
+                          (fdiv(sg * SEGE + lane * E, p.div_gs) - (fdiv(sg * SEGE, p.div_gs) & ~3));
                 uint4 cw[8];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rb);
@@ -762,6 +814,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                                                   make_float2(xf.z, xf.w), a2[r][t]);
                         }
                     }
+                    if (GW) fold_group(ssc);     // a chunk lies in one group
                 } else {
                     // one 16-byte chunk = 4 words; x' for one word at a time
 #pragma unroll
@@ -783,6 +836,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                             word_fma2<FMT, NS, EW>(w, xv, a2[r]);
                         }
                         word_fma2<FMT, NS, EW>(F<FMT>::ZW, xv, az);
+                        if (GW && (q + 1) % GW == 0) fold_group(ssc + q / GW);
                     }
                 }
             }
@@ -838,7 +892,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1)
                 const int o = (rg - s_start) * 8 + rr;
                 if (o < s_O) {
                     const float dot = (sum * unscale[2 * s_xr]) * unscale[2 * s_xr + 1];   // exact: powers of two
-                    s_y[(long long)t * s_O + o] = dot * row_scale[(rg - rg0) * 8 + rr];
+                    s_y[(long long)t * s_O + o] = GW ? dot : dot * row_scale[(rg - rg0) * 8 + rr];
                 }
             }
         }
@@ -870,12 +924,13 @@ struct Group {
     bool silu;
 };
 
-template <int FMT, int NS, int MS>
+template <int FMT, int NS, int MS, int GW>
 cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     constexpr int EW = FMT == B200Q_F32 ? 1 : FMT == B200Q_I8 ? 4 : FMT == B200Q_I4 ? 8 : 16;
     const int nseg = (p.ld + kSeg - 1) / kSeg;
     const size_t k_alloc = FMT == B200Q_F32 ? (size_t)p.k_pad : (size_t)nseg * (kSeg / 4) * EW;
-    const size_t stage = (size_t)kStage + 16;                // ring stage + its full and empty mbarriers
+    // ring stage (codes, then group scales) + its full and empty mbarriers
+    const size_t stage = (size_t)kStage + (GW ? (size_t)32 * p.gbox : 0) + 16;
     const int rg_cta = (p.n_rg + grid - 1) / grid;
     const size_t nxr = (size_t)p.nx_max * NS;
     auto fixed_for = [&](int nw, int rr) {
@@ -884,7 +939,7 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     };
     // warps and depth first (round of kRound), then grow the round to all of
     // the CTA's row groups if the partials still fit (one round: no barrier)
-    int depth = 3, nw = kMaxWarps;
+    int depth = 3, nw = max_warps<NS, GW>();
     while (nw > 4 && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) --nw;
     if (fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) depth = 2;
     while (nw > 4 && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) --nw;
@@ -906,7 +961,7 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     static bool attr_set[64] = {};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS, MS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS, MS, GW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemMax);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
@@ -930,13 +985,13 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS, MS>, q);
+    e = cudaLaunchKernelEx(&cfg, qmv_decode_kernel<FMT, NS, MS, GW>, q);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int FMT, int MS>
+template <int FMT, int MS, int GW>
 cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
     if (!g_sms) {
         int dev = 0;
@@ -953,8 +1008,13 @@ cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
     p.row_bytes = (int)(t0.ld < kSeg ? t0.ld : kSeg);
     p.k_pad = (int)t0.k_pad;
     int slot = -1, n_rg = 0;
+    if (GW) {
+        p.gbox = t0.sc_box;
+        p.div_gs = make_fastdiv((uint32_t)t0.gs);
+    }
     for (int j = 0; j < g.n; ++j) {
         p.map[j] = g.t[j]->dec_map;
+        if (GW) p.smap[j] = g.t[j]->sc_map;
         p.scales[j] = g.t[j]->scales;
         p.O[j] = g.t[j]->O;
         p.rg_start[j] = n_rg;
@@ -983,21 +1043,38 @@ cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
             p.xb[p.xslot[j]] = g.xb[j] ? g.xb[j] + (long long)s0 * t0.I : nullptr;
             p.y[j] = g.y[j] + (long long)s0 * g.t[j]->O;
         }
-        cudaError_t e = ns == 2 ? launch_ns<FMT, 2, MS>(p, grid, st) : launch_ns<FMT, 1, MS>(p, grid, st);
+        cudaError_t e = ns == 2 ? launch_ns<FMT, 2, MS, GW>(p, grid, st) : launch_ns<FMT, 1, MS, GW>(p, grid, st);
         if (e != cudaSuccess) return e;
         s0 += ns;
     }
     return cudaSuccess;
 }
 
+// Group-wise scales take the kernel variant for the group's span in words
+// of a chunk (every set of a launch has the same group size); one variant
+// per format serves all set counts.
 template <int FMT>
 cudaError_t launch_group_fmt(const Group &g, int S, cudaStream_t st) {
-    return g.n <= 2 ? launch_group_ms<FMT, 2>(g, S, st) : launch_group_ms<FMT, kMaxSets>(g, S, st);
+    constexpr int E = F<FMT>::E, EW = FMT == B200Q_F32 ? 1 : E / 4;
+    const int gs = g.t[0]->gs;
+    if (gs == 0) return g.n <= 2 ? launch_group_ms<FMT, 2, 0>(g, S, st) : launch_group_ms<FMT, kMaxSets, 0>(g, S, st);
+    if (gs % E == 0) return launch_group_ms<FMT, kMaxSets, 4>(g, S, st);
+    if constexpr (FMT == B200Q_I4) {
+        if (gs == 2 * EW) return launch_group_ms<FMT, kMaxSets, 2>(g, S, st);
+    } else if constexpr (FMT == B200Q_I2) {
+        if (gs == EW) return launch_group_ms<FMT, kMaxSets, 1>(g, S, st);
+        if (gs == 2 * EW) return launch_group_ms<FMT, kMaxSets, 2>(g, S, st);
+    }
+    return cudaErrorInvalidValue;   // not a group size the decode kernel takes
 }
 
 cudaError_t launch_group(const Group &g, int S, cudaStream_t st, bool *handled) {
     *handled = false;
     if (S < 1 || S > 15 || g.n < 1 || g.n > kMaxSets) return cudaSuccess;
+    for (int j = 1; j < g.n; ++j)
+        if (g.t[j]->gs != g.t[0]->gs) return cudaSuccess;   // mixed scale layouts: one tensor at a time
+    // the group arithmetic is 32-bit
+    if (g.t[0]->gs && g.t[0]->k_pad + (long long)kSeg * 8 >= (1ll << 31)) return cudaSuccess;
     cudaError_t e = cudaSuccess;
     switch (g.t[0]->fmt) {
     case B200Q_F32: e = launch_group_fmt<B200Q_F32>(g, S, st); break;

@@ -84,10 +84,10 @@ struct Deq<B200Q_I2> {
 
 struct RowSet {
     const uint8_t *codes;
-    const float *scales;   // [O] per row, or [O, G] per row and group
+    const float *scales;   // [O] per row, or [O, G] per row and group (row stride G)
     float *y;
     int gs;                // 0: per-row scales
-    int G;                 // groups per row
+    int G;                 // row stride of the group scales
 };
 
 // SUB = 0: per-row scales, or groups that are whole chunks (gs a multiple of
@@ -321,8 +321,8 @@ cudaError_t launch_fix_row_tails(const Tensor &t, long long rb, cudaStream_t st)
 
 cudaError_t launch_qmv_simt(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
                             cudaStream_t st) {
-    RowSet a{t.codes, t.scales, y, t.gs, t.G};
-    RowSet b = tu ? RowSet{tu->codes, tu->scales, yu, tu->gs, tu->G} : a;
+    RowSet a{t.codes, t.scales, y, t.gs, t.G_ld};
+    RowSet b = tu ? RowSet{tu->codes, tu->scales, yu, tu->gs, tu->G_ld} : a;
     const int n_sets = tu ? 2 : 1;
     const long long rows = (long long)t.O * n_sets;
     const int tok_blocks = (S + kTok - 1) / kTok;

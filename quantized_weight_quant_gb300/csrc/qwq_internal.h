@@ -16,9 +16,11 @@ namespace qwq {
 //        followed by padding up to ld (a multiple of kRowAlign).  Padding
 //        bytes, the unused high bits of a row's last byte, and the rows
 //        o >= O all hold the format's zero-point code, so they decode to 0.
-// scales: [o_pad] f32; rows o >= O have scale 0.
+// scales: [o_pad] f32, or [o_pad, G_ld] with group-wise scales (G used, the
+//        rest of a row 0); rows o >= O have scale 0.
 struct Tensor {
     CUtensorMap dec_map;  // codes as uint32 [o_pad, ld / 4], box 8 rows x 512 bytes (decode stages)
+    CUtensorMap sc_map;   // group scales as f32 [o_pad, G_ld], box 8 rows x sc_box (decode stages)
     int fmt;
     int O, I;
     int device;
@@ -30,6 +32,9 @@ struct Tensor {
     size_t bytes;     // one allocation: codes then scales
     int gs;           // group size of the scales; 0: one scale per row
     int G;            // scales per row (1, or ceil(I / gs))
+    int G_ld;         // device row stride of the scales in floats (G rounded up to 4, >= sc_box)
+    int sc_box;       // group scales one decode stage (8 rows x 512 code bytes) spans, from a
+                      // 4-aligned first group, rounded up to 4
 };
 
 // Group sizes the kernels take: a multiple of a 16-byte chunk's element

@@ -87,3 +87,91 @@ def test_group_scales_refusals(q):
         assert "group size" in q.last_error()
     with q.tensor_upload(fmt, O, I, codes, np.ones(O, np.float32)) as t:
         assert q.tensor_group_size(t) == 0
+
+
+# rows of several decode stages (512 code bytes each) with a ragged tail, and
+# group sizes whose groups straddle stages or span several
+WIDE = [(0, 12, 700), (0, 260, 1500), (1, 48, 2100), (1, 16, 1300), (2, 96, 3000), (2, 2048, 5000),
+        (2, 16, 2500), (3, 192, 6000), (3, 16, 4100), (3, 32, 2200)]
+
+
+@pytest.mark.parametrize("fmt,gs,I", WIDE, ids=lambda v: str(v))
+@pytest.mark.parametrize("S", [1, 2, 5])
+def test_group_scales_wide_rows(q, fmt, gs, I, S):
+    O = 200
+    codes, gsc = _grouped(fmt, O, I, gs, gs + I)
+    x = synth.activations(S, I, I, 4)
+    y_ref, bound = oracle.matmul_gs(fmt, O, I, gs, codes, gsc, x)
+    with q.tensor_upload(fmt, O, I, codes, gsc, gs=gs) as t:
+        y = gpu_matmul(q, t, x, S, O)
+    assert_within(y, y_ref, bound, TOL_F32, "gs fmt%d gs%d I%d S%d" % (fmt, gs, I, S))
+
+
+@pytest.mark.parametrize("fmt,gs", [(1, 32), (2, 128), (2, 16), (3, 32)], ids=lambda v: str(v))
+@pytest.mark.parametrize("silu", [False, True], ids=["plain", "silu"])
+def test_group_scales_grouped_many_sets(q, fmt, gs, silu):
+    """Six tensors of different heights in one grouped call (blocks span
+    several tensors and inputs), every tensor checked on its own."""
+    import torch
+    Os, I, S = [300, 8, 640, 17, 129, 1024], 1536, 2
+    ws = [_grouped(fmt, O, I, gs, 40 + j) for j, O in enumerate(Os)]
+    xa = [synth.normal_f32((S, I), 41, 10 + j, std=2.0) for j in range(len(Os))]
+    xb = [synth.activations(S, I, 41, 20 + j) for j in range(len(Os))]
+    handles = [q.tensor_upload(fmt, O, I, c, s, gs=gs) for O, (c, s) in zip(Os, ws)]
+    try:
+        ys = [empty(S, O) for O in Os]
+        if silu:
+            q.matmul_grouped_silu(handles, [to_dev(a) for a in xa], [to_dev(b) for b in xb], ys, S)
+        else:
+            q.matmul_grouped(handles, [to_dev(a) for a in xa], ys, S)
+        torch.cuda.synchronize()
+        out = [y.cpu().numpy() for y in ys]
+    finally:
+        for h in handles:
+            h.free()
+    for j, (O, (c, s)) in enumerate(zip(Os, ws)):
+        xin = oracle.silu_mul(xa[j], xb[j])[0] if silu else xa[j]
+        y_ref, bound = oracle.matmul_gs(fmt, O, I, gs, c, s, xin)
+        assert_within(out[j], y_ref, bound, TOL_F32, "set %d" % j)
+
+
+def test_group_scales_mixed_layouts_in_a_group(q):
+    """Per-row and group-wise tensors in one grouped call run one at a time."""
+    import torch
+    fmt, O, I, S = 2, 96, 640, 1
+    c0, s0 = synth.quant_tensor(fmt, O, I, 3, 1, 5e-3, 2e-2)
+    c1, s1 = _grouped(fmt, O, I, 64, 4)
+    c2, s2 = _grouped(fmt, O, I, 128, 5)
+    x = synth.activations(S, I, 3, 9)
+    with q.tensor_upload(fmt, O, I, c0, s0) as a, q.tensor_upload(fmt, O, I, c1, s1, gs=64) as b, \
+            q.tensor_upload(fmt, O, I, c2, s2, gs=128) as c:
+        xd = to_dev(x)
+        ys = [empty(S, O) for _ in range(3)]
+        q.matmul_grouped([a, b, c], [xd] * 3, ys, S)
+        torch.cuda.synchronize()
+        out = [y.cpu().numpy() for y in ys]
+    refs = [oracle.matmul(fmt, O, I, c0, s0, x), oracle.matmul_gs(fmt, O, I, 64, c1, s1, x),
+            oracle.matmul_gs(fmt, O, I, 128, c2, s2, x)]
+    for j, (y_ref, bound) in enumerate(refs):
+        assert_within(out[j], y_ref, bound, TOL_F32, "mixed set %d" % j)
+
+
+@pytest.mark.parametrize("fmt,gs", [(0, 8), (1, 16), (2, 128), (2, 16), (3, 16), (3, 32), (3, 64)],
+                         ids=lambda v: str(v))
+def test_group_scales_run_the_decode_kernel(q, fmt, gs):
+    """Below 16 rows a group-wise tensor runs the staged decode kernel, one
+    launch per two rows (5 rows: 3 launches); from 16 rows the general SIMT
+    kernel, one launch for any number of rows."""
+    import torch
+    O, I = 256, 1024
+    codes, gsc = _grouped(fmt, O, I, gs, 6)
+    with q.tensor_upload(fmt, O, I, codes, gsc, gs=gs) as t:
+        xd = to_dev(synth.activations(16, I, 6, 1))
+        y = empty(16, O)
+        n0 = q.kernel_launches()
+        q.matmul(t, xd, y, 5)
+        n1 = q.kernel_launches()
+        q.matmul(t, xd, y, 16)
+        n2 = q.kernel_launches()
+        torch.cuda.synchronize()
+    assert (n1 - n0, n2 - n1) == (3, 1)
