@@ -66,6 +66,9 @@ def _bind(path: str):
     L.qref_matmul_gs.restype = c_int
     L.qref_rmsnorm.argtypes = [vp, vp, vp, c_long, c_long, ctypes.c_double, vp, vp, vp]
     L.qref_rmsnorm.restype = c_int
+    L.qref_mla_absorb.argtypes = [c_int, c_long, c_long, c_long, c_long, c_long, vp, vp, vp, vp, vp, vp,
+                                  c_long, c_long, ctypes.c_double, c_long, vp, vp, vp]
+    L.qref_mla_absorb.restype = c_int
     L.qref_round_bf16.argtypes = [ctypes.c_float]
     L.qref_round_bf16.restype = ctypes.c_float
     L.qref_matmul_bf16x.argtypes = [c_int, c_long, c_long, vp, vp, vp, c_long, vp,
@@ -230,6 +233,35 @@ def rmsnorm(x, w, eps: float, r=None):
     if rc:
         raise ValueError("qref_rmsnorm: bad argument")
     return h, y, yd
+
+
+def mla_absorb(fmt: int, H: int, Dn: int, Dv: int, K: int, codes, scales, q_nope, q_rope, lat, rope,
+               st0: int, scale: float, *, want_dbl: bool = False):
+    """MLA decode attention with weight absorption over a [H*(Dn+Dv), K]
+    weight tensor (per-row scales or None = 1.0).  q_nope [S, H, Dn], q_rope
+    [S, H, R], lat [T, K], rope [T, R]; the S new tokens are the last S
+    positions of the caches.  Returns (ctx f32 [S, H, Dv], bound f64) or
+    (ctx, bound, ctx f64) with want_dbl."""
+    codes = _check_codes(fmt, H * (Dn + Dv), K, codes)
+    scales = _f32(scales)
+    q_nope = _f32(q_nope)
+    S = q_nope.shape[0]
+    q_nope = q_nope.reshape(S, H, Dn)
+    lat = _f32(lat)
+    T = lat.shape[0]
+    lat = lat.reshape(T, K)
+    rope = _f32(rope).reshape(T, -1)
+    R = rope.shape[1]
+    q_rope = _f32(q_rope).reshape(S, H, R)
+    ctx = np.empty((S, H, Dv), np.float32)
+    bound = np.empty((S, H, Dv), np.float64)
+    cd = np.empty((S, H, Dv), np.float64) if want_dbl else None
+    rc = _L().qref_mla_absorb(fmt, H, Dn, Dv, K, R, _ptr(codes), _ptr(scales), _ptr(q_nope), _ptr(q_rope),
+                              _ptr(lat), _ptr(rope), T, st0, float(scale), S, _ptr(ctx), _ptr(cd),
+                              _ptr(bound))
+    if rc:
+        raise ValueError("qref_mla_absorb: bad argument")
+    return (ctx, bound, cd) if want_dbl else (ctx, bound)
 
 
 def round_bf16(v) -> np.ndarray:

@@ -40,6 +40,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -293,4 +294,133 @@ int qref_matmul_bf16x(int fmt, long O, long I, const uint8_t *codes, const float
     if (S < 0 || I < 0) return -1;
     for (long k = 0; k < S * I; ++k) xr_scratch[k] = qref_round_bf16(x[k]);
     return qref_matmul(fmt, O, I, codes, scales, xr_scratch, S, y, ydbl, bound);
+}
+
+/*
+ * MLA decode attention with weight absorption (page "第 8 章 · 02
+ * CUDA/Metal/Vulkan 三后端", section 四, the header of attention_absorb.comp,
+ * the Vulkan twin of coli_cuda_attention_absorb).  Per new token s and head h,
+ * four steps in the pages' order:
+ *
+ *   qabs[i]  = sum_d q_nope[s,h,d] * Wk[h,d,i]                  (absorb)
+ *   score_t  = (qabs . L[t] + q_rope[s,h] . Rr[t]) * scale      t in [st0, T-S+s]
+ *   p        = softmax over that window of score
+ *   clat[i]  = sum_t p_t * L[t,i]                               (latent context)
+ *   ctx[s,h,v] = sum_i clat[i] * Wv[h,v,i]                      (value rows)
+ *
+ * Wkv_b is one [H*(Dn+Dv), K] weight tensor (host layout of fmt, per-row
+ * scales; NULL scales mean 1.0): head h's key rows are h*(Dn+Dv) + d for
+ * d < Dn, its value rows follow at h*(Dn+Dv) + Dn + v; the weight value is
+ * scale[row] * deq(code), as in qref_matmul.  L is the latent cache [T, K],
+ * Rr the rope cache [T, R], both f32; the S new tokens sit at positions
+ * T-S .. T-1 and token s sees positions st0 .. T-S+s (causal).  q_nope is
+ * [S, H, Dn], q_rope [S, H, R], ctx [S, H, Dv].  Everything is in double,
+ * the softmax from its maximum; ctx is rounded once to f32.
+ *
+ * Error bound per output, from the f32 arithmetic of an implementation that
+ * rounds each step (relative error eps per accumulated term):
+ *     bound[s,h,v] = (1 + A) * sum_i |Wv[h,v,i]| * sum_t p_t |L[t,i]|
+ *     A = max_t |scale| * (sum_i QA_i |L[t,i]| + sum_j |q_rope_j Rr[t,j]|),
+ *     QA_i = sum_d |q_nope_d Wk[h,d,i]|
+ * (a score error of eps * A moves p_t by at most 2 eps A p_t, and the value
+ * step adds its own eps).  Returns 0, or -1 for a bad argument (S < 1,
+ * T < S, st0 < 0 or st0 > T - S: every window must hold a position).
+ */
+int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
+                    const uint8_t *codes, const float *scales,
+                    const float *q_nope, const float *q_rope,
+                    const float *lat, const float *rope,
+                    long T, long st0, double scale, long S,
+                    float *ctx, double *ctxdbl, double *bound)
+{
+    long rb = qref_row_bytes(fmt, K);
+    if (rb < 0 || H < 1 || Dn < 1 || Dv < 1 || K < 1 || R < 0 || S < 1 || T < S || st0 < 0 || st0 > T - S)
+        return -1;
+    if (!codes || !q_nope || (R > 0 && (!q_rope || !rope)) || !lat || !ctx) return -1;
+    long HS = H * S;
+#ifdef _OPENMP
+    int nt = qref_max_threads();
+#pragma omp parallel for schedule(dynamic) num_threads(nt)
+#endif
+    for (long hs = 0; hs < HS; ++hs) {
+        long s = hs / H, h = hs % H;
+        long key0 = h * (Dn + Dv), val0 = key0 + Dn;
+        long first = st0, last = T - S + s;            /* the window token s sees */
+        long nwin = last - first + 1;
+        double *qabs = (double *)malloc(sizeof(double) * (size_t)K);
+        double *qa = (double *)malloc(sizeof(double) * (size_t)K);
+        double *clat = (double *)malloc(sizeof(double) * (size_t)K);
+        double *cabs = (double *)malloc(sizeof(double) * (size_t)K);
+        double *score = (double *)malloc(sizeof(double) * (size_t)nwin);
+        double *sabs = (double *)malloc(sizeof(double) * (size_t)nwin);
+        if (!qabs || !qa || !clat || !cabs || !score || !sabs) {
+            free(qabs); free(qa); free(clat); free(cabs); free(score); free(sabs);
+            continue;
+        }
+        const float *qn = q_nope + (s * H + h) * Dn;
+        const float *qr = R > 0 ? q_rope + (s * H + h) * R : NULL;
+
+        /* absorb: qabs = sum over the head's key rows of q_nope[d] * row d */
+        for (long i = 0; i < K; ++i) qabs[i] = qa[i] = 0.0;
+        for (long d = 0; d < Dn; ++d) {
+            const uint8_t *krow = codes + (key0 + d) * rb;
+            double ksc = scales ? (double)scales[key0 + d] : 1.0;
+            for (long i = 0; i < K; ++i) {
+                double kw = ksc * qref_weight(fmt, krow, i);
+                qabs[i] += (double)qn[d] * kw;
+                qa[i] += fabs((double)qn[d] * kw);
+            }
+        }
+        /* scores over the window, then the softmax from their maximum */
+        double smax = -HUGE_VAL, amax = 0.0;
+        for (long w = 0; w < nwin; ++w) {
+            const float *lt = lat + (first + w) * K;
+            double dot = 0.0, a = 0.0;
+            for (long i = 0; i < K; ++i) {
+                dot += qabs[i] * (double)lt[i];
+                a += qa[i] * fabs((double)lt[i]);
+            }
+            for (long j = 0; j < R; ++j) {
+                double t = (double)qr[j] * (double)rope[(first + w) * R + j];
+                dot += t;
+                a += fabs(t);
+            }
+            score[w] = dot * scale;
+            sabs[w] = a * fabs(scale);
+            if (score[w] > smax) smax = score[w];
+            if (sabs[w] > amax) amax = sabs[w];
+        }
+        double z = 0.0;
+        for (long w = 0; w < nwin; ++w) {
+            score[w] = exp(score[w] - smax);
+            z += score[w];
+        }
+        /* latent context and its magnitude */
+        for (long i = 0; i < K; ++i) clat[i] = cabs[i] = 0.0;
+        for (long w = 0; w < nwin; ++w) {
+            double p = score[w] / z;
+            const float *lt = lat + (first + w) * K;
+            for (long i = 0; i < K; ++i) {
+                clat[i] += p * (double)lt[i];
+                cabs[i] += p * fabs((double)lt[i]);
+            }
+        }
+        /* value rows */
+        for (long v = 0; v < Dv; ++v) {
+            const uint8_t *vrow = codes + (val0 + v) * rb;
+            double vsc = scales ? (double)scales[val0 + v] : 1.0;
+            double acc = 0.0, b = 0.0;
+            for (long i = 0; i < K; ++i) {
+                double vw = vsc * qref_weight(fmt, vrow, i);
+                acc += clat[i] * vw;
+                b += fabs(vw) * cabs[i];
+            }
+            long out = (s * H + h) * Dv + v;
+            ctx[out] = (float)acc;
+            if (ctxdbl) ctxdbl[out] = acc;
+            if (bound) bound[out] = (1.0 + amax) * b;
+        }
+        free(qabs); free(qa); free(clat); free(cabs); free(score); free(sabs);
+    }
+    return 0;
 }

@@ -382,4 +382,107 @@ def check_row_bytes():
     assert Q.row_bytes(7, 4) == -1
 
 
+def _dense_weights(fmt, codes, sc, O, I):
+    """Weight values scale * (code - zero point) by the library routes of
+    check_library_reduction, [O, I] float64."""
+    if fmt == F32:
+        W = codes.view(np.float32).astype(np.float64)
+    elif fmt == I8:
+        W = codes.view(np.int8).astype(np.float64)
+    else:
+        W = (_unpack_fields(codes, fmt, I) - {I4: 8, I2: 2}[fmt]).astype(np.float64)
+    return W * sc.astype(np.float64)[:, None]
+
+
+def _mla_case(fmt, H, Dn, Dv, K, R, S, T, seed):
+    codes, sc = synth.quant_tensor(fmt, H * (Dn + Dv), K, seed, 1, 5e-3, 2e-2)
+    qn = synth.normal_f32((S, H, Dn), seed, 2, std=4.0)
+    qr = synth.normal_f32((S, H, R), seed, 3)
+    lat = synth.normal_f32((T, K), seed, 4)
+    rope = synth.normal_f32((T, R), seed, 5)
+    return codes, sc, qn, qr, lat, rope
+
+
+MLA_CASES = [  # fmt, H, Dn, Dv, K, R, S, T, st0, scale
+    (I4, 3, 8, 5, 40, 6, 3, 11, 2, 0.3),
+    (I8, 2, 4, 7, 33, 4, 1, 9, 0, 0.5),
+    (F32, 2, 6, 6, 20, 2, 2, 5, 3, 1.0),
+    (I2, 4, 3, 2, 27, 3, 4, 12, 1, 0.7),
+]
+
+
+def check_mla_naive():
+    """Absorption is an identity: decompress every position's keys and values
+    (k_t = Wk L_t, v_t = Wv L_t, the non-absorbed MLA form), then textbook
+    causal attention over [st0, T-S+s] in numpy float64.  The error bound is
+    recomputed from its definition."""
+    for fmt, H, Dn, Dv, K, R, S, T, st0, scale in MLA_CASES:
+        codes, sc, qn, qr, lat, rope = _mla_case(fmt, H, Dn, Dv, K, R, S, T, 11 + fmt)
+        _, bound, cd = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, st0, scale, want_dbl=True)
+        W = _dense_weights(fmt, codes, sc, H * (Dn + Dv), K).reshape(H, Dn + Dv, K)
+        Wk, Wv = W[:, :Dn], W[:, Dn:]
+        L, Rr = lat.astype(np.float64), rope.astype(np.float64)
+        keys = np.einsum("hdk,tk->thd", Wk, L)
+        vals = np.einsum("hvk,tk->thv", Wv, L)
+        for s in range(S):
+            win = np.arange(st0, T - S + s + 1)
+            for h in range(H):
+                z = (keys[win, h] @ qn[s, h].astype(np.float64) + Rr[win] @ qr[s, h].astype(np.float64)) * scale
+                p = np.exp(z - z.max())
+                p /= p.sum()
+                ref = p @ vals[win, h]
+                assert np.all(np.abs(cd[s, h] - ref) <= 1e-12 * bound[s, h]), (fmt, s, h)
+                qa = np.abs(Wk[h] * qn[s, h].astype(np.float64)[:, None]).sum(0)
+                A = (np.abs(L[win]) @ qa + np.abs(Rr[win] * qr[s, h].astype(np.float64)).sum(1)).max() * abs(scale)
+                b = (1 + A) * (np.abs(Wv[h]) @ (p @ np.abs(L[win])))
+                assert np.allclose(bound[s, h], b, rtol=1e-12, atol=0), (fmt, s, h)
+
+
+def check_mla_uniform_window():
+    """With q = 0 (or scale = 0) every score is equal: the context is the plain
+    mean of the latent rows in the window, through the value rows."""
+    fmt, H, Dn, Dv, K, R, S, T = I4, 2, 5, 4, 24, 4, 3, 10
+    codes, sc, qn, qr, lat, rope = _mla_case(fmt, H, Dn, Dv, K, R, S, T, 21)
+    Wv = _dense_weights(fmt, codes, sc, H * (Dn + Dv), K).reshape(H, Dn + Dv, K)[:, Dn:]
+    for st0 in (0, 4, T - S):
+        for args in ((np.zeros_like(qn), np.zeros_like(qr), 0.9), (qn, qr, 0.0)):
+            _, bound, cd = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, args[0], args[1], lat, rope, st0, args[2],
+                                        want_dbl=True)
+            for s in range(S):
+                mean = lat[st0:T - S + s + 1].astype(np.float64).mean(0)
+                for h in range(H):
+                    assert np.all(np.abs(cd[s, h] - Wv[h] @ mean) <= 1e-12 * bound[s, h]), (st0, s, h)
+
+
+def check_mla_window_edges():
+    """Latent and rope rows outside a token's window do not move its context;
+    the first and last rows inside it do."""
+    fmt, H, Dn, Dv, K, R, S, T, st0 = I8, 2, 4, 3, 16, 4, 3, 9, 2
+    codes, sc, qn, qr, lat, rope = _mla_case(fmt, H, Dn, Dv, K, R, S, T, 31)
+    base, _ = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, st0, 0.4)
+    for t in range(T):
+        for which in ("lat", "rope"):
+            l2, r2 = lat.copy(), rope.copy()
+            (l2 if which == "lat" else r2)[t] += np.float32(3.0)
+            got, _ = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, l2, r2, st0, 0.4)
+            for s in range(S):
+                inside = st0 <= t <= T - S + s
+                same = np.array_equal(got[s], base[s])
+                assert same != inside, (which, t, s)
+
+
+def check_mla_shift_invariance():
+    """Adding one vector to every rope row shifts all of a token's scores by the
+    same amount, which the softmax ignores."""
+    fmt, H, Dn, Dv, K, R, S, T = I4, 2, 4, 4, 24, 6, 2, 8
+    codes, sc, qn, qr, lat, rope = _mla_case(fmt, H, Dn, Dv, K, R, S, T, 41)
+    rope = np.round(rope * 64) / np.float32(64)               # on a 1/64 grid: the shift below is exact
+    _, bound, cd = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, 1, 0.5, want_dbl=True)
+    shifted = rope + synth.rng(41, 9).integers(-3, 4, size=(1, R)).astype(np.float32)
+    _, _, cd2 = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, shifted, 1, 0.5, want_dbl=True)
+    assert np.all(np.abs(cd - cd2) <= 1e-12 * bound)
+    assert not np.array_equal(Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr * 2, lat, rope, 1, 0.5)[0],
+                              Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, 1, 0.5)[0])
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

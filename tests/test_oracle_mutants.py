@@ -54,6 +54,22 @@ MUTANTS = {
                              "double inv = 1.0 / (sqrt(ss / (double)D) + eps);"),
     "rms_abs_not_square": ("ss += (double)hv * (double)hv;", "ss += fabs((double)hv);"),
     "rms_weight_dropped": ("double v = (double)hv * (double)w[d] * inv;", "double v = (double)hv * inv;"),
+    "mla_window_from_zero": ("long first = st0, last = T - S + s;", "long first = 0, last = T - S + s;"),
+    "mla_window_short_by_one": ("long first = st0, last = T - S + s;", "long first = st0, last = T - S + s - 1;"),
+    "mla_window_not_causal": ("long first = st0, last = T - S + s;", "long first = st0, last = T - 1;"),
+    "mla_values_from_key_rows": ("long key0 = h * (Dn + Dv), val0 = key0 + Dn;",
+                                 "long key0 = h * (Dn + Dv), val0 = key0;"),
+    "mla_head_stride_dn": ("long key0 = h * (Dn + Dv), val0 = key0 + Dn;",
+                           "long key0 = h * Dn, val0 = key0 + Dn;"),
+    "mla_rope_dropped": ("                dot += t;\n", "                (void)t;\n"),
+    "mla_scale_dropped": ("score[w] = dot * scale;", "score[w] = dot;"),
+    "mla_softmax_unnormalized": ("double p = score[w] / z;", "double p = score[w];"),
+    "mla_q_head_token_swapped": ("const float *qn = q_nope + (s * H + h) * Dn;",
+                                 "const float *qn = q_nope + (h * S + s) * Dn;"),
+    "mla_key_scale_dropped": ("double ksc = scales ? (double)scales[key0 + d] : 1.0;", "double ksc = 1.0;"),
+    "mla_value_scale_dropped": ("double vsc = scales ? (double)scales[val0 + v] : 1.0;", "double vsc = 1.0;"),
+    "mla_bound_without_softmax_term": ("bound[out] = (1.0 + amax) * b;", "bound[out] = b;"),
+    "mla_latent_not_weighted": ("clat[i] += p * (double)lt[i];", "clat[i] += (double)lt[i] / (double)nwin;"),
     "rms_residual_dropped": ("float hv = r ? (float)((double)x[s * D + d] + (double)r[s * D + d]) : x[s * D + d];\n            if (h)",
                              "float hv = x[s * D + d];\n            if (h)"),
 }
