@@ -426,6 +426,8 @@ def run_ours(args):
     if not args.no_moe:
         line["moe_layer"] = moe_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
     line["layer_glue"] = glue_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
+    if not args.no_mla:
+        line["mla_decode"] = mla_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
     # end to end through the host-buffer C-ABI call
     e2e_steps = max(3, min(args.steps, 20))
     e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 2)
@@ -596,6 +598,100 @@ def moe_measure(q, steps, warmup, stream):
             "bytes_per_layer": layer_bytes}
 
 
+MLA_SHAPE = {"H": 64, "Dn": 128, "Dv": 128, "K": 512, "R": 64}
+
+
+def mla_fma(H, Dn, Dv, K, R, S, T, st0=0):
+    """Multiply-adds of one absorbed-attention call: absorb, scores, latent
+    context, value rows (each token's causal window)."""
+    win = sum(T - S + s - st0 + 1 for s in range(S))
+    return H * (S * Dn * K + win * (K + R) + win * K + S * Dv * K)
+
+
+def mla_bytes(H, Dn, Dv, K, R, S, T, st0=0):
+    """Cache rows of the window, int4 codes + row scales of Wkv_b, q and ctx."""
+    rows = H * (Dn + Dv)
+    return (T - st0) * (K + R) * 4 + rows * ((K + 1) // 2 + 4) + S * H * (Dn + R + Dv) * 4
+
+
+def mla_measure(q, steps, warmup, stream, cases=((1, 4096), (4, 4096), (1, 32768))):
+    """MLA decode attention with weight absorption (b200q_mla_absorb), int4
+    Wkv_b [64 * 256, 512], latent 512 + rope 64, paged caches, per call:
+    a CUDA graph of calls cycling over enough copies of the weights and
+    caches to exceed L2 twice.  The dominant kernel does f32 FMAs on the
+    SIMT pipe, so the roofline is the FP32 FMA peak at the sampled SM clock
+    (152 SMs x 128 lanes x 2 FLOP x MHz); the HBM fraction is given beside it."""
+    import torch
+    import synth
+    sh = MLA_SHAPE
+    H, Dn, Dv, K, R = sh["H"], sh["Dn"], sh["Dv"], sh["K"], sh["R"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = {"workload": "MLA absorb decode, int4 Wkv_b, H=64 Dn=Dv=128 K=512 R=64, 64-position pages", "cases": []}
+    for S, T in cases:
+        per_copy = T * (K + R) * 4 + H * (Dn + Dv) * (K // 2 + 4)
+        copies = max(2, min(16, -(-2 * L2_BYTES // per_copy)))
+        ws, kvs = [], []
+        for c in range(copies):
+            codes, sc = synth.quant_tensor(I4, H * (Dn + Dv), K, 0, 900 + c, 5e-3, 2e-2)
+            ws.append(q.tensor_upload(I4, H * (Dn + Dv), K, codes, sc))
+            kv = q.PagedKV(K, R, T)
+            kv.lat_pool.normal_()
+            kv.rope_pool.normal_()
+            kvs.append(kv)
+        qn = torch.from_numpy(synth.normal_f32((S, H, Dn), 0, 901)).cuda()
+        qr = torch.from_numpy(synth.normal_f32((S, H, R), 0, 902)).cuda()
+        ctx = torch.empty((S, H, Dv), device="cuda")
+        scale = (Dn + R) ** -0.5
+
+        def call(c):
+            kvs[c].attend(ws[c], H, Dn, Dv, qn, qr, T, 0, scale, ctx, S, stream)
+
+        with torch.cuda.stream(stream):
+            for r in range(max(warmup, copies)):
+                call(r % copies)
+        torch.cuda.synchronize()
+        n = 2 * copies
+        g = torch.cuda.CUDAGraph()
+        n0 = q.kernel_launches()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(n):
+                call(r % copies)
+        launches = (q.kernel_launches() - n0) / n
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, steps // 4)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+        ck = clk.summary()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+        fma = mla_fma(H, Dn, Dv, K, R, S, T)
+        nbytes = mla_bytes(H, Dn, Dv, K, R, S, T)
+        mhz = ck.get("sm_mhz") or 2032.0
+        peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        tflops = 2 * fma / (us * 1e-6) / 1e12
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out["cases"].append({
+            "S": S, "T": T, "us_per_call": round(us, 2), "tokens_per_s": round(S / (us * 1e-6), 1),
+            "launches_per_call": launches, "copies": copies,
+            "roofline": {"bound": "alu", "achieved": round(tflops, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
+                         "frac": round(tflops / peak, 4),
+                         "peak_source": "FP32 FMA: %d SMs x 128 lanes x 2 FLOP x %.0f MHz (sampled)" % (sms, mhz)},
+            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks()["hbm_gbs"], 4),
+            "fma_per_call": fma, "bytes_per_call": nbytes, "clocks": ck})
+        for t in ws:
+            t.free()
+        del kvs
+        torch.cuda.empty_cache()
+    return out
+
+
 def glue_measure(q, steps, warmup, stream):
     """Layer glue: RMSNorm with a residual (h = x + r written back, y = norm(h) * w),
     D = 6144, at S = 1 (a chain of dependent calls as one CUDA graph) and
@@ -699,11 +795,13 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe", action="store_true")
-    ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill", "moe"])
+    ap.add_argument("--no-mla", action="store_true")
+    ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill", "moe", "mla"])
     ap.add_argument("--fmt", default="i4", choices=["f32", "i8", "i4", "i2"])
     ap.add_argument("--O", type=int, default=12288)
     ap.add_argument("--I", type=int, default=6144)
     ap.add_argument("--S", type=int, default=1)
+    ap.add_argument("--T", type=int, default=0, help="cached positions of the mla workload (0: its default cases)")
     ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: enough for 3x L2)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -719,6 +817,12 @@ def main():
         import quantized_weight_quant_gb300 as q
         torch.cuda.set_device(0)
         print(json.dumps(moe_measure(q, args.steps, args.warmup, torch.cuda.Stream())), flush=True)
+    elif args.workload == "mla":
+        import torch
+        import quantized_weight_quant_gb300 as q
+        torch.cuda.set_device(0)
+        cases = ((args.S, args.T),) if args.T else ((1, 4096), (4, 4096), (1, 32768))
+        print(json.dumps(mla_measure(q, args.steps, args.warmup, torch.cuda.Stream(), cases)), flush=True)
     else:
         run_ours(args)
 

@@ -310,8 +310,10 @@ int b200q_tensor_info(const b200q_tensor *t, int *fmt, int *O, int *I, int *devi
 /*
  * Synchronizes the current device and reports whether any kernel of the
  * library gave up on a bounded device-side wait since the last call
- * (B200Q_ETIMEOUT; such a kernel leaves its outputs incomplete), or a CUDA
- * error (B200Q_ECUDA).  Clears the record.  B200Q_OK otherwise.
+ * (B200Q_ETIMEOUT; such a kernel leaves its outputs incomplete), met a NULL or
+ * unaligned KV-cache page (B200Q_EINVAL, b200q_mla_absorb and
+ * b200q_kv_append; the call's outputs are then undefined), or a CUDA error
+ * (B200Q_ECUDA).  Clears the record.  B200Q_OK otherwise.
  */
 int b200q_device_status(void);
 
@@ -321,6 +323,67 @@ int b200q_device_status(void);
  * region.
  */
 long long b200q_kernel_launches(void);
+
+/*
+ * ---- MLA decode attention with weight absorption ----
+ *
+ * Source: the three-backends chapter ("第 8 章 · 02 CUDA/Metal/Vulkan 三后端"),
+ * section 四, the header of attention_absorb.comp (the Vulkan form of
+ * coli_cuda_attention_absorb); the KV pages of section 一 (COLI_KV_PAGE_TOKENS:
+ * the latent and rope caches are allocated 64 positions to a page and rows are
+ * appended at their absolute position).  For each new token s < S and head
+ * h < H:
+ *     qabs[i]    = sum_d q_nope[s,h,d] * Wk[h,d,i]               d < Dn, i < K
+ *     score_t    = (qabs . L[t] + q_rope[s,h] . Rr[t]) * scale   t in [st0, T-S+s]
+ *     p          = softmax(score)
+ *     clat[i]    = sum_t p_t * L[t,i]
+ *     ctx[s,h,v] = sum_i clat[i] * Wv[h,v,i]                     v < Dv
+ * Wk and Wv are rows of one tensor wkv_b of H * (Dn + Dv) rows and K columns
+ * (any format, per-row scales): head h's key rows are h * (Dn + Dv) + d, its
+ * value rows h * (Dn + Dv) + Dn + v; each weight is scale[row] * (code - zero
+ * point).  The S new tokens occupy positions T-S .. T-1 of the caches (append
+ * them first); token s sees positions st0 .. T-S+s.
+ */
+enum { B200Q_KV_PAGE_TOKENS = 64 };
+
+/*
+ *   wkv_b       tensor handle, O = H * (Dn + Dv), I = K; per-row scales
+ *               (group-wise scales: B200Q_EINVAL); K a multiple of 4, at most 768
+ *   q_nope      device [S, H, Dn] f32, 16-byte aligned
+ *   q_rope      device [S, H, R] f32, 16-byte aligned (unused when R = 0)
+ *   lat_pages   DEVICE array of ceil(T / 64) device pointers; page p holds
+ *               positions 64p .. 64p+63 as [64, K] f32 rows.  Every page must
+ *               be a full 64-row allocation, 16-byte aligned, non-NULL
+ *   rope_pages  the same for the rope cache, [64, R] f32 pages (unused when R = 0)
+ *   R           rope width, a multiple of 4 (K + R at most 716)
+ *   T           positions in the caches, S <= T <= 2^30
+ *   st0         first position any token sees, 0 <= st0 <= T - S; pages
+ *               wholly before st0 are never read
+ *   scale       softmax scale, finite
+ *   ctx         device [S, H, Dv] f32 output, 16-byte aligned, not
+ *               overlapping q_nope or q_rope
+ * Asynchronous on `stream`; four kernel launches; a stream-ordered workspace
+ * of about 4 * H * S * K * (1 + splits) bytes, splits <= 512 (the cache is
+ * split so that the attention kernel fills the GPU).  S = 0 is a no-op.
+ * Numerics: f32 arithmetic throughout (absorb, scores, expf softmax, latent
+ * context, value rows); within 1e-5 of the bound
+ *     (1 + max_t |scale| (sum_i QA_i |L[t,i]| + sum_j |q_rope_j Rr[t,j]|))
+ *       * sum_i |Wv[h,v,i]| * sum_t p_t |L[t,i]|,   QA_i = sum_d |q_nope_d Wk[h,d,i]|
+ * of the exact result.  A NULL or unaligned page is reported by
+ * b200q_device_status.
+ */
+int b200q_mla_absorb(const b200q_tensor *wkv_b, int H, int Dn, int Dv, const float *q_nope, const float *q_rope,
+                     const float *const *lat_pages, const float *const *rope_pages, int R, int T, int st0,
+                     float scale, float *ctx, int S, void *stream);
+
+/*
+ * Appends n rows to the paged caches at absolute positions pos .. pos+n-1
+ * (device copies; one launch): lat_rows device [n, K] f32 into lat_pages,
+ * rope_rows device [n, R] f32 into rope_pages (device page-pointer arrays as in
+ * b200q_mla_absorb).  n = 0 is a no-op.  Asynchronous on `stream`.
+ */
+int b200q_kv_append(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos, const float *lat_rows,
+                    const float *rope_rows, int n, void *stream);
 
 /* Text of the calling thread's last error ("" if none). */
 const char *b200q_last_error(void);

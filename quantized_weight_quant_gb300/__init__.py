@@ -63,6 +63,10 @@ def _load():
     L.b200q_matmul_grouped_silu.restype = ci
     L.b200q_rmsnorm.argtypes = [vp, vp, vp, vp, vp, ci, ci, cf, vp]
     L.b200q_rmsnorm.restype = ci
+    L.b200q_mla_absorb.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp, ci, ci, ci, cf, vp, ci, vp]
+    L.b200q_mla_absorb.restype = ci
+    L.b200q_kv_append.argtypes = [vp, vp, ci, ci, ci, vp, vp, ci, vp]
+    L.b200q_kv_append.restype = ci
     L.b200q_silu_mul.argtypes = [vp, vp, vp, cl, vp]
     L.b200q_silu_mul.restype = ci
     L.b200q_matmul_host.argtypes = [vp, vp, vp, ci, vp]
@@ -279,6 +283,70 @@ def rmsnorm(x, w, y, S: int, D: int, eps: float, r=None, h=None, stream=None) ->
     """y = (x + r) * w / sqrt(mean((x + r)^2) + eps) per row; h receives x + r
     when given (b200q_rmsnorm)."""
     _check(lib.b200q_rmsnorm(_dptr(x), _dptr(r), _dptr(h), _dptr(w), _dptr(y), S, D, eps, _stream(stream)))
+
+
+KV_PAGE_TOKENS = 64
+
+
+def _page_table(a) -> int:
+    """Device address of a page-pointer array: an int64 CUDA tensor or an int."""
+    if a is None:
+        return 0
+    if isinstance(a, int):
+        return a
+    import torch
+    if not a.is_cuda or a.dtype != torch.int64 or not a.is_contiguous():
+        raise ValueError("expected a contiguous int64 CUDA tensor of page pointers")
+    return a.data_ptr()
+
+
+def mla_absorb(t, H: int, Dn: int, Dv: int, q_nope, q_rope, lat_pages, rope_pages, R: int, T: int, st0: int,
+               scale: float, ctx, S: int, stream=None) -> None:
+    """MLA decode attention with weight absorption (b200q_mla_absorb): ctx
+    [S, H, Dv] from q_nope [S, H, Dn], q_rope [S, H, R] and the paged caches
+    (lat_pages / rope_pages: device arrays of page pointers, e.g. PagedKV's)."""
+    _check(lib.b200q_mla_absorb(_h(t), H, Dn, Dv, _dptr(q_nope), _dptr(q_rope), _page_table(lat_pages),
+                                _page_table(rope_pages), R, T, st0, scale, _dptr(ctx), S, _stream(stream)))
+
+
+def kv_append(lat_pages, rope_pages, K: int, R: int, pos: int, lat_rows, rope_rows, n: int, stream=None) -> None:
+    """Rows n of lat_rows [n, K] / rope_rows [n, R] into the paged caches at
+    positions pos .. pos+n-1 (b200q_kv_append)."""
+    _check(lib.b200q_kv_append(_page_table(lat_pages), _page_table(rope_pages), K, R, pos, _dptr(lat_rows),
+                               _dptr(rope_rows), n, _stream(stream)))
+
+
+class PagedKV:
+    """A paged latent / rope cache in torch device memory: pages of 64
+    positions ([64, K] and [64, R] f32) carved from one pool each, and the
+    device page tables b200q_mla_absorb reads.  `order` places logical page p
+    at pool slot order[p] (any permutation), so the tables need not be in
+    address order."""
+
+    def __init__(self, K: int, R: int, max_tokens: int, device="cuda", order=None):
+        import torch
+        n = max(1, -(-max_tokens // KV_PAGE_TOKENS))
+        self.K, self.R, self.n_pages = K, R, n
+        self.lat_pool = torch.zeros((n, KV_PAGE_TOKENS, K), dtype=torch.float32, device=device)
+        self.rope_pool = torch.zeros((n, KV_PAGE_TOKENS, max(R, 1)), dtype=torch.float32, device=device)
+        slots = list(range(n)) if order is None else [int(v) for v in order]
+        if sorted(slots) != list(range(n)):
+            raise ValueError("order must be a permutation of range(n_pages)")
+        lb, rb = self.lat_pool.data_ptr(), self.rope_pool.data_ptr()
+        self.lat_pages = torch.tensor([lb + q * KV_PAGE_TOKENS * K * 4 for q in slots], dtype=torch.int64,
+                                      device=device)
+        self.rope_pages = torch.tensor([rb + q * KV_PAGE_TOKENS * max(R, 1) * 4 for q in slots],
+                                       dtype=torch.int64, device=device)
+        self.slots = slots
+
+    def append(self, lat_rows, rope_rows, pos: int, n: int, stream=None) -> None:
+        kv_append(self.lat_pages, self.rope_pages if self.R else None, self.K, self.R, pos, lat_rows,
+                  rope_rows if self.R else None, n, stream)
+
+    def attend(self, t, H: int, Dn: int, Dv: int, q_nope, q_rope, T: int, st0: int, scale: float, ctx, S: int,
+               stream=None) -> None:
+        mla_absorb(t, H, Dn, Dv, q_nope, q_rope, self.lat_pages, self.rope_pages if self.R else None, self.R, T,
+                   st0, scale, ctx, S, stream)
 
 
 def matmul_host(t, x_host, y_host, S: int, stream=None) -> None:

@@ -31,6 +31,15 @@ cudaError_t launch_decode_group(const Tensor *const *ts, int n, const float *con
                                 float *const *ys, bool silu, int S, cudaStream_t st, bool *handled);
 cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st);
 cudaError_t workspace_free(void *ptr, cudaStream_t st);
+size_t mla_smem_bytes(int K, int R);
+int mla_max_latent();
+size_t mla_workspace_floats(int H, int S, int K, int T, int st0);
+cudaError_t launch_mla_absorb(const Tensor &w, int H, int Dn, int Dv, const float *q_nope, const float *q_rope,
+                              const float *const *lat_pages, const float *const *rope_pages, int R, int T, int st0,
+                              float scale, float *ctx, int S, float *ws, cudaStream_t st);
+cudaError_t launch_kv_append(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos,
+                             const float *lat_rows, const float *rope_rows, int n, cudaStream_t st);
+cudaError_t mla_take_error(unsigned int *code);
 
 namespace {
 
@@ -167,11 +176,14 @@ long long b200q_kernel_launches(void) { return g_launches.load(std::memory_order
 int b200q_device_status(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "b200q_device_status");
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, m = 0;
     e = decode_take_error(&a);
     if (e == cudaSuccess) e = prefill_take_error(&b);
+    if (e == cudaSuccess) e = mla_take_error(&m);
     if (e != cudaSuccess) return cuda_fail(e, "b200q_device_status");
-    if (a || b) return fail(B200Q_ETIMEOUT, "b200q_device_status: a kernel gave up on a bounded wait");
+    if (a || b || m == (unsigned)(-B200Q_ETIMEOUT))
+        return fail(B200Q_ETIMEOUT, "b200q_device_status: a kernel gave up on a bounded wait");
+    if (m) return fail(B200Q_EINVAL, "b200q_device_status: an MLA call met a NULL or unaligned cache page");
     return B200Q_OK;
 }
 
@@ -589,6 +601,68 @@ int b200q_matmul_host(const b200q_tensor *h, const float *x_host, float *y_host,
     e = cudaMemcpyAsync(y_host, yd, yb, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "b200q_matmul_host: copy y to host");
+    return B200Q_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int b200q_mla_absorb(const b200q_tensor *wkv_b, int H, int Dn, int Dv, const float *q_nope, const float *q_rope,
+                     const float *const *lat_pages, const float *const *rope_pages, int R, int T, int st0,
+                     float scale, float *ctx, int S, void *stream) {
+    const char *who = "b200q_mla_absorb";
+    int rc = check_tensor(wkv_b, who);
+    if (rc) return rc;
+    const Tensor &w = *reinterpret_cast<const Tensor *>(wkv_b);
+    if (S < 0) return fail(B200Q_EINVAL, "%s: S must be >= 0 (got %d)", who, S);
+    if (S == 0) return B200Q_OK;
+    if (H < 1 || Dn < 1 || Dv < 1 || R < 0)
+        return fail(B200Q_EINVAL, "%s: need H, Dn, Dv >= 1 and R >= 0 (got %d, %d, %d, %d)", who, H, Dn, Dv, R);
+    if ((long long)H * (Dn + Dv) != w.O)
+        return fail(B200Q_EINVAL, "%s: the tensor has %d rows, H * (Dn + Dv) = %lld", who, w.O,
+                    (long long)H * (Dn + Dv));
+    if (w.gs) return fail(B200Q_EINVAL, "%s: the weight tensor must have per-row scales", who);
+    const int K = w.I;
+    if (K % 4 || R % 4 || K > mla_max_latent())
+        return fail(B200Q_EINVAL, "%s: need K and R multiples of 4 and K <= %d (got K=%d, R=%d)", who,
+                    mla_max_latent(), K, R);
+    if (mla_smem_bytes(K, R) > 227 * 1024)
+        return fail(B200Q_EINVAL, "%s: K + R = %d is too wide for one tile in shared memory", who, K + R);
+    if (T < S || st0 < 0 || st0 > T - S || T > (1 << 30))
+        return fail(B200Q_EINVAL, "%s: need S <= T <= 2^30 and 0 <= st0 <= T - S (got T=%d, st0=%d, S=%d)", who, T,
+                    st0, S);
+    if ((long long)H * S > (1 << 20)) return fail(B200Q_EINVAL, "%s: H * S above 2^20", who);
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return fail(B200Q_EINVAL, "%s: scale must be finite", who);
+    if (!q_nope || !ctx || !lat_pages || (R && (!q_rope || !rope_pages)))
+        return fail(B200Q_EINVAL, "%s: device pointers must not be NULL", who);
+    if (!aligned16(q_nope) || !aligned16(ctx) || (R && !aligned16(q_rope)) || ((uintptr_t)lat_pages & 7u) ||
+        (R && ((uintptr_t)rope_pages & 7u)))
+        return fail(B200Q_EINVAL, "%s: q_nope, q_rope and ctx must be 16-byte aligned, the page arrays 8-byte", who);
+    const size_t cb = (size_t)S * H * Dv * 4;
+    if (overlap(ctx, cb, q_nope, (size_t)S * H * Dn * 4) || (R && overlap(ctx, cb, q_rope, (size_t)S * H * R * 4)))
+        return fail(B200Q_EINVAL, "%s: ctx must not overlap q_nope or q_rope", who);
+    cudaStream_t st = (cudaStream_t)stream;
+    float *ws = nullptr;
+    cudaError_t e = workspace_alloc((void **)&ws, mla_workspace_floats(H, S, K, T, st0) * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    e = launch_mla_absorb(w, H, Dn, Dv, q_nope, q_rope, lat_pages, rope_pages, R, T, st0, scale, ctx, S, ws, st);
+    cudaError_t e2 = workspace_free(ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    if (e2 != cudaSuccess) return cuda_fail(e2, who);
+    return B200Q_OK;
+}
+
+int b200q_kv_append(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos, const float *lat_rows,
+                    const float *rope_rows, int n, void *stream) {
+    const char *who = "b200q_kv_append";
+    if (n < 0 || K < 1 || R < 0 || pos < 0 || (long long)pos + n > (1ll << 30))
+        return fail(B200Q_EINVAL, "%s: need n >= 0, K >= 1, R >= 0, 0 <= pos, pos + n <= 2^30", who);
+    if (n == 0) return B200Q_OK;
+    if (!lat_pages || !lat_rows || (R && (!rope_pages || !rope_rows)))
+        return fail(B200Q_EINVAL, "%s: device pointers must not be NULL", who);
+    cudaError_t e = launch_kv_append(lat_pages, rope_pages, K, R, pos, lat_rows, rope_rows, n, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, who);
     return B200Q_OK;
 }
 

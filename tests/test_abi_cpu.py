@@ -124,3 +124,19 @@ def test_rmsnorm_argument_errors_without_gpu(built_lib):
     assert L.b200q_rmsnorm(16, None, None, 32, 48 + 4, 1, 8, 1e-6, None) == q.EINVAL    # misaligned y
     assert L.b200q_rmsnorm(4096, None, None, 0x10000, 4096 + 16, 1, 8, 1e-6, None) == q.EINVAL   # y overlaps x
     assert "overlap" in q.last_error()
+
+
+def test_mla_argument_errors_without_gpu(built_lib):
+    import quantized_weight_quant_gb300 as q
+    L = q.lib
+    # no tensor: refused before anything touches a device
+    assert L.b200q_mla_absorb(None, 2, 4, 4, 16, 32, 48, 64, 4, 8, 0, 0.5, 80, 1, None) == q.EINVAL
+    assert "NULL" in q.last_error() or "tensor" in q.last_error()
+    # cache appends: bad counts and NULL pointers
+    assert L.b200q_kv_append(16, 32, 8, 4, 0, 48, 64, -1, None) == q.EINVAL
+    assert L.b200q_kv_append(16, 32, 8, 4, -3, 48, 64, 2, None) == q.EINVAL
+    assert L.b200q_kv_append(None, 32, 8, 4, 0, 48, 64, 2, None) == q.EINVAL
+    assert "NULL" in q.last_error()
+    assert L.b200q_kv_append(16, None, 8, 4, 0, 48, None, 2, None) == q.EINVAL
+    assert L.b200q_kv_append(16, None, 8, 0, 0, 48, None, 0, None) == q.OK     # n = 0: no-op
+    assert q.KV_PAGE_TOKENS == 64
