@@ -212,9 +212,12 @@ __device__ __forceinline__ float reduce16(float (&v)[16], int lane) {
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+// KT, RT > 0: latent and rope widths fixed at compile time (strides and
+// loop bounds resolved by the compiler); 0: taken from p.
+template <int KT, int RT>
 __global__ void __launch_bounds__(kAttnThreads, 1) mla_attn_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int K = p.K, R = p.R, KR = K + R, HS = p.H * p.S;
+    const int K = KT ? KT : p.K, R = KT ? RT : p.R, KR = K + R, HS = p.H * p.S;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *qs = reinterpret_cast<float *>(smem);       // [kRows][KR]: qabs | q_rope
     float *ls = qs + kRows * KR;                        // [2][kTile][K]
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) mla_attn_kernel(const __grid_
                     acc[mi][q].z *= al[mi];
                     acc[mi][q].w *= al[mi];
                 }
-            for (int t = tv0; t < tv1; ++t) {
+            auto add_position = [&](int t) {
                 const float4 pv = *reinterpret_cast<const float4 *>(ps + t * kRows + mg * 4);
                 const float pm[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
@@ -428,6 +431,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) mla_attn_kernel(const __grid_
                         }
                     }
                 }
+            };
+            if (tv0 == 0 && tv1 == kTile) {           // a whole tile: fixed trip count
+#pragma unroll 8
+                for (int t = 0; t < kTile; ++t) add_position(t);
+            } else {
+                for (int t = tv0; t < tv1; ++t) add_position(t);
             }
         }
         __syncthreads();   // slot and weights free: refill the slot with tile j + 2
@@ -725,10 +734,17 @@ cudaError_t launch_mla_absorb(const Tensor &w, int H, int Dn, int Dv, const floa
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = mla_smem_bytes(K, R);
-    e = allow_smem(mla_attn_kernel, smem, &attr[dev & 63]);
-    if (e != cudaSuccess) return e;
     dim3 grid(n_split, (HS + kRows - 1) / kRows);
-    mla_attn_kernel<<<grid, kAttnThreads, smem, st>>>(p);
+    if (K == 512 && R == 64) {      // the pages' model shape: widths fixed at compile time
+        e = allow_smem(mla_attn_kernel<512, 64>, smem, &attr[dev & 63]);
+        if (e != cudaSuccess) return e;
+        mla_attn_kernel<512, 64><<<grid, kAttnThreads, smem, st>>>(p);
+    } else {
+        static bool attr_g[64] = {};
+        e = allow_smem(mla_attn_kernel<0, 0>, smem, &attr_g[dev & 63]);
+        if (e != cudaSuccess) return e;
+        mla_attn_kernel<0, 0><<<grid, kAttnThreads, smem, st>>>(p);
+    }
     count_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
