@@ -13,9 +13,9 @@
 // positions 64p .. 64p+63 as [64, K] and [64, R] f32 rows.
 //
 // Four kernels.
-//   1. absorb: one CTA per (head, 32 code words of a row, 4 tokens); its 8
-//      warps take every 8th key row, each lane one 32-bit word of codes, and
-//      the 8 partial sums are added in warp order.
+//   1. absorb: one CTA per (head, 32 code words of a row, 4 tokens); its 16
+//      warps take every 16th key row, each lane one 32-bit word of codes, and
+//      the 16 partial sums are added in warp order.
 //   2. attention partials, split over the cache (flash-decoding): a CTA owns
 //      16 (head, token) rows and a contiguous run of 32-position tiles.  One
 //      thread streams the tiles into a two-slot shared-memory ring with bulk
@@ -95,12 +95,12 @@ struct Word<B200Q_I2> {
 
 // ---------------------------------------------------------------- absorb
 template <int FMT>
-__global__ void __launch_bounds__(256) mla_absorb_kernel(const uint8_t *__restrict__ codes,
+__global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restrict__ codes,
                                                          const float *__restrict__ scales, long long ld, int H,
                                                          int Dn, int Dv, int K, const float *__restrict__ q_nope,
                                                          int S, float *__restrict__ qabs) {
     constexpr int EW = Word<FMT>::EW;
-    constexpr int kPh = 8;                              // warps = row phases
+    constexpr int kPh = 16;                             // warps = row phases
     extern __shared__ float red[];                      // [kPh][kTokBlock][EW][32]
     const int h = blockIdx.x, s0 = blockIdx.z * kTokBlock;
     const int ns = min(kTokBlock, S - s0);
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(256) mla_absorb_kernel(const uint8_t *__restri
 #pragma unroll
         for (int e = 0; e < EW; ++e) acc[t][e] = 0.f;
     if (word < nwords) {
-        constexpr int kB = 16;                          // rows per batch: all their loads in flight
+        constexpr int kB = EW >= 16 ? 4 : 8;            // rows per batch: all their loads in flight
         for (int d0 = ph; d0 < Dn; d0 += kPh * kB) {
             uint32_t wb[kB];
             float u[kB][kTokBlock];
@@ -478,9 +478,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) mla_attn_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per (row, 128 latent columns): split weights exp(m_z - max) in
-// shared memory, then each thread sums its column over the splits in a fixed
-// order, 16 loads in flight.
+// One CTA per (row, 128 latent columns): each thread issues the loads of its
+// column's partials first (64 at a time), warp 0 meanwhile forms the split
+// weights exp(m_z - max) in shared memory, then the column is summed over the
+// splits in a fixed order.
 constexpr int kCombThreads = 128;
 
 __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float *__restrict__ part_m,
@@ -491,6 +492,13 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float *
     __shared__ float inv_l;
     const int r = blockIdx.x, i = blockIdx.y * kCombThreads + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the first kB partials of this column go out before the split weights are
+    // formed (they do not depend on them)
+    constexpr int kB = 64;
+    float pv[kB];
+#pragma unroll
+    for (int b = 0; b < kB; ++b)
+        pv[b] = i < K && b < n_split ? part_c[((long long)b * HS + r) * K + i] : 0.f;
     if (warp == 0) {
         float mx = -INFINITY;
         for (int z = lane; z < n_split; z += 32) mx = fmaxf(mx, part_m[(long long)z * HS + r]);
@@ -509,10 +517,11 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float *
     }
     __syncthreads();
     if (i >= K) return;
-    constexpr int kB = 16;
     float c = 0.f;
-    for (int z0 = 0; z0 < n_split; z0 += kB) {
-        float pv[kB];
+#pragma unroll
+    for (int b = 0; b < kB; ++b)
+        if (b < n_split) c = fmaf(wz[b], pv[b], c);
+    for (int z0 = kB; z0 < n_split; z0 += kB) {      // more than kB splits: further batches
 #pragma unroll
         for (int b = 0; b < kB; ++b) pv[b] = z0 + b < n_split ? part_c[((long long)(z0 + b) * HS + r) * K + i] : 0.f;
 #pragma unroll
@@ -641,12 +650,12 @@ cudaError_t run_absorb(const Tensor &w, int H, int Dn, int Dv, const float *q_no
     static bool attr[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = (size_t)8 * kTokBlock * EW * 32 * 4;
+    const size_t smem = (size_t)16 * kTokBlock * EW * 32 * 4;   // int2: 128 KB
     cudaError_t e = allow_smem(mla_absorb_kernel<FMT>, smem, &attr[dev & 63]);
     if (e != cudaSuccess) return e;
     const int K = w.I, nwords = (K + EW - 1) / EW;
     dim3 grid(H, (nwords + 31) / 32, (S + kTokBlock - 1) / kTokBlock);
-    mla_absorb_kernel<FMT><<<grid, 256, smem, st>>>(w.codes, w.scales, w.ld, H, Dn, Dv, K, q_nope, S, qabs);
+    mla_absorb_kernel<FMT><<<grid, 512, smem, st>>>(w.codes, w.scales, w.ld, H, Dn, Dv, K, q_nope, S, qabs);
     count_launch();
     return cudaGetLastError();
 }
