@@ -58,6 +58,16 @@ __device__ unsigned int g_mla_err = 0;        // first error a kernel recorded (
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_mla_err, 0u, (unsigned)(-code)); }
 
+// Programmatic dependent launch: every kernel here is launched so that it may
+// start while the previous kernel in the stream drains.  Each thread runs
+// dependency_wait() before its first read of another kernel's output and
+// before its first global write (the stream-ordered workspace may be memory a
+// previous call still reads); work on the weights comes before it.
+__device__ __forceinline__ void dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- 32-bit word of codes -> EW exact values (code - zero point), by the
 // 2^23 + field trick: the field sits in the mantissa of 2^23, one subtraction.
 template <int FMT>
@@ -113,23 +123,33 @@ __global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restri
     for (int t = 0; t < kTokBlock; ++t)
 #pragma unroll
         for (int e = 0; e < EW; ++e) acc[t][e] = 0.f;
+    bool waited = false;
     if (word < nwords) {
         constexpr int kB = EW >= 16 ? 4 : 8;            // rows per batch: all their loads in flight
         for (int d0 = ph; d0 < Dn; d0 += kPh * kB) {
             uint32_t wb[kB];
+            float sc[kB];
             float u[kB][kTokBlock];
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
                 const int d = d0 + b * kPh;
                 wb[b] = 0u;
-                float sc = 0.f;
+                sc[b] = 0.f;
                 if (d < Dn) {
                     wb[b] = __ldg(reinterpret_cast<const uint32_t *>(codes + (key0 + d) * ld) + word);
-                    sc = __ldg(scales + key0 + d);
+                    sc[b] = __ldg(scales + key0 + d);
                 }
+            }
+            if (!waited) {                               // q_nope comes from the previous kernel
+                dependency_wait();
+                waited = true;
+            }
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int d = d0 + b * kPh;
 #pragma unroll
                 for (int t = 0; t < kTokBlock; ++t)
-                    u[b][t] = d < Dn && t < ns ? __ldg(q_nope + ((long long)(s0 + t) * H + h) * Dn + d) * sc : 0.f;
+                    u[b][t] = d < Dn && t < ns ? __ldg(q_nope + ((long long)(s0 + t) * H + h) * Dn + d) * sc[b] : 0.f;
             }
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
@@ -142,6 +162,7 @@ __global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restri
             }
         }
     }
+    if (!waited) dependency_wait();
 #pragma unroll
     for (int t = 0; t < kTokBlock; ++t)
 #pragma unroll
@@ -238,6 +259,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) mla_attn_kernel(const __grid_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    dependency_wait();   // qabs (and the cache rows appended before it) come from earlier kernels
 
     // thread 0: tile j of this CTA's run into slot j & 1
     auto issue = [&](int j) {
@@ -492,6 +514,7 @@ __global__ void __launch_bounds__(kCombThreads) mla_combine_kernel(const float *
     __shared__ float inv_l;
     const int r = blockIdx.x, i = blockIdx.y * kCombThreads + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    dependency_wait();
     // the first kB partials of this column go out before the split weights are
     // formed (they do not depend on them)
     constexpr int kB = 64;
@@ -550,11 +573,6 @@ __global__ void __launch_bounds__(kValThreads) mla_value_kernel(const uint8_t *_
     const int h = blockIdx.x, s0 = blockIdx.z * kTokBlock;
     const int ns = min(kTokBlock, S - s0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int idx = threadIdx.x; idx < ns * K / 4; idx += blockDim.x) {
-        const int t = idx / (K / 4), i4 = idx - t * (K / 4);
-        reinterpret_cast<float4 *>(clat)[idx] =     // clat rows are (head, token), head-major
-            reinterpret_cast<const float4 *>(clat_g + ((long long)h * S + s0 + t) * K)[i4];
-    }
     const int nwords = (K + EW - 1) / EW;
     const long long val0 = (long long)h * (Dn + Dv) + Dn;
     const int v0 = blockIdx.y * kValRows + warp * 4;
@@ -567,6 +585,12 @@ __global__ void __launch_bounds__(kValThreads) mla_value_kernel(const uint8_t *_
         sc[k] = live ? __ldg(scales + val0 + v0 + k) : 0.f;
 #pragma unroll
         for (int b = 0; b < kWL; ++b) cw[k][b] = live && lane + 32 * b < nwords ? __ldg(row + lane + 32 * b) : 0u;
+    }
+    dependency_wait();   // clat comes from the combine kernel
+    for (int idx = threadIdx.x; idx < ns * K / 4; idx += blockDim.x) {
+        const int t = idx / (K / 4), i4 = idx - t * (K / 4);
+        reinterpret_cast<float4 *>(clat)[idx] =     // clat rows are (head, token), head-major
+            reinterpret_cast<const float4 *>(clat_g + ((long long)h * S + s0 + t) * K)[i4];
     }
     __syncthreads();
     float a[4][kTokBlock];
@@ -635,6 +659,23 @@ __global__ void kv_append_kernel(float *const *lat_pages, float *const *rope_pag
 
 int g_sms = 0;
 
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
+    count_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <class Kern>
 cudaError_t allow_smem(Kern k, size_t bytes, bool *done) {
     if (bytes <= 48 * 1024 || *done) return cudaSuccess;
@@ -655,9 +696,8 @@ cudaError_t run_absorb(const Tensor &w, int H, int Dn, int Dv, const float *q_no
     if (e != cudaSuccess) return e;
     const int K = w.I, nwords = (K + EW - 1) / EW;
     dim3 grid(H, (nwords + 31) / 32, (S + kTokBlock - 1) / kTokBlock);
-    mla_absorb_kernel<FMT><<<grid, 512, smem, st>>>(w.codes, w.scales, w.ld, H, Dn, Dv, K, q_nope, S, qabs);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(mla_absorb_kernel<FMT>, grid, dim3(512), smem, st, (const uint8_t *)w.codes,
+                      (const float *)w.scales, (long long)w.ld, H, Dn, Dv, K, q_nope, S, qabs);
 }
 
 template <int FMT>
@@ -666,9 +706,8 @@ cudaError_t run_value(const Tensor &w, int H, int Dn, int Dv, int S, const float
     const int K = w.I;
     const size_t smem = (size_t)kTokBlock * K * 4;     // <= 12 KB
     dim3 grid(H, (Dv + kValRows - 1) / kValRows, (S + kTokBlock - 1) / kTokBlock);
-    mla_value_kernel<FMT><<<grid, kValThreads, smem, st>>>(w.codes, w.scales, w.ld, H, Dn, Dv, K, S, clat, ctx);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(mla_value_kernel<FMT>, grid, dim3(kValThreads), smem, st, (const uint8_t *)w.codes,
+                      (const float *)w.scales, (long long)w.ld, H, Dn, Dv, K, S, (const float *)clat, ctx);
 }
 
 }  // namespace
@@ -747,24 +786,20 @@ cudaError_t launch_mla_absorb(const Tensor &w, int H, int Dn, int Dv, const floa
     if (K == 512 && R == 64) {      // the pages' model shape: widths fixed at compile time
         e = allow_smem(mla_attn_kernel<512, 64>, smem, &attr[dev & 63]);
         if (e != cudaSuccess) return e;
-        mla_attn_kernel<512, 64><<<grid, kAttnThreads, smem, st>>>(p);
+        e = launch_pdl(mla_attn_kernel<512, 64>, grid, dim3(kAttnThreads), smem, st, p);
     } else {
         static bool attr_g[64] = {};
         e = allow_smem(mla_attn_kernel<0, 0>, smem, &attr_g[dev & 63]);
         if (e != cudaSuccess) return e;
-        mla_attn_kernel<0, 0><<<grid, kAttnThreads, smem, st>>>(p);
+        e = launch_pdl(mla_attn_kernel<0, 0>, grid, dim3(kAttnThreads), smem, st, p);
     }
-    count_launch();
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     // the splits merged into clat (the qabs buffer, which the attention
     // kernel has finished with), then the value rows
     float *clat = qabs;
-    mla_combine_kernel<<<dim3(HS, (K + kCombThreads - 1) / kCombThreads), kCombThreads, 0, st>>>(pm, pl, pc, n_split,
-                                                                                               HS, K, clat);
-    count_launch();
-    e = cudaGetLastError();
+    e = launch_pdl(mla_combine_kernel, dim3(HS, (K + kCombThreads - 1) / kCombThreads), dim3(kCombThreads), 0, st,
+                   (const float *)pm, (const float *)pl, (const float *)pc, n_split, HS, K, clat);
     if (e != cudaSuccess) return e;
     switch (w.fmt) {
     case B200Q_F32: return run_value<B200Q_F32>(w, H, Dn, Dv, S, clat, ctx, st);
