@@ -323,14 +323,20 @@ def cpu_baseline_decode(O, I, S, fmt=I4, seconds=3.0):
             "sample": "full O=%d I=%d S=%d int4 matmul, %d calls in %.1f s" % (O, I, S, n, dt)}
 
 
-def prefill_measure(q, steps, warmup, stream):
+def prefill_measure(q, steps, warmup, stream, gs=0):
     """W4A16 prefill O=12288, I=6144, S=1571 through b200q_matmul (tensor-core
-    path); returns None while that path is not available."""
+    path; gs > 0: group-wise scales, one per row and gs columns); returns None
+    while that path is not available."""
     import torch
     import synth
     O, I, S = 12288, 6144, 1571
-    codes, scales = synth.quant_tensor(I4, O, I, 0, 1, 5e-3, 2e-2)
-    t = q.tensor_upload(I4, O, I, codes, scales)
+    if gs:
+        codes = synth.codes(I4, O, I, 0, 1)
+        scales = synth.uniform_f32((O, -(-I // gs)), 5e-3, 2e-2, 0, 2)
+        t = q.tensor_upload(I4, O, I, codes, scales, gs=gs)
+    else:
+        codes, scales = synth.quant_tensor(I4, O, I, 0, 1, 5e-3, 2e-2)
+        t = q.tensor_upload(I4, O, I, codes, scales)
     try:
         if q.matmul_path(t, S) != q.PATH_TC:
             return None
@@ -476,11 +482,13 @@ def run_sweep(args):
     print(json.dumps(glue_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)), flush=True)
     pf = prefill_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream)
     print(json.dumps({"workload": "prefill W4A16 12288x6144 S=1571", "result": pf}), flush=True)
+    pf = prefill_measure(q, max(5, min(args.steps, 20)), max(3, args.warmup), stream, gs=128)
+    print(json.dumps({"workload": "prefill W4A16 12288x6144 S=1571 gs=128", "result": pf}), flush=True)
 
 
 def run_single(args):
     """One configuration (for profiling runs): --workload decode|prefill with
-    --fmt/--O/--I/--S/--copies; one JSON line."""
+    --fmt/--O/--I/--S/--copies (--gs: group-wise scales); one JSON line."""
     import torch
     import quantized_weight_quant_gb300 as q
     torch.cuda.set_device(0)
@@ -490,10 +498,11 @@ def run_single(args):
     bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
     per = algorithmic_bytes(bits, args.O, args.I, args.S)
     R = args.copies or max(2, min(64, -(-3 * L2_BYTES // per)))
-    wl = Decode(q, fmt, args.O, args.I, args.S, R)
+    wl = Decode(q, fmt, args.O, args.I, args.S, R, gs=args.gs)
     ms, launches = time_steps(wl, args.steps, args.warmup, stream)
     sec = ms * 1e-3
-    print(json.dumps({"workload": "%s %s O=%d I=%d S=%d" % (args.workload, args.fmt, args.O, args.I, args.S),
+    print(json.dumps({"workload": "%s %s O=%d I=%d S=%d gs=%d" % (args.workload, args.fmt, args.O, args.I, args.S,
+                                                                  args.gs),
                       "path": q.matmul_path(wl.tensors[0], args.S),
                       "GB/s": round(wl.bytes_per_step * args.steps / sec / 1e9, 1),
                       "frac_hbm": round(wl.bytes_per_step * args.steps / sec / 1e9 / pk["hbm_gbs"], 4),
@@ -801,6 +810,7 @@ def main():
     ap.add_argument("--O", type=int, default=12288)
     ap.add_argument("--I", type=int, default=6144)
     ap.add_argument("--S", type=int, default=1)
+    ap.add_argument("--gs", type=int, default=0, help="group size of the scales (0: one per row)")
     ap.add_argument("--T", type=int, default=0, help="cached positions of the mla workload (0: its default cases)")
     ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: enough for 3x L2)")
     args = ap.parse_args()

@@ -106,9 +106,14 @@ b200q_tensor *b200q_tensor_upload(int fmt, int O, int I, const void *codes, cons
  *           B200Q_EINVAL otherwise
  *   scales  HOST pointer to [O, ceil(I / gs)] floats, row-major; the last
  *           group of a row may be short
- * Such tensors run on the f32 path's SIMT kernel at every S (the bound is
- * taken with the group scales); the tensor-core paths and
- * b200q_matmul_tc_noalloc refuse them (B200Q_EINVAL).
+ * Paths (the bound is taken with the group scales):
+ *   - the f32 path: the decode kernel below 16 rows, the SIMT kernel beyond;
+ *   - int8 / int4, the bf16 tensor-core path (AUTO from b200q_tc_min_s()
+ *     rows, and b200q_matmul_tc_noalloc): the dequantizer forms
+ *     bf16((code - zero point) * scale) with one rounding per weight, like
+ *     the bf16 rounding of x, so that path's 4e-3 bar still holds;
+ *   - the three-piece path (B200Q_PATH_TCX) refuses them (B200Q_EINVAL): a
+ *     rounded weight would break its f32 accuracy.
  */
 b200q_tensor *b200q_tensor_upload_grouped(int fmt, int O, int I, int gs, const void *codes, const float *scales);
 

@@ -130,13 +130,14 @@ int tcx_min_s() {
 }
 
 // AUTO: int8 / int4 take the bf16 tensor-core path from tc_min_s() rows, the
-// f32-accurate tensor-core path (x in three bf16 pieces) from tcx_min_s()
-// rows, the SIMT f32 path below; f32 and int2 tensors always the SIMT path.
+// f32-accurate tensor-core path (x in three bf16 pieces; per-row scales only)
+// from tcx_min_s() rows, the SIMT f32 path below; f32 and int2 tensors always
+// the SIMT path.
 int select_path(const Tensor &t, int S, int path) {
     if (path != B200Q_PATH_AUTO) return path;
-    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8 || t.gs) return B200Q_PATH_F32;
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return B200Q_PATH_F32;
     if (S >= tc_min_s()) return B200Q_PATH_TC;
-    if (S >= tcx_min_s()) return B200Q_PATH_TCX;
+    if (!t.gs && S >= tcx_min_s()) return B200Q_PATH_TCX;
     return B200Q_PATH_F32;
 }
 
@@ -149,8 +150,9 @@ int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, floa
     if (path == B200Q_PATH_TC || path == B200Q_PATH_TCX) {
         if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
             return fail(B200Q_EINVAL, "%s: the tensor-core paths take int8 and int4 tensors only", who);
-        if (t.gs || (tu && tu->gs))
-            return fail(B200Q_EINVAL, "%s: tensors with group-wise scales run on the f32 path only", who);
+        if (path == B200Q_PATH_TCX && (t.gs || (tu && tu->gs)))
+            return fail(B200Q_EINVAL,
+                        "%s: tensors with group-wise scales take the f32 and the bf16 tensor-core paths only", who);
         e = path == B200Q_PATH_TC ? launch_prefill_tc(t, tu, x, y, yu, S, st, &handled)
                                   : launch_tcx(t, tu, x, y, yu, S, st, &handled);
         if (e == cudaSuccess && !handled)
@@ -510,8 +512,8 @@ int b200q_matmul_tc_noalloc(const b200q_tensor *h, const float *x, float *y, int
     int rc = check_tensor(h, "b200q_matmul_tc_noalloc");
     if (rc) return rc;
     const Tensor &t = *reinterpret_cast<const Tensor *>(h);
-    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8 || t.gs)
-        return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: takes int8 and int4 tensors with per-row scales only");
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
+        return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: takes int8 and int4 tensors only");
     if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul_tc_noalloc: S must be >= 0 (got %d)", S);
     if (S == 0) return B200Q_OK;
     const size_t need = (size_t)S * (size_t)t.k_pad * 2;

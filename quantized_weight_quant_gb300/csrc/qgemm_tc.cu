@@ -201,6 +201,45 @@ __device__ __forceinline__ uint2 deq_i8_word(uint32_t w) {
     return make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
 }
 
+// Group-wise scales.  The group scale s is split into bf16 parts s_hi =
+// bf16(s), s_lo = bf16(s - s_hi) (together s to ~2^-17); a pair of exact bf16
+// codes c becomes fma(c, s_hi, bf16(c * s_lo)), rounded once: the product
+// c * s_hi is exact inside the FMA and the correction term carries an error
+// of at most 2^-17 |c s|, so each weight is c * s rounded to bf16 (relative
+// error 2^-9 + 2^-16), like the bf16 rounding of x.
+struct ScalePair {
+    uint32_t hi, lo;   // (s_hi, s_hi) and (s_lo, s_lo) as bf16x2
+};
+
+__device__ __forceinline__ ScalePair split_scale(float s) {
+    const uint32_t h = pack_bf16(s, s);
+    const float sh = __uint_as_float(h << 16);
+    const float sl = s - sh;                        // exact in f32
+    return ScalePair{h, pack_bf16(sl, sl)};
+}
+
+__device__ __forceinline__ uint32_t scale_pair(uint32_t b2, const ScalePair &sp) {
+    uint32_t t, r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(b2), "r"(sp.lo));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(b2), "r"(sp.hi), "r"(t));
+    return r;
+}
+
+__device__ __forceinline__ uint4 scale_word4(uint4 e, const ScalePair &sp) {
+    return make_uint4(scale_pair(e.x, sp), scale_pair(e.y, sp), scale_pair(e.z, sp), scale_pair(e.w, sp));
+}
+
+// Division by the group size as a multiply and a shift (exact for
+// 0 <= n < 2^31): m = ceil(2^(31+c) / gs), c = ceil(log2 gs).
+struct GroupDiv {
+    uint32_t m;
+    int sh;
+};
+
+__device__ __forceinline__ int group_of(int n, const GroupDiv &d) {
+    return (int)(((unsigned long long)(unsigned)n * d.m) >> d.sh);
+}
+
 struct GemmParams {
     const float *scales;
     const float2 *unscale;   // x pieces: per token, 2^-k as two exact factors
@@ -208,12 +247,21 @@ struct GemmParams {
     int O, S;
     int m_tiles, n_tiles, nk;
     int code_bytes;      // bytes of one code tile row per k-block (32 int4, 64 int8)
+    int g_ld;            // group-wise scales: row stride of scales (floats)
+    int g_last;          // last group index a padded column may reach (clamp)
+    int g_one;           // a thread's 32 columns of a k-block lie in one group (gs % 32 == 0)
+    GroupDiv gdiv;       // by the group size
 };
 
 // BNT: columns of the B tile (tokens, or x pieces).  PIECES: B holds three
 // bf16 pieces per token (rows 3s, 3s+1, 3s+2, summing to x exactly) and the
-// epilogue adds each token's three columns.
-template <int FMT, int BNT, bool PIECES>
+// epilogue adds each token's three columns.  GS: group-wise scales, applied
+// by the dequantizers (A = bf16((code - zero point) * scale[o, group]), one
+// rounding per weight, see scale_pair); the epilogue then applies no row
+// scale.  An int4
+// code word (8 columns) or an int8 16-byte chunk (16 columns) always lies in
+// one group (gs is a multiple of 16 for int8, of 16 or 32 for int4).
+template <int FMT, int BNT, bool PIECES, bool GS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const GemmParams p) {
@@ -332,8 +380,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
+        // group-wise scales of the thread's 4 code words (int4) or 2 chunks
+        // (int8) of k-block kb, loaded one k-block ahead
+        constexpr int kGW = FMT == B200Q_I4 ? 4 : 2;
+        constexpr int kGCols = FMT == B200Q_I4 ? 8 : 16;
+        float gsn[kGW];
+        ScalePair gsc[kGW];
+        auto load_gs = [&](int tile, int kb, float(&dst)[kGW]) {
+            const long long o = (long long)(tile / p.n_tiles) * BM + r;
+            if (p.g_one) {                               // one group for all of the thread's columns
+                dst[0] = __ldg(p.scales + o * p.g_ld + min(group_of(kb * BK + 32 * half, p.gdiv), p.g_last));
+                return;
+            }
+#pragma unroll
+            for (int i = 0; i < kGW; ++i) {
+                const int g = min(group_of(kb * BK + 32 * half + kGCols * i, p.gdiv), p.g_last);
+                dst[i] = __ldg(p.scales + o * p.g_ld + g);
+            }
+        };
+        if (GS && blockIdx.x < n_tiles_total) load_gs(blockIdx.x, 0, gsn);
         for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
             for (int kb = 0; kb < p.nk; ++kb) {
+                if constexpr (GS) {
+                    if (p.g_one) {
+                        const ScalePair sp = split_scale(gsn[0]);
+#pragma unroll
+                        for (int i = 0; i < kGW; ++i) gsc[i] = sp;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kGW; ++i) gsc[i] = split_scale(gsn[i]);
+                    }
+                    if (kb + 1 < p.nk) load_gs(tile, kb + 1, gsn);
+                    else if (tile + (int)gridDim.x < n_tiles_total) load_gs(tile + gridDim.x, 0, gsn);
+                }
                 if (!mbar_wait(smem_u32(&tma_full[stage]), phase)) {
                     ok = false;
                     break;
@@ -347,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int c = 4 * half + i;
-                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = deq_i4_word(wv[i]);
+                        const uint4 e = deq_i4_word(wv[i]);
+                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = GS ? scale_word4(e, gsc[i]) : e;
                     }
                 } else {
 #pragma unroll
@@ -356,9 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * h);
                         const uint2 lo = deq_i8_word(cw.x), hi = deq_i8_word(cw.y);
                         const uint2 lo2 = deq_i8_word(cw.z), hi2 = deq_i8_word(cw.w);
-                        *reinterpret_cast<uint4 *>(arow + (((2 * h) ^ sw) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-                        *reinterpret_cast<uint4 *>(arow + (((2 * h + 1) ^ sw) << 4)) =
-                            make_uint4(lo2.x, lo2.y, hi2.x, hi2.y);
+                        uint4 e0 = make_uint4(lo.x, lo.y, hi.x, hi.y), e1 = make_uint4(lo2.x, lo2.y, hi2.x, hi2.y);
+                        if (GS) {
+                            e0 = scale_word4(e0, gsc[hh]);
+                            e1 = scale_word4(e1, gsc[hh]);
+                        }
+                        *reinterpret_cast<uint4 *>(arow + (((2 * h) ^ sw) << 4)) = e0;
+                        *reinterpret_cast<uint4 *>(arow + (((2 * h + 1) ^ sw) << 4)) = e1;
                     }
                 }
                 fence_async_smem();
@@ -380,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BNT;
             const int o = m0 + quarter * 32 + lane;
-            const float sc = o < p.O ? p.scales[o] : 0.f;
+            const float sc = o < p.O ? (GS ? 1.f : p.scales[o]) : 0.f;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kAccStride;
             if constexpr (PIECES) {
                 float v[BNT];
@@ -583,7 +667,7 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out) {
 }
 
 // b_rows: rows of the bf16 B operand (tokens, or the padded pieces rows).
-template <int FMT, int BNT, bool PIECES>
+template <int FMT, int BNT, bool PIECES, bool GS = false>
 cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const float2 *unscale, float *y, int S,
                      cudaStream_t st) {
     constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
@@ -604,6 +688,14 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
     p.n_tiles = PIECES ? 1 : (S + BNT - 1) / BNT;
     p.nk = (int)(t.k_pad / BK);
     p.code_bytes = code_bytes;
+    if (GS) {
+        int c = 0;
+        while ((1ll << c) < t.gs) ++c;
+        p.gdiv = GroupDiv{(uint32_t)(((1ull << (31 + c)) + t.gs - 1) / t.gs), 31 + c};
+        p.g_ld = t.G_ld;
+        p.g_last = t.G_ld - 1;
+        p.g_one = t.gs % 32 == 0;
+    }
     constexpr int C_BYTES = BM * code_bytes;
     constexpr int kStages = stages_for<FMT, BNT>();
     const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BNT * BK * 2 + C_BYTES) + (3 * kStages + 4) * 8 + 16;
@@ -613,21 +705,22 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     static bool attr[64] = {};
     if (!attr[dev]) {
-        e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT, BNT, PIECES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT, BNT, PIECES, GS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         attr[dev] = true;
     }
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < g_sms ? tiles : g_sms;
-    qgemm_tc_kernel<FMT, BNT, PIECES><<<grid, kThreads, smem, st>>>(map_codes, map_x, p);
+    qgemm_tc_kernel<FMT, BNT, PIECES, GS><<<grid, kThreads, smem, st>>>(map_codes, map_x, p);
     count_launch();
     return cudaGetLastError();
 }
 
 template <int FMT>
 cudaError_t run_gemm_x(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, cudaStream_t st) {
-    return run_gemm<FMT, BN, false>(t, xb, S, nullptr, y, S, st);
+    return t.gs ? run_gemm<FMT, BN, false, true>(t, xb, S, nullptr, y, S, st)
+                : run_gemm<FMT, BN, false, false>(t, xb, S, nullptr, y, S, st);
 }
 
 }  // namespace

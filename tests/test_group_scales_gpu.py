@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import TOL_F32, assert_within, empty, gpu_matmul, to_dev
+from gpu_util import TOL_F32, TOL_TC, assert_within, empty, gpu_matmul, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -38,9 +38,10 @@ def test_group_scales_vs_oracle(q, fmt, gs, O, I, S):
     y_ref, bound = oracle.matmul_gs(fmt, O, I, gs, codes, gsc, x)
     with q.tensor_upload(fmt, O, I, codes, gsc, gs=gs) as t:
         assert q.tensor_group_size(t) == gs
-        assert q.matmul_path(t, S) == q.PATH_F32
+        tc = fmt in (1, 2) and S >= q.tc_min_s()           # int8 / int4 from the threshold: bf16 tensor cores
+        assert q.matmul_path(t, S) == (q.PATH_TC if tc else q.PATH_F32)
         y = gpu_matmul(q, t, x, S, O)
-    assert_within(y, y_ref, bound, TOL_F32, "gs fmt%d gs%d O%d I%d S%d" % (fmt, gs, O, I, S))
+    assert_within(y, y_ref, bound, TOL_TC if tc else TOL_F32, "gs fmt%d gs%d O%d I%d S%d" % (fmt, gs, O, I, S))
 
 
 def test_group_scales_int4_12288x6144_gs128(q):
@@ -76,11 +77,9 @@ def test_group_scales_refusals(q):
     codes, gsc = _grouped(fmt, O, I, gs, 3)
     with q.tensor_upload(fmt, O, I, codes, gsc, gs=gs) as t:
         x = to_dev(synth.activations(20, I, 3, 3))
-        for path in (q.PATH_TC, q.PATH_TCX):
-            with pytest.raises(q.B200QError):
-                q.matmul_ex(t, x, empty(20, O), 20, path)
-        with pytest.raises(q.B200QError):
-            q.matmul_tc_noalloc(t, x, empty(20, O), 20)
+        with pytest.raises(q.B200QError):                      # the three-piece path needs exact weights
+            q.matmul_ex(t, x, empty(20, O), 20, q.PATH_TCX)
+        assert q.matmul_path(t, 8) == q.PATH_F32
     big = np.ones(O * I, np.float32)                 # enough scales for any group size
     for bad in (0, -1, 24, 48):                      # through the C entry point itself
         assert not q.lib.b200q_tensor_upload_grouped(fmt, O, I, bad, codes.ctypes.data, big.ctypes.data)
@@ -160,8 +159,9 @@ def test_group_scales_mixed_layouts_in_a_group(q):
                          ids=lambda v: str(v))
 def test_group_scales_run_the_decode_kernel(q, fmt, gs):
     """Below 16 rows a group-wise tensor runs the staged decode kernel, one
-    launch per two rows (5 rows: 3 launches); from 16 rows the general SIMT
-    kernel, one launch for any number of rows."""
+    launch per two rows (5 rows: 3 launches); from 16 rows f32 and int2 run
+    the general SIMT kernel (one launch), int8 and int4 the bf16 tensor-core
+    path (x to bf16, then the GEMM: two launches)."""
     import torch
     O, I = 256, 1024
     codes, gsc = _grouped(fmt, O, I, gs, 6)
@@ -174,4 +174,43 @@ def test_group_scales_run_the_decode_kernel(q, fmt, gs):
         q.matmul(t, xd, y, 16)
         n2 = q.kernel_launches()
         torch.cuda.synchronize()
-    assert (n1 - n0, n2 - n1) == (3, 1)
+    assert (n1 - n0, n2 - n1) == (3, 2 if fmt in (1, 2) else 1)
+
+
+TC_CASES = [  # fmt, gs, O, I, S
+    (2, 128, 300, 1000, 40), (2, 16, 129, 640, 17), (2, 32, 256, 2048, 200), (2, 96, 130, 3000, 33),
+    (1, 16, 200, 700, 64), (1, 48, 128, 1536, 100), (1, 128, 77, 4096, 18),
+]
+
+
+@pytest.mark.parametrize("fmt,gs,O,I,S", TC_CASES, ids=lambda v: str(v))
+def test_group_scales_tensor_core_path(q, fmt, gs, O, I, S):
+    """bf16 tensor-core path with group scales (dequantizer forms
+    bf16((code - zero point) * scale)), within the path's 4e-3 bar; tiles
+    span several k-blocks, groups that straddle k-blocks, ragged O and I."""
+    codes, gsc = _grouped(fmt, O, I, gs, O + gs)
+    x = synth.activations(S, I, I, 5)
+    y_ref, bound = oracle.matmul_gs(fmt, O, I, gs, codes, gsc, x)
+    with q.tensor_upload(fmt, O, I, codes, gsc, gs=gs) as t:
+        y = gpu_matmul(q, t, x, S, O, path=q.PATH_TC)
+        y2 = empty(S, O)
+        q.matmul_tc_noalloc(t, to_dev(x), y2, S)
+        import torch
+        torch.cuda.synchronize()
+        y2 = y2.cpu().numpy()
+    assert_within(y, y_ref, bound, TOL_TC, "tc gs fmt%d gs%d" % (fmt, gs))
+    assert np.array_equal(y, y2)                            # the no-alloc call runs the same kernel
+
+
+def test_group_scales_prefill_full_size_sampled(q):
+    """int4 [12288, 6144] gs=128 at S=1571 on the tensor cores: 96 sampled rows
+    (every tile row block) against the oracle run on those rows."""
+    fmt, O, I, gs, S = 2, 12288, 6144, 128, 1571
+    codes, gsc = _grouped(fmt, O, I, gs, 11)
+    x = synth.activations(S, I, 11, 6)
+    with q.tensor_upload(fmt, O, I, codes, gsc, gs=gs) as t:
+        assert q.matmul_path(t, S) == q.PATH_TC
+        y = gpu_matmul(q, t, x, S, O)
+    rows = np.sort(synth.rng(11, 7).choice(O, 96, replace=False))
+    y_ref, bound = oracle.matmul_gs(fmt, len(rows), I, gs, codes[rows], gsc[rows], x)
+    assert_within(y[:, rows], y_ref, bound, TOL_TC, "tc gs full size")
