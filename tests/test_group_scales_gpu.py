@@ -54,9 +54,11 @@ def test_group_scales_int4_12288x6144_gs128(q):
     assert_within(y, y_ref, bound, TOL_F32, "gs int4 12288x6144")
 
 
-def test_group_scales_gate_up_and_grouped_call(q):
+@pytest.mark.parametrize("S", [2, 20], ids=["decode", "tensor_cores"])
+def test_group_scales_gate_up_and_grouped_call(q, S):
     import torch
-    fmt, O, I, gs, S = 2, 256, 512, 64, 2
+    fmt, O, I, gs = 2, 256, 512, 64
+    tol = TOL_TC if S >= q.tc_min_s() else TOL_F32
     (cg, sg), (cu, su) = _grouped(fmt, O, I, gs, 7), _grouped(fmt, O, I, gs, 8)
     x = synth.activations(S, I, 9, 3)
     yg_ref, bg = oracle.matmul_gs(fmt, O, I, gs, cg, sg, x)
@@ -69,7 +71,7 @@ def test_group_scales_gate_up_and_grouped_call(q):
         torch.cuda.synchronize()
         for got, ref, b, what in ((yg, yg_ref, bg, "gate"), (yu, yu_ref, bu, "up"), (zg, yg_ref, bg, "grouped gate"),
                                   (zu, yu_ref, bu, "grouped up")):
-            assert_within(got.cpu().numpy(), ref, b, TOL_F32, what)
+            assert_within(got.cpu().numpy(), ref, b, tol, what)
 
 
 def test_group_scales_refusals(q):
