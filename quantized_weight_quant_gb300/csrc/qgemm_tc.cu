@@ -38,6 +38,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "qwq_internal.h"
@@ -49,9 +50,14 @@ constexpr int BM = 128, BN = 176, BK = 64;
 // Pipeline stages (code tile + x tile + dequantized A tile; 42.5 KB for int4
 // at 176 tokens): as many as fit in 227 KB of shared memory, at most 8, since
 // the stage ring has to cover a TMA round trip plus dequantization.
-template <int FMT, int BNT>
+// Group-scale tile of a stage when the producer copies the scales (GSM = 2):
+// 128 rows x 4 f32 from a 4-aligned first group.
+constexpr int kScaleBox = 4;
+constexpr int kScaleTile = BM * kScaleBox * 4;      // 2 KB
+
+template <int FMT, int BNT, int GSM = 0>
 constexpr int stages_for() {
-    constexpr int per = BM * BK * 2 + BNT * BK * 2 + BM * (FMT == B200Q_I4 ? 32 : 64);
+    constexpr int per = BM * BK * 2 + BNT * BK * 2 + BM * (FMT == B200Q_I4 ? 32 : 64) + (GSM == 2 ? kScaleTile : 0);
     constexpr int n = (232448 - 1024 - 512) / per;
     return n > 8 ? 8 : n;
 }
@@ -255,17 +261,21 @@ struct GemmParams {
 
 // BNT: columns of the B tile (tokens, or x pieces).  PIECES: B holds three
 // bf16 pieces per token (rows 3s, 3s+1, 3s+2, summing to x exactly) and the
-// epilogue adds each token's three columns.  GS: group-wise scales, applied
+// epilogue adds each token's three columns.  GSM: 0 per-row scales; 1 / 2
+// group-wise scales, which the dequantizers load themselves (1) or find in
+// the stage, copied by the producer with the code tile (2: a k-block's groups
+// lie within 4 floats from a 4-aligned first group).  Group-wise scales, applied
 // by the dequantizers (A = bf16((code - zero point) * scale[o, group]), one
 // rounding per weight, see scale_pair); the epilogue then applies no row
 // scale.  An int4
 // code word (8 columns) or an int8 16-byte chunk (16 columns) always lies in
 // one group (gs is a multiple of 16 for int8, of 16 or 32 for int4).
-template <int FMT, int BNT, bool PIECES, bool GS = false>
+template <int FMT, int BNT, bool PIECES, int GSM = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
-                    const GemmParams p) {
-    constexpr int kStages = stages_for<FMT, BNT>();
+                    const __grid_constant__ CUtensorMap map_sc, const GemmParams p) {
+    constexpr bool GS = GSM != 0;
+    constexpr int kStages = stages_for<FMT, BNT, GSM>();
     constexpr uint32_t kIdesc = idesc_for(BNT);
     static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 256 && (!PIECES || BNT <= 48), "token tile");
     extern __shared__ uint8_t smem_raw[];
@@ -277,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *a_s = smem;                                 // [kStages][A_BYTES]
     uint8_t *b_s = a_s + kStages * A_BYTES;              // [kStages][B_BYTES]
     uint8_t *c_s = b_s + kStages * B_BYTES;              // [kStages][C_BYTES]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(c_s + kStages * C_BYTES);
+    constexpr int S_BYTES = GSM == 2 ? kScaleTile : 0;
+    uint8_t *s_s = c_s + kStages * C_BYTES;              // [kStages][BM][kScaleBox] f32 (GSM = 2)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_s + kStages * S_BYTES);
     uint64_t *tma_full = bars, *a_full = bars + kStages, *empty = bars + 2 * kStages;
     uint64_t *acc_full = bars + 3 * kStages, *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
@@ -323,9 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t bar = smem_u32(&tma_full[stage]);
-                    mbar_expect_tx(bar, (uint32_t)(C_BYTES + B_BYTES));
+                    mbar_expect_tx(bar, (uint32_t)(C_BYTES + B_BYTES + S_BYTES));
                     tma_load_2d(smem_u32(c_s + stage * C_BYTES), &map_codes, kb * p.code_bytes, m0, bar);
                     tma_load_2d(smem_u32(b_s + stage * B_BYTES), &map_x, kb * BK, n0, bar);
+                    if (GSM == 2)   // the k-block's group scales, from its first group rounded down to 16 bytes
+                        tma_load_2d(smem_u32(s_s + stage * S_BYTES), &map_sc, group_of(kb * BK, p.gdiv) & ~3, m0,
+                                    bar);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -398,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dst[i] = __ldg(p.scales + o * p.g_ld + g);
             }
         };
-        if (GS && blockIdx.x < n_tiles_total) load_gs(blockIdx.x, 0, gsn);
+        if (GSM == 1 && blockIdx.x < n_tiles_total) load_gs(blockIdx.x, 0, gsn);
         for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
             for (int kb = 0; kb < p.nk; ++kb) {
-                if constexpr (GS) {
+                if constexpr (GSM == 1) {
                     if (p.g_one) {
                         const ScalePair sp = split_scale(gsn[0]);
 #pragma unroll
@@ -416,6 +431,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(smem_u32(&tma_full[stage]), phase)) {
                     ok = false;
                     break;
+                }
+                if constexpr (GSM == 2) {
+                    const float *srow = reinterpret_cast<const float *>(s_s + stage * S_BYTES) + r * kScaleBox;
+                    const int g0 = group_of(kb * BK, p.gdiv) & ~3;
+                    if (p.g_one) {
+                        const ScalePair sp = split_scale(srow[group_of(kb * BK + 32 * half, p.gdiv) - g0]);
+#pragma unroll
+                        for (int i = 0; i < kGW; ++i) gsc[i] = sp;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kGW; ++i)
+                            gsc[i] = split_scale(srow[group_of(kb * BK + 32 * half + kGCols * i, p.gdiv) - g0]);
+                    }
                 }
                 const uint8_t *crow = c_s + stage * C_BYTES + r * (C_BYTES / BM);
                 uint8_t *arow = a_s + stage * A_BYTES + r * 128;
@@ -667,11 +695,17 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out) {
 }
 
 // b_rows: rows of the bf16 B operand (tokens, or the padded pieces rows).
-template <int FMT, int BNT, bool PIECES, bool GS = false>
+template <int FMT, int BNT, bool PIECES, int GSM = 0>
 cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const float2 *unscale, float *y, int S,
                      cudaStream_t st) {
+    constexpr bool GS = GSM != 0;
     constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
-    CUtensorMap map_codes, map_x;
+    CUtensorMap map_codes, map_x, map_sc;
+    memset(&map_sc, 0, sizeof map_sc);
+    if (GSM == 2 &&
+        !tmap_encode_2d(&map_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, t.scales, (uint64_t)t.G_ld, (uint64_t)t.o_pad,
+                        (uint64_t)t.G_ld * 4, kScaleBox, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     if (!tmap_encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
                    (uint64_t)t.ld, code_bytes, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
@@ -697,30 +731,35 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
         p.g_one = t.gs % 32 == 0;
     }
     constexpr int C_BYTES = BM * code_bytes;
-    constexpr int kStages = stages_for<FMT, BNT>();
-    const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BNT * BK * 2 + C_BYTES) + (3 * kStages + 4) * 8 + 16;
+    constexpr int kStages = stages_for<FMT, BNT, GSM>();
+    const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BNT * BK * 2 + C_BYTES + (GSM == 2 ? kScaleTile : 0)) +
+                        (3 * kStages + 4) * 8 + 16;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     static bool attr[64] = {};
     if (!attr[dev]) {
-        e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT, BNT, PIECES, GS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT, BNT, PIECES, GSM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         attr[dev] = true;
     }
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < g_sms ? tiles : g_sms;
-    qgemm_tc_kernel<FMT, BNT, PIECES, GS><<<grid, kThreads, smem, st>>>(map_codes, map_x, p);
+    qgemm_tc_kernel<FMT, BNT, PIECES, GSM><<<grid, kThreads, smem, st>>>(map_codes, map_x, map_sc, p);
     count_launch();
     return cudaGetLastError();
 }
 
 template <int FMT>
 cudaError_t run_gemm_x(const Tensor &t, const __nv_bfloat16 *xb, float *y, int S, cudaStream_t st) {
-    return t.gs ? run_gemm<FMT, BN, false, true>(t, xb, S, nullptr, y, S, st)
-                : run_gemm<FMT, BN, false, false>(t, xb, S, nullptr, y, S, st);
+    if (!t.gs) return run_gemm<FMT, BN, false, 0>(t, xb, S, nullptr, y, S, st);
+    // the producer copies the scales when a k-block's groups fit 4 floats
+    // from a 4-aligned first group: gs a multiple of 64, or 16 / 32
+    const bool boxed = t.gs % BK == 0 || t.gs == 16 || t.gs == 32;
+    return boxed ? run_gemm<FMT, BN, false, 2>(t, xb, S, nullptr, y, S, st)
+                 : run_gemm<FMT, BN, false, 1>(t, xb, S, nullptr, y, S, st);
 }
 
 }  // namespace
