@@ -59,11 +59,25 @@
 namespace qwq {
 namespace {
 
-constexpr int kMaxWarps = 15;
-// Consumer warps of a variant: two tokens with group-wise scales hold a
-// second set of sums, so those variants run fewer, larger threads (no spills).
-template <int NS, int GW>
-constexpr int max_warps() { return NS == 2 && GW ? 11 : kMaxWarps; }
+constexpr int kMaxWarps = 16;
+// Consumer warps of a variant (measured on the format sweep):
+//   * f32 and int8, one token: 16 (under the 120 registers 17 warps allow);
+//     their rings drop to 2 stages to make room, which these formats
+//     tolerate (more weight bytes per instruction);
+//   * int4 and int2, one token: 15 with 3-stage rings (the integer-bound
+//     formats lose more from the shallower ring than they gain from the
+//     sixteenth warp);
+//   * two tokens: 15, or 11 with group-wise scales (a second set of sums,
+//     no spills); for int4 and int2 their larger staged x is paid for with a
+//     ring stage, for f32 and int8 with warps.
+template <int FMT, int NS, int GW>
+constexpr int max_warps() {
+    return NS == 2 ? (GW ? 11 : 15) : (FMT == B200Q_F32 || FMT == B200Q_I8) ? 16 : 15;
+}
+// Whether a launch that does not fit gives up a ring stage before a warp:
+// one token for f32 / int8, two tokens for int4 / int2.
+template <int FMT, int NS>
+constexpr bool stage_before_warp() { return (NS == 1) == (FMT == B200Q_F32 || FMT == B200Q_I8); }
 constexpr int kMaxSets = B200Q_GROUP_MAX;  // tensors per launch
 constexpr int kSeg = 512;            // bytes per row per stage: 32 lanes x 16 B
 constexpr int kStage = 8 * kSeg;     // one stage: 8 rows x 512 B (one TMA box)
@@ -325,7 +339,7 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z));
 // scale and adds it to the row's sum; the producer copies each stage's
 // scales (8 rows x gbox, from a 4-aligned first group) next to its codes.
 template <int FMT, int NS, int MS, int GW>
-__global__ void __launch_bounds__((max_warps<NS, GW>() + 1) * 32, 1)
+__global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     qmv_decode_kernel(const __grid_constant__ DecParams<MS> p) {
     constexpr int E = F<FMT>::E;
     constexpr int SEGE = (kSeg / 16) * E;            // elements of a row in one stage
@@ -939,7 +953,8 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     };
     // warps and depth first (round of kRound), then grow the round to all of
     // the CTA's row groups if the partials still fit (one round: no barrier)
-    int depth = 3, nw = max_warps<NS, GW>();
+    int depth = 3, nw = max_warps<FMT, NS, GW>();
+    if (stage_before_warp<FMT, NS>() && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) depth = 2;
     while (nw > 4 && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) --nw;
     if (fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) depth = 2;
     while (nw > 4 && fixed_for(nw, kRound) + (size_t)nw * depth * stage > kSmemMax) --nw;
