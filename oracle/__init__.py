@@ -66,7 +66,7 @@ def _bind(path: str):
     L.qref_matmul_gs.restype = c_int
     L.qref_rmsnorm.argtypes = [vp, vp, vp, c_long, c_long, ctypes.c_double, vp, vp, vp]
     L.qref_rmsnorm.restype = c_int
-    L.qref_mla_absorb.argtypes = [c_int, c_long, c_long, c_long, c_long, c_long, vp, vp, vp, vp, vp, vp,
+    L.qref_mla_absorb.argtypes = [c_int, c_long, c_long, c_long, c_long, c_long, vp, vp, c_long, vp, vp, vp, vp,
                                   c_long, c_long, ctypes.c_double, c_long, vp, vp, vp]
     L.qref_mla_absorb.restype = c_int
     L.qref_round_bf16.argtypes = [ctypes.c_float]
@@ -236,9 +236,10 @@ def rmsnorm(x, w, eps: float, r=None):
 
 
 def mla_absorb(fmt: int, H: int, Dn: int, Dv: int, K: int, codes, scales, q_nope, q_rope, lat, rope,
-               st0: int, scale: float, *, want_dbl: bool = False):
+               st0: int, scale: float, *, gs: int = 0, want_dbl: bool = False):
     """MLA decode attention with weight absorption over a [H*(Dn+Dv), K]
-    weight tensor (per-row scales or None = 1.0).  q_nope [S, H, Dn], q_rope
+    weight tensor (per-row scales or None = 1.0; gs >= 1: group-wise scales
+    [H*(Dn+Dv), ceil(K / gs)]).  q_nope [S, H, Dn], q_rope
     [S, H, R], lat [T, K], rope [T, R]; the S new tokens are the last S
     positions of the caches.  Returns (ctx f32 [S, H, Dv], bound f64) or
     (ctx, bound, ctx f64) with want_dbl."""
@@ -256,7 +257,7 @@ def mla_absorb(fmt: int, H: int, Dn: int, Dv: int, K: int, codes, scales, q_nope
     ctx = np.empty((S, H, Dv), np.float32)
     bound = np.empty((S, H, Dv), np.float64)
     cd = np.empty((S, H, Dv), np.float64) if want_dbl else None
-    rc = _L().qref_mla_absorb(fmt, H, Dn, Dv, K, R, _ptr(codes), _ptr(scales), _ptr(q_nope), _ptr(q_rope),
+    rc = _L().qref_mla_absorb(fmt, H, Dn, Dv, K, R, _ptr(codes), _ptr(scales), gs, _ptr(q_nope), _ptr(q_rope),
                               _ptr(lat), _ptr(rope), T, st0, float(scale), S, _ptr(ctx), _ptr(cd),
                               _ptr(bound))
     if rc:

@@ -308,10 +308,11 @@ int qref_matmul_bf16x(int fmt, long O, long I, const uint8_t *codes, const float
  *   clat[i]  = sum_t p_t * L[t,i]                               (latent context)
  *   ctx[s,h,v] = sum_i clat[i] * Wv[h,v,i]                      (value rows)
  *
- * Wkv_b is one [H*(Dn+Dv), K] weight tensor (host layout of fmt, per-row
- * scales; NULL scales mean 1.0): head h's key rows are h*(Dn+Dv) + d for
- * d < Dn, its value rows follow at h*(Dn+Dv) + Dn + v; the weight value is
- * scale[row] * deq(code), as in qref_matmul.  L is the latent cache [T, K],
+ * Wkv_b is one [H*(Dn+Dv), K] weight tensor (host layout of fmt): head h's
+ * key rows are h*(Dn+Dv) + d for d < Dn, its value rows follow at
+ * h*(Dn+Dv) + Dn + v.  The weight value is scale * deq(code), with per-row
+ * scales [rows] as in qref_matmul (gs = 0; NULL scales mean 1.0), or
+ * group-wise scales [rows, ceil(K / gs)] as in qref_matmul_gs (gs >= 1).  L is the latent cache [T, K],
  * Rr the rope cache [T, R], both f32; the S new tokens sit at positions
  * T-S .. T-1 and token s sees positions st0 .. T-S+s (causal).  q_nope is
  * [S, H, Dn], q_rope [S, H, R], ctx [S, H, Dv].  Everything is in double,
@@ -326,8 +327,15 @@ int qref_matmul_bf16x(int fmt, long O, long I, const uint8_t *codes, const float
  * step adds its own eps).  Returns 0, or -1 for a bad argument (S < 1,
  * T < S, st0 < 0 or st0 > T - S: every window must hold a position).
  */
+/* Scale of element i of weight row `row` (see qref_mla_absorb). */
+static double mla_scale(const float *scales, long gs, long G, long row, long i)
+{
+    if (!scales) return 1.0;
+    return gs ? (double)scales[row * G + i / gs] : (double)scales[row];
+}
+
 int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
-                    const uint8_t *codes, const float *scales,
+                    const uint8_t *codes, const float *scales, long gs,
                     const float *q_nope, const float *q_rope,
                     const float *lat, const float *rope,
                     long T, long st0, double scale, long S,
@@ -336,8 +344,9 @@ int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
     long rb = qref_row_bytes(fmt, K);
     if (rb < 0 || H < 1 || Dn < 1 || Dv < 1 || K < 1 || R < 0 || S < 1 || T < S || st0 < 0 || st0 > T - S)
         return -1;
-    if (!codes || !q_nope || (R > 0 && (!q_rope || !rope)) || !lat || !ctx) return -1;
+    if (!codes || !q_nope || (R > 0 && (!q_rope || !rope)) || !lat || !ctx || gs < 0 || (gs && !scales)) return -1;
     long HS = H * S;
+    long G = gs ? (K + gs - 1) / gs : 1;
 #ifdef _OPENMP
     int nt = qref_max_threads();
 #pragma omp parallel for schedule(dynamic) num_threads(nt)
@@ -364,9 +373,8 @@ int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
         for (long i = 0; i < K; ++i) qabs[i] = qa[i] = 0.0;
         for (long d = 0; d < Dn; ++d) {
             const uint8_t *krow = codes + (key0 + d) * rb;
-            double ksc = scales ? (double)scales[key0 + d] : 1.0;
             for (long i = 0; i < K; ++i) {
-                double kw = ksc * qref_weight(fmt, krow, i);
+                double kw = mla_scale(scales, gs, G, key0 + d, i) * qref_weight(fmt, krow, i);
                 qabs[i] += (double)qn[d] * kw;
                 qa[i] += fabs((double)qn[d] * kw);
             }
@@ -408,10 +416,9 @@ int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
         /* value rows */
         for (long v = 0; v < Dv; ++v) {
             const uint8_t *vrow = codes + (val0 + v) * rb;
-            double vsc = scales ? (double)scales[val0 + v] : 1.0;
             double acc = 0.0, b = 0.0;
             for (long i = 0; i < K; ++i) {
-                double vw = vsc * qref_weight(fmt, vrow, i);
+                double vw = mla_scale(scales, gs, G, val0 + v, i) * qref_weight(fmt, vrow, i);
                 acc += clat[i] * vw;
                 b += fabs(vw) * cabs[i];
             }

@@ -394,8 +394,10 @@ def _dense_weights(fmt, codes, sc, O, I):
     return W * sc.astype(np.float64)[:, None]
 
 
-def _mla_case(fmt, H, Dn, Dv, K, R, S, T, seed):
+def _mla_case(fmt, H, Dn, Dv, K, R, S, T, seed, gs=0):
     codes, sc = synth.quant_tensor(fmt, H * (Dn + Dv), K, seed, 1, 5e-3, 2e-2)
+    if gs:
+        sc = synth.uniform_f32((H * (Dn + Dv), -(-K // gs)), 5e-3, 2e-2, seed, 6)
     qn = synth.normal_f32((S, H, Dn), seed, 2, std=4.0)
     qr = synth.normal_f32((S, H, R), seed, 3)
     lat = synth.normal_f32((T, K), seed, 4)
@@ -403,11 +405,13 @@ def _mla_case(fmt, H, Dn, Dv, K, R, S, T, seed):
     return codes, sc, qn, qr, lat, rope
 
 
-MLA_CASES = [  # fmt, H, Dn, Dv, K, R, S, T, st0, scale
-    (I4, 3, 8, 5, 40, 6, 3, 11, 2, 0.3),
-    (I8, 2, 4, 7, 33, 4, 1, 9, 0, 0.5),
-    (F32, 2, 6, 6, 20, 2, 2, 5, 3, 1.0),
-    (I2, 4, 3, 2, 27, 3, 4, 12, 1, 0.7),
+MLA_CASES = [  # fmt, H, Dn, Dv, K, R, S, T, st0, scale, gs
+    (I4, 3, 8, 5, 40, 6, 3, 11, 2, 0.3, 0),
+    (I8, 2, 4, 7, 33, 4, 1, 9, 0, 0.5, 0),
+    (F32, 2, 6, 6, 20, 2, 2, 5, 3, 1.0, 0),
+    (I2, 4, 3, 2, 27, 3, 4, 12, 1, 0.7, 0),
+    (I4, 2, 5, 4, 48, 4, 2, 10, 1, 0.4, 16),     # group-wise scales, 3 groups per row
+    (I8, 3, 4, 6, 40, 4, 1, 8, 0, 0.6, 12),      # a short last group
 ]
 
 
@@ -416,10 +420,16 @@ def check_mla_naive():
     (k_t = Wk L_t, v_t = Wv L_t, the non-absorbed MLA form), then textbook
     causal attention over [st0, T-S+s] in numpy float64.  The error bound is
     recomputed from its definition."""
-    for fmt, H, Dn, Dv, K, R, S, T, st0, scale in MLA_CASES:
-        codes, sc, qn, qr, lat, rope = _mla_case(fmt, H, Dn, Dv, K, R, S, T, 11 + fmt)
-        _, bound, cd = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, st0, scale, want_dbl=True)
-        W = _dense_weights(fmt, codes, sc, H * (Dn + Dv), K).reshape(H, Dn + Dv, K)
+    for fmt, H, Dn, Dv, K, R, S, T, st0, scale, gs in MLA_CASES:
+        codes, sc, qn, qr, lat, rope = _mla_case(fmt, H, Dn, Dv, K, R, S, T, 11 + fmt, gs)
+        _, bound, cd = Q.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, st0, scale, gs=gs,
+                                    want_dbl=True)
+        if gs:      # scale of column i: its group's, expanded over the row
+            ones = np.ones(H * (Dn + Dv), np.float32)
+            W = _dense_weights(fmt, codes, ones, H * (Dn + Dv), K) * np.repeat(sc.astype(np.float64), gs, 1)[:, :K]
+        else:
+            W = _dense_weights(fmt, codes, sc, H * (Dn + Dv), K)
+        W = W.reshape(H, Dn + Dv, K)
         Wk, Wv = W[:, :Dn], W[:, Dn:]
         L, Rr = lat.astype(np.float64), rope.astype(np.float64)
         keys = np.einsum("hdk,tk->thd", Wk, L)

@@ -66,8 +66,12 @@ MUTANTS = {
     "mla_softmax_unnormalized": ("double p = score[w] / z;", "double p = score[w];"),
     "mla_q_head_token_swapped": ("const float *qn = q_nope + (s * H + h) * Dn;",
                                  "const float *qn = q_nope + (h * S + s) * Dn;"),
-    "mla_key_scale_dropped": ("double ksc = scales ? (double)scales[key0 + d] : 1.0;", "double ksc = 1.0;"),
-    "mla_value_scale_dropped": ("double vsc = scales ? (double)scales[val0 + v] : 1.0;", "double vsc = 1.0;"),
+    "mla_key_scale_dropped": ("double kw = mla_scale(scales, gs, G, key0 + d, i) *", "double kw = 1.0 *"),
+    "mla_value_scale_dropped": ("double vw = mla_scale(scales, gs, G, val0 + v, i) *", "double vw = 1.0 *"),
+    "mla_first_group_scale_only": ("return gs ? (double)scales[row * G + i / gs] : (double)scales[row];",
+                                   "return gs ? (double)scales[row * G] : (double)scales[row];"),
+    "mla_group_stride_one": ("return gs ? (double)scales[row * G + i / gs] : (double)scales[row];",
+                             "return gs ? (double)scales[row + i / gs] : (double)scales[row];"),
     "mla_bound_without_softmax_term": ("bound[out] = (1.0 + amax) * b;", "bound[out] = b;"),
     "mla_latent_not_weighted": ("clat[i] += p * (double)lt[i];", "clat[i] += (double)lt[i] / (double)nwin;"),
     "rms_residual_dropped": ("float hv = r ? (float)((double)x[s * D + d] + (double)r[s * D + d]) : x[s * D + d];\n            if (h)",
