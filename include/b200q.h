@@ -344,16 +344,16 @@ long long b200q_kernel_launches(void);
  *     clat[i]    = sum_t p_t * L[t,i]
  *     ctx[s,h,v] = sum_i clat[i] * Wv[h,v,i]                     v < Dv
  * Wk and Wv are rows of one tensor wkv_b of H * (Dn + Dv) rows and K columns
- * (any format, per-row scales): head h's key rows are h * (Dn + Dv) + d, its
- * value rows h * (Dn + Dv) + Dn + v; each weight is scale[row] * (code - zero
- * point).  The S new tokens occupy positions T-S .. T-1 of the caches (append
+ * (any format): head h's key rows are h * (Dn + Dv) + d, its value rows
+ * h * (Dn + Dv) + Dn + v; each weight is scale * (code - zero point), the
+ * scale of its row or of its row and group of gs columns.  The S new tokens occupy positions T-S .. T-1 of the caches (append
  * them first); token s sees positions st0 .. T-S+s.
  */
 enum { B200Q_KV_PAGE_TOKENS = 64 };
 
 /*
- *   wkv_b       tensor handle, O = H * (Dn + Dv), I = K; per-row scales
- *               (group-wise scales: B200Q_EINVAL); K a multiple of 4, at most 768
+ *   wkv_b       tensor handle, O = H * (Dn + Dv), I = K; per-row or group-wise
+ *               scales; K a multiple of 4, at most 768
  *   q_nope      device [S, H, Dn] f32, 16-byte aligned
  *   q_rope      device [S, H, R] f32, 16-byte aligned (unused when R = 0)
  *   lat_pages   DEVICE array of ceil(T / 64) device pointers; page p holds

@@ -624,7 +624,6 @@ int b200q_mla_absorb(const b200q_tensor *wkv_b, int H, int Dn, int Dv, const flo
     if ((long long)H * (Dn + Dv) != w.O)
         return fail(B200Q_EINVAL, "%s: the tensor has %d rows, H * (Dn + Dv) = %lld", who, w.O,
                     (long long)H * (Dn + Dv));
-    if (w.gs) return fail(B200Q_EINVAL, "%s: the weight tensor must have per-row scales", who);
     const int K = w.I;
     if (K % 4 || R % 4 || K > mla_max_latent())
         return fail(B200Q_EINVAL, "%s: need K and R multiples of 4 and K <= %d (got K=%d, R=%d)", who,

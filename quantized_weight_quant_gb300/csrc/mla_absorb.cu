@@ -8,7 +8,8 @@
 //     ctx[s,h,v] = sum_i clat[i] * Wv[h,v,i]                      (value rows)
 // Wk / Wv are the key and value rows of one quantized weight tensor
 // [H*(Dn+Dv), K] (head h: key rows h*(Dn+Dv) + d, value rows after them),
-// weight = scale[row] * (code - zero point).  L and Rr are the latent and rope
+// weight = scale * (code - zero point), one scale per row or per row and group
+// of gs columns (a 32-bit code word always lies in one group).  L and Rr are the latent and rope
 // caches, paged by 64 positions (the CUDA chapter's KV pages): page p holds
 // positions 64p .. 64p+63 as [64, K] and [64, R] f32 rows.
 //
@@ -106,9 +107,10 @@ struct Word<B200Q_I2> {
 // ---------------------------------------------------------------- absorb
 template <int FMT>
 __global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restrict__ codes,
-                                                         const float *__restrict__ scales, long long ld, int H,
-                                                         int Dn, int Dv, int K, const float *__restrict__ q_nope,
-                                                         int S, float *__restrict__ qabs) {
+                                                         const float *__restrict__ scales, int gs, int g_ld,
+                                                         long long ld, int H, int Dn, int Dv, int K,
+                                                         const float *__restrict__ q_nope, int S,
+                                                         float *__restrict__ qabs) {
     constexpr int EW = Word<FMT>::EW;
     constexpr int kPh = 16;                             // warps = row phases
     extern __shared__ float red[];                      // [kPh][kTokBlock][EW][32]
@@ -118,6 +120,10 @@ __global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restri
     const int word = blockIdx.y * 32 + lane;
     const int nwords = (K + EW - 1) / EW;
     const long long key0 = (long long)h * (Dn + Dv);
+    // scale of this thread's word in a row: scales[row] (gs = 0), or the
+    // word's group column (a word lies in one group)
+    const long long s_ld = gs ? g_ld : 1;
+    const int s_col = gs ? (word * EW) / gs : 0;
     float acc[kTokBlock][EW];
 #pragma unroll
     for (int t = 0; t < kTokBlock; ++t)
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restri
         for (int e = 0; e < EW; ++e) acc[t][e] = 0.f;
     bool waited = false;
     if (word < nwords) {
-        constexpr int kB = EW >= 16 ? 4 : 8;            // rows per batch: all their loads in flight
+        constexpr int kB = EW >= 16 ? 2 : EW >= 8 ? 4 : 8;   // rows per batch: all their loads in flight
         for (int d0 = ph; d0 < Dn; d0 += kPh * kB) {
             uint32_t wb[kB];
             float sc[kB];
@@ -137,7 +143,7 @@ __global__ void __launch_bounds__(512) mla_absorb_kernel(const uint8_t *__restri
                 sc[b] = 0.f;
                 if (d < Dn) {
                     wb[b] = __ldg(reinterpret_cast<const uint32_t *>(codes + (key0 + d) * ld) + word);
-                    sc[b] = __ldg(scales + key0 + d);
+                    sc[b] = __ldg(scales + (key0 + d) * s_ld + s_col);
                 }
             }
             if (!waited) {                               // q_nope comes from the previous kernel
@@ -563,8 +569,8 @@ constexpr int kValRows = 16;                     // per CTA: 4 warps x 4 rows
 
 template <int FMT>
 __global__ void __launch_bounds__(kValThreads) mla_value_kernel(const uint8_t *__restrict__ codes,
-                                                                const float *__restrict__ scales, long long ld,
-                                                                int H, int Dn, int Dv, int K, int S,
+                                                                const float *__restrict__ scales, int gs, int g_ld,
+                                                                long long ld, int H, int Dn, int Dv, int K, int S,
                                                                 const float *__restrict__ clat_g,
                                                                 float *__restrict__ ctx) {
     constexpr int EW = Word<FMT>::EW;
@@ -582,7 +588,7 @@ __global__ void __launch_bounds__(kValThreads) mla_value_kernel(const uint8_t *_
     for (int k = 0; k < 4; ++k) {
         const bool live = v0 + k < Dv;
         const uint32_t *row = reinterpret_cast<const uint32_t *>(codes + (val0 + (live ? v0 + k : 0)) * ld);
-        sc[k] = live ? __ldg(scales + val0 + v0 + k) : 0.f;
+        sc[k] = live && !gs ? __ldg(scales + val0 + v0 + k) : 1.f;
 #pragma unroll
         for (int b = 0; b < kWL; ++b) cw[k][b] = live && lane + 32 * b < nwords ? __ldg(row + lane + 32 * b) : 0u;
     }
@@ -622,8 +628,17 @@ __global__ void __launch_bounds__(kValThreads) mla_value_kernel(const uint8_t *_
             for (int k = 0; k < 4; ++k) {
                 float wv[EW];
                 Word<FMT>::deq(cw[k][b], wv);
+                if (gs) {   // the word's partial sum times its group scale
+                    float part = 0.f;
 #pragma unroll
-                for (int e = 0; e < EW; ++e) a[k][t] = fmaf(wv[e], cl[e], a[k][t]);
+                    for (int e = 0; e < EW; ++e) part = fmaf(wv[e], cl[e], part);
+                    const bool live = v0 + k < Dv;
+                    const float g = live ? __ldg(scales + (val0 + v0 + k) * g_ld + (wd * EW) / gs) : 0.f;
+                    a[k][t] = fmaf(g, part, a[k][t]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) a[k][t] = fmaf(wv[e], cl[e], a[k][t]);
+                }
             }
         }
     }
@@ -697,7 +712,7 @@ cudaError_t run_absorb(const Tensor &w, int H, int Dn, int Dv, const float *q_no
     const int K = w.I, nwords = (K + EW - 1) / EW;
     dim3 grid(H, (nwords + 31) / 32, (S + kTokBlock - 1) / kTokBlock);
     return launch_pdl(mla_absorb_kernel<FMT>, grid, dim3(512), smem, st, (const uint8_t *)w.codes,
-                      (const float *)w.scales, (long long)w.ld, H, Dn, Dv, K, q_nope, S, qabs);
+                      (const float *)w.scales, w.gs, w.G_ld, (long long)w.ld, H, Dn, Dv, K, q_nope, S, qabs);
 }
 
 template <int FMT>
@@ -707,7 +722,8 @@ cudaError_t run_value(const Tensor &w, int H, int Dn, int Dv, int S, const float
     const size_t smem = (size_t)kTokBlock * K * 4;     // <= 12 KB
     dim3 grid(H, (Dv + kValRows - 1) / kValRows, (S + kTokBlock - 1) / kTokBlock);
     return launch_pdl(mla_value_kernel<FMT>, grid, dim3(kValThreads), smem, st, (const uint8_t *)w.codes,
-                      (const float *)w.scales, (long long)w.ld, H, Dn, Dv, K, S, (const float *)clat, ctx);
+                      (const float *)w.scales, w.gs, w.G_ld, (long long)w.ld, H, Dn, Dv, K, S, (const float *)clat,
+                      ctx);
 }
 
 }  // namespace

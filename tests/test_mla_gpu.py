@@ -19,8 +19,10 @@ def q():
     return q
 
 
-def _case(fmt, H, Dn, Dv, K, R, S, T, seed):
+def _case(fmt, H, Dn, Dv, K, R, S, T, seed, gs=0):
     codes, sc = synth.quant_tensor(fmt, H * (Dn + Dv), K, seed, 1, 5e-3, 2e-2)
+    if gs:
+        sc = synth.uniform_f32((H * (Dn + Dv), -(-K // gs)), 5e-3, 2e-2, seed, 6)
     qn = synth.normal_f32((S, H, Dn), seed, 2, std=4.0)
     qr = synth.normal_f32((S, H, R), seed, 3)
     lat = synth.normal_f32((T, K), seed, 4)
@@ -28,12 +30,12 @@ def _case(fmt, H, Dn, Dv, K, R, S, T, seed):
     return codes, sc, qn, qr, lat, rope
 
 
-def _run(q, fmt, H, Dn, Dv, K, R, S, T, st0, scale, seed=0, order=None, garbage=True):
+def _run(q, fmt, H, Dn, Dv, K, R, S, T, st0, scale, seed=0, order=None, garbage=True, gs=0):
     """Caches filled through b200q_kv_append into pages placed by `order`;
     with `garbage`, positions before st0 and the rest of the last page
     (positions >= T) hold NaN."""
     import torch
-    codes, sc, qn, qr, lat, rope = _case(fmt, H, Dn, Dv, K, R, S, T, seed)
+    codes, sc, qn, qr, lat, rope = _case(fmt, H, Dn, Dv, K, R, S, T, seed, gs)
     if garbage:                    # rows before the window: NaN, which neither side may read
         lat[:st0] = np.nan
         rope[:st0] = np.nan
@@ -46,12 +48,12 @@ def _run(q, fmt, H, Dn, Dv, K, R, S, T, st0, scale, seed=0, order=None, garbage=
         kv.rope_pool.fill_(float("nan"))
     kv.append(to_dev(lat), to_dev(rope) if R else None, 0, T)
     ctx = torch.empty((S, H, Dv), dtype=torch.float32, device="cuda")
-    with q.tensor_upload(fmt, H * (Dn + Dv), K, codes, sc) as t:
+    with q.tensor_upload(fmt, H * (Dn + Dv), K, codes, sc, gs=gs) as t:
         kv.attend(t, H, Dn, Dv, to_dev(qn), to_dev(qr) if R else None, T, st0, scale, ctx, S)
         torch.cuda.synchronize()
         assert q.device_status() == q.OK
         got = ctx.cpu().numpy()
-    ref, bound = oracle.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, st0, scale)
+    ref, bound = oracle.mla_absorb(fmt, H, Dn, Dv, K, codes, sc, qn, qr, lat, rope, st0, scale, gs=gs)
     return got, ref, bound
 
 
@@ -158,12 +160,30 @@ def test_mla_argument_errors(q):
         with pytest.raises(q.B200QError):
             kv.attend(t, H, Dn, Dv, qn, qr, 10, 0, 0.5, qn, 1)           # ctx overlaps q_nope
         kv.attend(t, H, Dn, Dv, qn, qr, 10, 0, 0.5, ctx, 0)              # S = 0: no-op
-    cg, sg = synth.codes(2, H * (Dn + Dv), K, 0, 1), synth.uniform_f32((H * (Dn + Dv), 1), 5e-3, 2e-2, 0, 2)
-    with q.tensor_upload(2, H * (Dn + Dv), K, cg, sg, gs=32) as t:
-        with pytest.raises(q.B200QError):
-            kv.attend(t, H, Dn, Dv, qn, qr, 10, 0, 0.5, ctx, 1)          # group-wise scales
     c6, s6 = synth.quant_tensor(2, H * (Dn + Dv), 18, 0, 1, 5e-3, 2e-2)
     with q.tensor_upload(2, H * (Dn + Dv), 18, c6, s6) as t:
         kv18 = q.PagedKV(18, R, 64)
         with pytest.raises(q.B200QError):
             kv18.attend(t, H, Dn, Dv, qn, qr, 10, 0, 0.5, ctx, 1)        # K not a multiple of 4
+
+
+GS_CASES = [  # fmt, gs, H, Dn, Dv, K, R, S, T, st0
+    (2, 32, 3, 16, 12, 256, 8, 2, 150, 3), (2, 128, 4, 8, 8, 512, 16, 1, 100, 0), (2, 16, 2, 8, 24, 96, 4, 3, 70, 10),
+    (1, 16, 3, 12, 10, 128, 8, 2, 90, 0), (1, 48, 2, 8, 8, 200, 4, 1, 64, 5), (3, 64, 2, 8, 8, 192, 8, 2, 80, 0),
+    (3, 16, 3, 4, 8, 64, 4, 1, 33, 1), (0, 8, 2, 4, 6, 40, 4, 2, 50, 7),
+]
+
+
+@pytest.mark.parametrize("case", GS_CASES, ids=lambda c: "f%d_gs%d_K%d_S%d" % (c[0], c[1], c[5], c[7]))
+def test_mla_group_scaled_weights(q, case):
+    """Wkv_b with group-wise scales (one per row and gs columns), every format."""
+    fmt, gs, H, Dn, Dv, K, R, S, T, st0 = case
+    got, ref, bound = _run(q, fmt, H, Dn, Dv, K, R, S, T, st0, 0.3, seed=gs + K, gs=gs)
+    assert_within(got.reshape(S, -1), ref.reshape(S, -1), bound.reshape(S, -1), TOL_F32, str(case))
+
+
+def test_mla_full_size_int4_group_scaled(q):
+    """64 heads, latent 512 + rope 64, 4096 positions, int4 Wkv_b with gs = 128."""
+    H, Dn, Dv, K, R, T, S = 64, 128, 128, 512, 64, 4096, 1
+    got, ref, bound = _run(q, 2, H, Dn, Dv, K, R, S, T, 0, (Dn + R) ** -0.5, seed=9, garbage=False, gs=128)
+    assert_within(got.reshape(S, -1), ref.reshape(S, -1), bound.reshape(S, -1), TOL_F32, "full gs")
