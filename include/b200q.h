@@ -390,6 +390,15 @@ int b200q_mla_absorb(const b200q_tensor *wkv_b, int H, int Dn, int Dv, const flo
 int b200q_kv_append(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos, const float *lat_rows,
                     const float *rope_rows, int n, void *stream);
 
+/*
+ * Self test of the bounded waits: one kernel waits, at most wait_us
+ * microseconds (1 .. 10^6), on an mbarrier that nothing arrives on, gives up
+ * and records B200Q_ETIMEOUT the way a kernel whose copies never land does.
+ * The next b200q_device_status reports it (and clears it); the context stays
+ * usable.  Asynchronous on `stream`; one launch.
+ */
+int b200q_selftest_timeout(int wait_us, void *stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char *b200q_last_error(void);
 

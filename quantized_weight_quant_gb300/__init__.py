@@ -67,6 +67,8 @@ def _load():
     L.b200q_mla_absorb.restype = ci
     L.b200q_kv_append.argtypes = [vp, vp, ci, ci, ci, vp, vp, ci, vp]
     L.b200q_kv_append.restype = ci
+    L.b200q_selftest_timeout.argtypes = [ci, vp]
+    L.b200q_selftest_timeout.restype = ci
     L.b200q_silu_mul.argtypes = [vp, vp, vp, cl, vp]
     L.b200q_silu_mul.restype = ci
     L.b200q_matmul_host.argtypes = [vp, vp, vp, ci, vp]
@@ -283,6 +285,12 @@ def rmsnorm(x, w, y, S: int, D: int, eps: float, r=None, h=None, stream=None) ->
     """y = (x + r) * w / sqrt(mean((x + r)^2) + eps) per row; h receives x + r
     when given (b200q_rmsnorm)."""
     _check(lib.b200q_rmsnorm(_dptr(x), _dptr(r), _dptr(h), _dptr(w), _dptr(y), S, D, eps, _stream(stream)))
+
+
+def selftest_timeout(wait_us: int, stream=None) -> None:
+    """A kernel waits wait_us on an mbarrier nothing completes and records a
+    timeout (b200q_selftest_timeout); device_status() then reports it."""
+    _check(lib.b200q_selftest_timeout(wait_us, _stream(stream)))
 
 
 KV_PAGE_TOKENS = 64

@@ -40,6 +40,7 @@ cudaError_t launch_mla_absorb(const Tensor &w, int H, int Dn, int Dv, const floa
 cudaError_t launch_kv_append(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos,
                              const float *lat_rows, const float *rope_rows, int n, cudaStream_t st);
 cudaError_t mla_take_error(unsigned int *code);
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st);
 
 namespace {
 
@@ -668,3 +669,11 @@ int b200q_kv_append(float *const *lat_pages, float *const *rope_pages, int K, in
 }
 
 }  // extern "C"
+
+extern "C" int b200q_selftest_timeout(int wait_us, void *stream) {
+    if (wait_us < 1 || wait_us > 1000000)
+        return fail(B200Q_EINVAL, "b200q_selftest_timeout: wait_us must be in [1, 1000000] (got %d)", wait_us);
+    cudaError_t e = launch_wait_selftest((unsigned long long)wait_us * 1000ull, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "b200q_selftest_timeout");
+    return B200Q_OK;
+}

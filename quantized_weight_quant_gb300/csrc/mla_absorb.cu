@@ -656,6 +656,20 @@ __global__ void __launch_bounds__(kValThreads) mla_value_kernel(const uint8_t *_
     }
 }
 
+// ---------------------------------------------------------------- bounded-wait self test
+// One thread waits, with the given limit, on an mbarrier that nothing
+// arrives on: the wait gives up and records B200Q_ETIMEOUT exactly as a
+// kernel whose copies never land would (b200q_selftest_timeout).
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(b, 0, limit_ns)) record_error(B200Q_ETIMEOUT);
+    }
+}
+
 // ---------------------------------------------------------------- cache append
 __global__ void kv_append_kernel(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos,
                                  const float *__restrict__ lat_rows, const float *__restrict__ rope_rows, int n) {
@@ -828,6 +842,12 @@ cudaError_t launch_mla_absorb(const Tensor &w, int H, int Dn, int Dv, const floa
 cudaError_t launch_kv_append(float *const *lat_pages, float *const *rope_pages, int K, int R, int pos,
                              const float *lat_rows, const float *rope_rows, int n, cudaStream_t st) {
     kv_append_kernel<<<n, 128, 0, st>>>(lat_pages, rope_pages, K, R, pos, lat_rows, rope_rows, n);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns);
     count_launch();
     return cudaGetLastError();
 }

@@ -140,3 +140,9 @@ def test_mla_argument_errors_without_gpu(built_lib):
     assert L.b200q_kv_append(16, None, 8, 4, 0, 48, None, 2, None) == q.EINVAL
     assert L.b200q_kv_append(16, None, 8, 0, 0, 48, None, 0, None) == q.OK     # n = 0: no-op
     assert q.KV_PAGE_TOKENS == 64
+
+
+def test_selftest_timeout_argument_errors_without_gpu(built_lib):
+    import quantized_weight_quant_gb300 as q
+    assert q.lib.b200q_selftest_timeout(0, None) == q.EINVAL
+    assert q.lib.b200q_selftest_timeout(2000000, None) == q.EINVAL

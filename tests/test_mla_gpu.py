@@ -187,3 +187,25 @@ def test_mla_full_size_int4_group_scaled(q):
     H, Dn, Dv, K, R, T, S = 64, 128, 128, 512, 64, 4096, 1
     got, ref, bound = _run(q, 2, H, Dn, Dv, K, R, S, T, 0, (Dn + R) ** -0.5, seed=9, garbage=False, gs=128)
     assert_within(got.reshape(S, -1), ref.reshape(S, -1), bound.reshape(S, -1), TOL_F32, "full gs")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(q):
+    """A wait that runs out (an mbarrier nothing arrives on, 2 ms limit) is
+    reported once by b200q_device_status; the next calls run normally."""
+    import torch
+    q.device_status()                                   # start from a clean record
+    q.selftest_timeout(2000)
+    with pytest.raises(q.B200QError) as ei:
+        q.device_status()
+    assert ei.value.status == q.ETIMEOUT
+    assert q.device_status() == q.OK                    # cleared
+    fmt, O, I = 2, 64, 256
+    codes, sc = synth.quant_tensor(fmt, O, I, 0, 1, 5e-3, 2e-2)
+    x = synth.activations(1, I, 0, 2)
+    y_ref, bound = oracle.matmul(fmt, O, I, codes, sc, x)
+    with q.tensor_upload(fmt, O, I, codes, sc) as t:
+        y = torch.empty((1, O), dtype=torch.float32, device="cuda")
+        q.matmul(t, to_dev(x), y, 1)
+        torch.cuda.synchronize()
+        assert_within(y.cpu().numpy(), y_ref, bound, TOL_F32, "after timeout")
+    assert q.device_status() == q.OK
