@@ -257,6 +257,8 @@ struct GemmParams {
     int g_last;          // last group index a padded column may reach (clamp)
     int g_one;           // a thread's 32 columns of a k-block lie in one group (gs % 32 == 0)
     GroupDiv gdiv;       // by the group size
+    int ksplit;          // > 1: CTA b takes tile b / ksplit over part (b % ksplit) of the k-blocks and
+                         // writes its partial result to plane (b % ksplit) of y ([ksplit][S][O])
 };
 
 // BNT: columns of the B tile (tokens, or x pieces).  PIECES: B holds three
@@ -296,6 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles_total = p.m_tiles * p.n_tiles;
+    // this CTA's work, walked identically by every warp role: persistent over
+    // tiles (each over all k-blocks), or with ksplit > 1 one tile over a
+    // contiguous part of its k-blocks
+    const bool split = p.ksplit > 1;
+    const int t_first = split ? (int)blockIdx.x / p.ksplit : (int)blockIdx.x;
+    const int t_step = split ? n_tiles_total : (int)gridDim.x;
+    const int kb0 = split ? ((int)blockIdx.x % p.ksplit) * p.nk / p.ksplit : 0;
+    const int kb1 = split ? ((int)blockIdx.x % p.ksplit + 1) * p.nk / p.ksplit : p.nk;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -327,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
+            for (int tile = t_first; tile < n_tiles_total && ok; tile += t_step) {
                 const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BNT;
-                for (int kb = 0; kb < p.nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1)) {
                         ok = false;
                         break;
@@ -361,12 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int t = 0;
-            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x, ++t) {
+            for (int tile = t_first; tile < n_tiles_total && ok; tile += t_step, ++t) {
                 const int ab = t & 1;
                 if (!mbar_wait(smem_u32(&acc_empty[ab]), ((t >> 1) & 1) ^ 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * kAccStride;
-                for (int kb = 0; kb < p.nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&a_full[stage]), phase)) {
                         ok = false;
                         break;
@@ -377,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         mma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), kIdesc,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                                 (kb > kb0 || k > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty[stage]));
                     if (++stage == kStages) {
                         stage = 0;
@@ -413,9 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dst[i] = __ldg(p.scales + o * p.g_ld + g);
             }
         };
-        if (GSM == 1 && blockIdx.x < n_tiles_total) load_gs(blockIdx.x, 0, gsn);
-        for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
-            for (int kb = 0; kb < p.nk; ++kb) {
+        if (GSM == 1 && t_first < n_tiles_total) load_gs(t_first, kb0, gsn);
+        for (int tile = t_first; tile < n_tiles_total && ok; tile += t_step) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if constexpr (GSM == 1) {
                     if (p.g_one) {
                         const ScalePair sp = split_scale(gsn[0]);
@@ -425,8 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kGW; ++i) gsc[i] = split_scale(gsn[i]);
                     }
-                    if (kb + 1 < p.nk) load_gs(tile, kb + 1, gsn);
-                    else if (tile + (int)gridDim.x < n_tiles_total) load_gs(tile + gridDim.x, 0, gsn);
+                    if (kb + 1 < kb1) load_gs(tile, kb + 1, gsn);
+                    else if (tile + t_step < n_tiles_total) load_gs(tile + t_step, kb0, gsn);
                 }
                 if (!mbar_wait(smem_u32(&tma_full[stage]), phase)) {
                     ok = false;
@@ -485,8 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- epilogue: TMEM lanes 32 * (warp % 4) ..
         const int quarter = warp & 3;
+        float *yplane = split ? p.y + (long long)((int)blockIdx.x % p.ksplit) * p.S * p.O : p.y;
         int t = 0;
-        for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++t) {
+        for (int tile = t_first; tile < n_tiles_total; tile += t_step, ++t) {
             const int ab = t & 1;
             if (!mbar_wait(smem_u32(&acc_full[ab]), (t >> 1) & 1)) break;
             tc_fence_after();
@@ -508,8 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int s3 = 0; s3 < BNT / 3; ++s3)
                         if (s3 < p.S) {
                             const float2 u = p.unscale[s3];
-                            const float dot = (((v[3 * s3] + v[3 * s3 + 1]) + v[3 * s3 + 2]) * u.x) * u.y;   // exact scaling
-                            p.y[(long long)s3 * p.O + o] = dot * sc;
+                            if (split) {   // still in the pieces' scaled units; unscaled after the planes are added
+                                yplane[(long long)s3 * p.O + o] = ((v[3 * s3] + v[3 * s3 + 1]) + v[3 * s3 + 2]) * sc;
+                            } else {
+                                const float dot = (((v[3 * s3] + v[3 * s3 + 1]) + v[3 * s3 + 2]) * u.x) * u.y;   // exact scaling
+                                yplane[(long long)s3 * p.O + o] = dot * sc;
+                            }
                         }
                 }
             } else {
@@ -521,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (o < p.O) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (s0 + j < p.S) p.y[(long long)(s0 + j) * p.O + o] = v[j] * sc;
+                            if (s0 + j < p.S) yplane[(long long)(s0 + j) * p.O + o] = v[j] * sc;
                     }
                 }
             }
@@ -697,7 +712,7 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out) {
 // b_rows: rows of the bf16 B operand (tokens, or the padded pieces rows).
 template <int FMT, int BNT, bool PIECES, int GSM = 0>
 cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const float2 *unscale, float *y, int S,
-                     cudaStream_t st) {
+                     cudaStream_t st, int ksplit = 1) {
     constexpr bool GS = GSM != 0;
     constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
     CUtensorMap map_codes, map_x, map_sc;
@@ -722,6 +737,7 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
     p.n_tiles = PIECES ? 1 : (S + BNT - 1) / BNT;
     p.nk = (int)(t.k_pad / BK);
     p.code_bytes = code_bytes;
+    p.ksplit = ksplit;
     if (GS) {
         int c = 0;
         while ((1ll << c) < t.gs) ++c;
@@ -746,7 +762,7 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
         attr[dev] = true;
     }
     const int tiles = p.m_tiles * p.n_tiles;
-    const int grid = tiles < g_sms ? tiles : g_sms;
+    const int grid = ksplit > 1 ? tiles * ksplit : tiles < g_sms ? tiles : g_sms;
     qgemm_tc_kernel<FMT, BNT, PIECES, GSM><<<grid, kThreads, smem, st>>>(map_codes, map_x, map_sc, p);
     count_launch();
     return cudaGetLastError();
@@ -803,6 +819,19 @@ cudaError_t workspace_free(void *ptr, cudaStream_t st);
 // f32-accurate tensor-core path (B200Q_PATH_TCX): x split into three exact
 // bf16 pieces, at most 15 tokens (45 piece columns) per GEMM launch.  With tu
 // the same pieces serve the second tensor.
+// y[s, o] = (sum of the ks planes' partials, in plane order) * 2^-k(s): the
+// split k-blocks' partials are kept in the pieces' scaled units so that the
+// unscaling (exact powers of two) rounds once, after the sum.
+__global__ void sum_planes_kernel(const float *__restrict__ planes, const float2 *__restrict__ unscale,
+                                  float *__restrict__ y, long long n, int O, int ks) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        float v = planes[i];
+        for (int k = 1; k < ks; ++k) v += planes[(long long)k * n + i];
+        const float2 u = unscale[i / O];
+        y[i] = (v * u.x) * u.y;
+    }
+}
+
 template <int FMT>
 cudaError_t run_tcx_chunk(const Tensor &t, const Tensor *tu, const __nv_bfloat16 *pc, int bnt,
                           const float2 *unscale, float *y, float *yu, int ns, cudaStream_t st) {
@@ -810,9 +839,33 @@ cudaError_t run_tcx_chunk(const Tensor &t, const Tensor *tu, const __nv_bfloat16
     for (int k = 0; k < (tu ? 2 : 1) && e == cudaSuccess; ++k) {
         const Tensor &tt = k ? *tu : t;
         float *yy = k ? yu : y;
-        e = bnt == 16   ? run_gemm<FMT, 16, true>(tt, pc, bnt, unscale, yy, ns, st)
-            : bnt == 32 ? run_gemm<FMT, 32, true>(tt, pc, bnt, unscale, yy, ns, st)
-                        : run_gemm<FMT, 48, true>(tt, pc, bnt, unscale, yy, ns, st);
+        // fewer row tiles than half the SMs: split each tile's k-blocks over
+        // several CTAs (each keeps at least 4 k-blocks); their partials go to
+        // planes of a workspace and are added in plane order
+        const int tiles = tt.o_pad / BM, nk = (int)(tt.k_pad / BK);
+        int ks = tiles * 2 <= g_sms ? g_sms / tiles : 1;
+        if (ks > 4) ks = 4;
+        if (ks > nk / 4) ks = nk / 4 > 1 ? nk / 4 : 1;
+        float *dst = yy;
+        const long long n = (long long)ns * tt.O;
+        if (ks > 1) {
+            e = workspace_alloc((void **)&dst, (size_t)ks * n * sizeof(float), st);
+            if (e != cudaSuccess) break;
+        }
+        e = bnt == 16   ? run_gemm<FMT, 16, true>(tt, pc, bnt, unscale, dst, ns, st, ks)
+            : bnt == 32 ? run_gemm<FMT, 32, true>(tt, pc, bnt, unscale, dst, ns, st, ks)
+                        : run_gemm<FMT, 48, true>(tt, pc, bnt, unscale, dst, ns, st, ks);
+        if (ks > 1) {
+            if (e == cudaSuccess) {
+                long long blocks = (n + 255) / 256;
+                if (blocks > (long long)g_sms * 4) blocks = (long long)g_sms * 4;
+                sum_planes_kernel<<<(int)blocks, 256, 0, st>>>(dst, unscale, yy, n, tt.O, ks);
+                count_launch();
+                e = cudaGetLastError();
+            }
+            cudaError_t ef = workspace_free(dst, st);
+            if (e == cudaSuccess) e = ef;
+        }
     }
     return e;
 }
