@@ -301,11 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this CTA's work, walked identically by every warp role: persistent over
     // tiles (each over all k-blocks), or with ksplit > 1 one tile over a
     // contiguous part of its k-blocks
-    const bool split = p.ksplit > 1;
+    const bool split = PIECES && p.ksplit > 1;         // only the three-piece path splits (compile-time off otherwise)
     const int t_first = split ? (int)blockIdx.x / p.ksplit : (int)blockIdx.x;
     const int t_step = split ? n_tiles_total : (int)gridDim.x;
     const int kb0 = split ? ((int)blockIdx.x % p.ksplit) * p.nk / p.ksplit : 0;
     const int kb1 = split ? ((int)blockIdx.x % p.ksplit + 1) * p.nk / p.ksplit : p.nk;
+    // Loop heads of every role.  Variants that cannot split use blockIdx /
+    // gridDim / p.nk directly (unsigned stepping, as written before splitting
+    // existed): the compiler then schedules them ~5% faster.
+#define QWQ_TILE_FIRST (PIECES ? (unsigned)t_first : blockIdx.x)
+#define QWQ_TILE_STEP (PIECES ? (unsigned)t_step : gridDim.x)
+#define QWQ_KB_FIRST (PIECES ? kb0 : 0)
+#define QWQ_KB_END (PIECES ? kb1 : p.nk)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -337,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int tile = t_first; tile < n_tiles_total && ok; tile += t_step) {
+            for (int tile = QWQ_TILE_FIRST; tile < n_tiles_total && ok; tile += QWQ_TILE_STEP) {
                 const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BNT;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = QWQ_KB_FIRST; kb < QWQ_KB_END; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1)) {
                         ok = false;
                         break;
@@ -371,12 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int t = 0;
-            for (int tile = t_first; tile < n_tiles_total && ok; tile += t_step, ++t) {
+            for (int tile = QWQ_TILE_FIRST; tile < n_tiles_total && ok; tile += QWQ_TILE_STEP, ++t) {
                 const int ab = t & 1;
                 if (!mbar_wait(smem_u32(&acc_empty[ab]), ((t >> 1) & 1) ^ 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * kAccStride;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = QWQ_KB_FIRST; kb < QWQ_KB_END; ++kb) {
                     if (!mbar_wait(smem_u32(&a_full[stage]), phase)) {
                         ok = false;
                         break;
@@ -387,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         mma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), kIdesc,
-                                 (kb > kb0 || k > 0) ? 1u : 0u);
+                                 (kb > QWQ_KB_FIRST || k > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty[stage]));
                     if (++stage == kStages) {
                         stage = 0;
@@ -424,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         if (GSM == 1 && t_first < n_tiles_total) load_gs(t_first, kb0, gsn);
-        for (int tile = t_first; tile < n_tiles_total && ok; tile += t_step) {
-            for (int kb = kb0; kb < kb1; ++kb) {
+        for (int tile = QWQ_TILE_FIRST; tile < n_tiles_total && ok; tile += QWQ_TILE_STEP) {
+            for (int kb = QWQ_KB_FIRST; kb < QWQ_KB_END; ++kb) {
                 if constexpr (GSM == 1) {
                     if (p.g_one) {
                         const ScalePair sp = split_scale(gsn[0]);
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         float *yplane = split ? p.y + (long long)((int)blockIdx.x % p.ksplit) * p.S * p.O : p.y;
         int t = 0;
-        for (int tile = t_first; tile < n_tiles_total; tile += t_step, ++t) {
+        for (int tile = QWQ_TILE_FIRST; tile < n_tiles_total; tile += QWQ_TILE_STEP, ++t) {
             const int ab = t & 1;
             if (!mbar_wait(smem_u32(&acc_full[ab]), (t >> 1) & 1)) break;
             tc_fence_after();
@@ -552,6 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
+#undef QWQ_TILE_FIRST
+#undef QWQ_TILE_STEP
+#undef QWQ_KB_FIRST
+#undef QWQ_KB_END
 }
 
 // x f32 [S, I] -> bf16 [S, k_pad] (RNE, zero past I); int4 tensors get each
