@@ -5,7 +5,9 @@
  *
  *     y[s,o] = scale[o] * sum_i deq(W[o,i]) * x[s,i]
  *
- * against S activation rows.  Sources for the operation: the page "CUDA 后端"
+ * against S activation rows, plus the calls built on it: the gate/up pair,
+ * grouped expert calls, RMSNorm glue and MLA decode attention with weight
+ * absorption over paged caches.  Sources for the operation: the page "CUDA 后端"
  * (colibri-analysis 09), section 1, "设备侧库 backend_cuda.cu" (the resident
  * tensor, `weight_at`, `quant_matmul` and the five extern "C" functions of the
  * backend), and the page "第 8 章 · 02 CUDA/Metal/Vulkan 三后端", section 四
@@ -34,6 +36,10 @@
  *                   rounded to bf16 (nearest, ties to even) inside the call,
  *                   products and sums are f32 on the tensor cores:
  *                   |y - y_exact| <= 4e-3 * |scale[o]| * sum_i |deq * x|
+ * Tensors with group-wise scales (b200q_tensor_upload_grouped) follow the same
+ * bounds with the scale taken per group: on the tensor-core path each weight
+ * is (code - zero point) * scale rounded to bf16 once; the three-piece path
+ * refuses them.
  * NaN and Inf inputs are outside the contract, and so are f32-weight products
  * |w * x| below the f32 normal range (2^-126): f32 arithmetic rounds them on
  * the subnormal grid.  Quantized formats stage each row of x scaled by an
