@@ -422,11 +422,12 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes, f32 x/y",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded: int4 codes uniform 0..15, scales U[5e-3,2e-2], x ~ N(0,1))",
         "config": {"workload": "int4 decode GEMV O=12288 I=6144 S=1, one step = one token through "
                                "%d resident copies" % R,
-                   "O": O, "I": I, "S": S, "copies": R, "global_batch": S * world,
+                   "O": O, "I": I, "S": S, "weights": "int4 codes, f32 row scales", "x_y": "f32",
+                   "copies": R, "global_batch": S * world,
                    "l2": "inputs larger than L2: %d distinct weight copies, %.0f MB per step > 3x L2"
                          % (R, wl.bytes_per_step / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -820,7 +821,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4 codes, f64 accumulation", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "int4 decode GEMV O=12288 I=6144 S=1 (one step = one call of the CPU oracle "
                                "on the whole tensor)", "O": O, "I": I, "S": S},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
