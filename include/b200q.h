@@ -367,7 +367,8 @@ enum { B200Q_KV_PAGE_TOKENS = 64 };
  *               be a full 64-row allocation, 16-byte aligned, non-NULL
  *   rope_pages  the same for the rope cache, [64, R] f32 pages (unused when R = 0)
  *   R           rope width, a multiple of 4 (K + R at most 716)
- *   T           positions in the caches, S <= T <= 2^30
+ *   T           positions in the caches, S <= T <= 2^30 (and H * S <= 2^20,
+ *               S <= 262140)
  *   st0         first position any token sees, 0 <= st0 <= T - S; pages
  *               wholly before st0 are never read
  *   scale       softmax scale, finite

@@ -635,6 +635,7 @@ int b200q_mla_absorb(const b200q_tensor *wkv_b, int H, int Dn, int Dv, const flo
         return fail(B200Q_EINVAL, "%s: need S <= T <= 2^30 and 0 <= st0 <= T - S (got T=%d, st0=%d, S=%d)", who, T,
                     st0, S);
     if ((long long)H * S > (1 << 20)) return fail(B200Q_EINVAL, "%s: H * S above 2^20", who);
+    if (S > 4 * 65535) return fail(B200Q_EINVAL, "%s: S above %d (token blocks of 4 per grid row)", who, 4 * 65535);
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return fail(B200Q_EINVAL, "%s: scale must be finite", who);
     if (!q_nope || !ctx || !lat_pages || (R && (!q_rope || !rope_pages)))
         return fail(B200Q_EINVAL, "%s: device pointers must not be NULL", who);
