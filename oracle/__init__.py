@@ -260,6 +260,8 @@ def mla_absorb(fmt: int, H: int, Dn: int, Dv: int, K: int, codes, scales, q_nope
     rc = _L().qref_mla_absorb(fmt, H, Dn, Dv, K, R, _ptr(codes), _ptr(scales), gs, _ptr(q_nope), _ptr(q_rope),
                               _ptr(lat), _ptr(rope), T, st0, float(scale), S, _ptr(ctx), _ptr(cd),
                               _ptr(bound))
+    if rc == -2:
+        raise MemoryError("qref_mla_absorb: out of host memory for the per-row scratch vectors")
     if rc:
         raise ValueError("qref_mla_absorb: bad argument")
     return (ctx, bound, cd) if want_dbl else (ctx, bound)

@@ -324,8 +324,10 @@ int qref_matmul_bf16x(int fmt, long O, long I, const uint8_t *codes, const float
  *     A = max_t |scale| * (sum_i QA_i |L[t,i]| + sum_j |q_rope_j Rr[t,j]|),
  *     QA_i = sum_d |q_nope_d Wk[h,d,i]|
  * (a score error of eps * A moves p_t by at most 2 eps A p_t, and the value
- * step adds its own eps).  Returns 0, or -1 for a bad argument (S < 1,
- * T < S, st0 < 0 or st0 > T - S: every window must hold a position).
+ * step adds its own eps).  Returns 0, -1 for a bad argument (S < 1,
+ * T < S, st0 < 0 or st0 > T - S: every window must hold a position), or -2
+ * when host memory for the per-row scratch vectors cannot be had (the
+ * outputs are then incomplete and must not be used).
  */
 /* Scale of element i of weight row `row` (see qref_mla_absorb). */
 static double mla_scale(const float *scales, long gs, long G, long row, long i)
@@ -347,6 +349,7 @@ int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
     if (!codes || !q_nope || (R > 0 && (!q_rope || !rope)) || !lat || !ctx || gs < 0 || (gs && !scales)) return -1;
     long HS = H * S;
     long G = gs ? (K + gs - 1) / gs : 1;
+    int oom = 0;                                       /* set by any row whose scratch malloc failed */
 #ifdef _OPENMP
     int nt = qref_max_threads();
 #pragma omp parallel for schedule(dynamic) num_threads(nt)
@@ -364,6 +367,10 @@ int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
         double *sabs = (double *)malloc(sizeof(double) * (size_t)nwin);
         if (!qabs || !qa || !clat || !cabs || !score || !sabs) {
             free(qabs); free(qa); free(clat); free(cabs); free(score); free(sabs);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            oom = 1;
             continue;
         }
         const float *qn = q_nope + (s * H + h) * Dn;
@@ -429,5 +436,5 @@ int qref_mla_absorb(int fmt, long H, long Dn, long Dv, long K, long R,
         }
         free(qabs); free(qa); free(clat); free(cabs); free(score); free(sabs);
     }
-    return 0;
+    return oom ? -2 : 0;
 }
