@@ -328,27 +328,122 @@ def time_e2e(wl, steps, warmup):
     return (t1 - t0) * 1e3, h2d, d2h
 
 
-def cpu_baseline_decode(O, I, S, fmt=I4, seconds=3.0):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def time_oracle(fn, seconds, min_calls=1):
+    """Calls fn() until `seconds` of wall time (and at least min_calls calls)
+    have passed, after one untimed warm call; returns (calls, seconds)."""
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds and n >= min_calls:
+            return n, dt
+
+
+def cpu_baseline_decode(O, I, S, fmt=I4, seconds=3.0, seconds_1=2.0):
     """The oracle as it stands on the host cores, on the full decode workload
-    repeated until `seconds` of CPU time have passed."""
+    repeated until `seconds` have passed: on all cores, then on one core."""
     import oracle
     import synth
     lo, hi = (5e-3, 2e-2)
     codes, scales = synth.quant_tensor(fmt, O, I, 0, 1, lo, hi)
     x = synth.activations(S, I, 0, 9999)
-    oracle.set_threads(0)
-    oracle.matmul(fmt, O, I, codes, scales, x)          # warm
-    n, t0 = 0, time.perf_counter()
-    while True:
-        oracle.matmul(fmt, O, I, codes, scales, x)
-        n += 1
-        dt = time.perf_counter() - t0
-        if dt >= seconds:
-            break
     bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
-    gbs = algorithmic_bytes(bits, O, I, S) * n / dt / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": "full O=%d I=%d S=%d int4 matmul, %d calls in %.1f s" % (O, I, S, n, dt)}
+    per = algorithmic_bytes(bits, O, I, S)
+    oracle.set_threads(0)
+    cores = oracle.max_threads()
+    n, dt = time_oracle(lambda: oracle.matmul(fmt, O, I, codes, scales, x), seconds)
+    oracle.set_threads(1)
+    n1, dt1 = time_oracle(lambda: oracle.matmul(fmt, O, I, codes, scales, x), seconds_1)
+    oracle.set_threads(0)
+    return {"value": round(per * n / dt / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": "full O=%d I=%d S=%d int4 matmul, %d calls in %.1f s" % (O, I, S, n, dt),
+            "cores_1": {"value": round(per * n1 / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                        "sample": "the same call on one core, %d calls in %.1f s" % (n1, dt1)}}
+
+
+def run_cpu_plan(args):
+    """The oracle timed on every workload on the host cores (one JSON line
+    each): configs 1, 2 and 4 at S=1 on all cores and on one core, config 2
+    at S=4, the MoE expert layer and the W4A16 prefill call on all cores."""
+    import oracle
+    import synth
+    model = cpu_model()
+    oracle.set_threads(0)
+    cores = oracle.max_threads()
+
+    def emit(name, per_call_bytes, flops, fn, threads, seconds):
+        oracle.set_threads(threads)
+        n, dt = time_oracle(fn, seconds)
+        oracle.set_threads(0)
+        ms = dt * 1e3 / n
+        line = {"workload": name, "impl": "oracle", "cores": cores if threads == 0 else threads,
+                "cpu_model": model, "ms_per_call": round(ms, 3), "calls": n,
+                "GB/s": round(per_call_bytes / (ms * 1e-3) / 1e9, 4),
+                "GFLOP/s": round(flops / (ms * 1e-3) / 1e9, 3)}
+        print(json.dumps(line), flush=True)
+
+    cases = [("int8 256x512 S=1", 1, 256, 512, 1, (1e-3, 1e-2)),
+             ("int4 12288x6144 S=1", I4, 12288, 6144, 1, (5e-3, 2e-2)),
+             ("int4 12288x6144 S=4", I4, 12288, 6144, 4, (5e-3, 2e-2))]
+    cases += [("%s 8192x8192 S=1" % nm, f, 8192, 8192, 1, (1e-3, 2e-2))
+              for nm, f in (("f32", 0), ("int8", 1), ("int4", 2), ("int2", 3))]
+    for name, fmt, O, I, S, (lo, hi) in cases:
+        codes, scales = synth.quant_tensor(fmt, O, I, 0, 1, lo, hi)
+        x = synth.activations(S, I, 0, 9999)
+        bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
+        fn = (lambda c=codes, sc=scales, xx=x, f=fmt, o=O, i=I: oracle.matmul(f, o, i, c, sc, xx))
+        for threads in ((0, 1) if S == 1 else (0,)):
+            emit(name, algorithmic_bytes(bits, O, I, S), 2.0 * O * I * S, fn, threads, 1.0)
+    # MoE expert layer, S=1: 8 experts' gate/up, silu(g)*u, down
+    D, F = 6144, 2048
+    ex = []
+    for e in range(8):
+        cg, sg = synth.quant_tensor(I4, F, D, 0, 10 + 3 * e, 5e-3, 2e-2)
+        cu, su = synth.quant_tensor(I4, F, D, 0, 11 + 3 * e, 5e-3, 2e-2)
+        cd, sd = synth.quant_tensor(I4, D, F, 0, 12 + 3 * e, 5e-3, 2e-2)
+        ex.append((cg, sg, cu, su, cd, sd))
+    xm = synth.activations(1, D, 0, 9999)
+
+    def moe():
+        for cg, sg, cu, su, cd, sd in ex:
+            g, _, u, _ = oracle.matmul_gate_up(I4, F, D, cg, sg, cu, su, xm)
+            _, h = oracle.silu_mul(g, u)
+            oracle.matmul(I4, D, F, cd, sd, h)
+    moe_bytes = 8 * (2 * algorithmic_bytes(4, F, D, 1) + algorithmic_bytes(4, D, F, 1))
+    emit("MoE layer S=1, 8 experts (gate/up, silu*up, down)", moe_bytes, 8 * 3 * 2.0 * F * D, moe, 0, 1.0)
+    # W4A16 prefill call, all cores (one call is about ten seconds)
+    O, I, S = 12288, 6144, 1571
+    codes, scales = synth.quant_tensor(I4, O, I, 0, 1, 5e-3, 2e-2)
+    x = synth.activations(S, I, 0, 9999)
+    oracle.set_threads(0)
+    t0 = time.perf_counter()
+    oracle.matmul(I4, O, I, codes, scales, x)
+    dt = time.perf_counter() - t0
+    print(json.dumps({"workload": "prefill W4A16 12288x6144 S=1571", "impl": "oracle", "cores": cores,
+                      "cpu_model": model, "ms_per_call": round(dt * 1e3, 1), "calls": 1,
+                      "GFLOP/s": round(2.0 * O * I * S / dt / 1e9, 3)}), flush=True)
 
 
 def prefill_measure(q, steps, warmup, stream, gs=0):
@@ -481,6 +576,11 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(O, I, S)
     if rank == 0:
+        # the headline's own figures close the line (a reader that keeps only
+        # the end of stdout still has them): decode roofline, prefill last
+        for k in ("e2e_host_call", "cpu_baseline", "e2e", "roofline", "prefill_w4a16"):
+            if k in line:
+                line[k] = line.pop(k)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -825,7 +925,7 @@ def run_reference(args):
         "config": {"workload": "int4 decode GEMV O=12288 I=6144 S=1 (one step = one call of the CPU oracle "
                                "on the whole tensor)", "O": O, "I": I, "S": S},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": "full O=12288 I=6144 S=1 int4 matmul per step"},
+                         "cpu_model": cpu_model(), "sample": "full O=12288 I=6144 S=1 int4 matmul per step"},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -841,7 +941,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-moe", action="store_true")
     ap.add_argument("--no-mla", action="store_true")
-    ap.add_argument("--workload", default="default", choices=["default", "sweep", "decode", "prefill", "moe", "mla"])
+    ap.add_argument("--workload", default="default",
+                    choices=["default", "sweep", "decode", "prefill", "moe", "mla", "cpu"])
     ap.add_argument("--fmt", default="i4", choices=["f32", "i8", "i4", "i2"])
     ap.add_argument("--O", type=int, default=12288)
     ap.add_argument("--I", type=int, default=6144)
@@ -854,6 +955,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "cpu":
+        run_cpu_plan(args)
     elif args.workload == "sweep":
         run_sweep(args)
     elif args.workload in ("decode", "prefill"):

@@ -302,9 +302,11 @@ int b200q_matmul_host(const b200q_tensor *t, const float *x_host, float *y_host,
  * All calls on a device share the array, which keeps the last call's
  * contents; calls whose work overlaps in time on the GPU (for instance on two
  * streams without ordering between them) race on it and must be serialized by
- * the caller.  The first call on each device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.
+ * the caller.  Every call looks up the array's device address in the
+ * current device's context (cudaGetSymbolAddress, a host-side query), so a
+ * context that was reset and recreated gets its own address; the first
+ * lookup on a device may load the library's device code into that context,
+ * so make the first call on each device before any stream capture.
  */
 int b200q_matmul_tc_noalloc(const b200q_tensor *t, const float *x, float *y, int S, void *stream);
 
@@ -334,6 +336,17 @@ int b200q_device_status(void);
  * region.
  */
 long long b200q_kernel_launches(void);
+
+/*
+ * Number of device workspace allocations the library has made on its
+ * callers' behalf so far (all devices, all threads): the creation of a
+ * device's stream-ordered memory pool, every allocation from it (the
+ * tensor-core paths' converted copy of x, split-K partials, MLA and grouped
+ * call scratch) and the host-buffer call's staging buffer.  Tensor uploads
+ * (the tensors' own memory) are not counted.  A call that must not allocate,
+ * such as b200q_matmul_tc_noalloc, leaves it unchanged.
+ */
+long long b200q_workspace_allocations(void);
 
 /*
  * ---- MLA decode attention with weight absorption ----

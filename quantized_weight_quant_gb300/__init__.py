@@ -84,6 +84,8 @@ def _load():
     L.b200q_device_status.restype = ci
     L.b200q_kernel_launches.argtypes = []
     L.b200q_kernel_launches.restype = cll
+    L.b200q_workspace_allocations.argtypes = []
+    L.b200q_workspace_allocations.restype = cll
     L.b200q_last_error.argtypes = []
     L.b200q_last_error.restype = ctypes.c_char_p
     return L
@@ -99,6 +101,11 @@ def last_error() -> str:
 def kernel_launches() -> int:
     """Kernels launched through the library so far in this process."""
     return int(lib.b200q_kernel_launches())
+
+
+def workspace_allocations() -> int:
+    """Device workspace allocations the library has made so far in this process."""
+    return int(lib.b200q_workspace_allocations())
 
 
 def device_status() -> int:

@@ -11,6 +11,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "qwq_internal.h"
 
@@ -106,6 +107,41 @@ Staging g_staging[64];
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+namespace {
+std::atomic<long long> g_ws_allocs{0};
+std::atomic<int> g_sm_count[64];
+struct SmemAttr {
+    const void *fn;
+    int dev, bytes;
+};
+std::mutex g_attr_mu;
+std::vector<SmemAttr> g_attr_done;
+}  // namespace
+
+void count_workspace_alloc() { g_ws_allocs.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count(int dev) {
+    if (dev < 0 || dev >= 64) return 1;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+cudaError_t allow_dynamic_smem(const void *fn, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (const SmemAttr &a : g_attr_done)
+        if (a.fn == fn && a.dev == dev && a.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_attr_done.push_back(SmemAttr{fn, dev, bytes});
+    return e;
+}
+
 void read_thresholds() {
     std::call_once(g_tc_once, [] {
         auto env_int = [](const char *name, int dflt) {
@@ -175,6 +211,8 @@ extern "C" {
 const char *b200q_last_error(void) { return g_err.c_str(); }
 
 long long b200q_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+long long b200q_workspace_allocations(void) { return g_ws_allocs.load(std::memory_order_relaxed); }
 
 int b200q_device_status(void) {
     cudaError_t e = cudaDeviceSynchronize();
@@ -323,6 +361,7 @@ b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, cons
                         (uint64_t)t->o_pad, (uint64_t)t->G_ld * sizeof(float), (uint32_t)t->sc_box, 8,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         e = cudaErrorNotSupported;
+    if (e == cudaSuccess && !gemm_maps_encode(*t)) e = cudaErrorNotSupported;
     if (e != cudaSuccess) {
         cuda_fail(e, who);
         cudaGetLastError();
@@ -587,6 +626,7 @@ int b200q_matmul_host(const b200q_tensor *h, const float *x_host, float *y_host,
             sg.cap = 0;
             if (e != cudaSuccess) return cuda_fail(e, "b200q_matmul_host: free staging");
         }
+        count_workspace_alloc();
         e = cudaMalloc(&sg.buf, xb_al + yb);
         if (e != cudaSuccess) {
             sg.buf = nullptr;

@@ -686,8 +686,6 @@ __global__ void kv_append_kernel(float *const *lat_pages, float *const *rope_pag
     for (int k = threadIdx.x; k < R; k += blockDim.x) rp[(size_t)off * R + k] = rope_rows[(size_t)i * R + k];
 }
 
-int g_sms = 0;
-
 template <class... P, class... A>
 cudaError_t launch_pdl(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A... args) {
     cudaLaunchConfig_t cfg = {};
@@ -706,22 +704,17 @@ cudaError_t launch_pdl(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cuda
 }
 
 template <class Kern>
-cudaError_t allow_smem(Kern k, size_t bytes, bool *done) {
-    if (bytes <= 48 * 1024 || *done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess) *done = true;
-    return e;
+cudaError_t allow_smem(Kern k, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return allow_dynamic_smem((const void *)k, 227 * 1024);
 }
 
 template <int FMT>
 cudaError_t run_absorb(const Tensor &w, int H, int Dn, int Dv, const float *q_nope, int S, float *qabs,
                        cudaStream_t st) {
     constexpr int EW = Word<FMT>::EW;
-    static bool attr[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
     const size_t smem = (size_t)16 * kTokBlock * EW * 32 * 4;   // int2: 128 KB
-    cudaError_t e = allow_smem(mla_absorb_kernel<FMT>, smem, &attr[dev & 63]);
+    cudaError_t e = allow_smem(mla_absorb_kernel<FMT>, smem);
     if (e != cudaSuccess) return e;
     const int K = w.I, nwords = (K + EW - 1) / EW;
     dim3 grid(H, (nwords + 31) / 32, (S + kTokBlock - 1) / kTokBlock);
@@ -751,14 +744,12 @@ int mla_max_latent() { return 4 * 64 * kQuads; }
 // Workspace floats a call needs (qabs + split partials); n_split from the
 // same rule the launcher uses.
 static int mla_splits(int H, int S, int T, int st0) {
-    if (!g_sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int n_sms = sm_count(dev);
     const int rb = (H * S + kRows - 1) / kRows;
     const int n_tiles = (T - 1) / kTile - st0 / kTile + 1;
-    int n = (g_sms + rb - 1) / rb;
+    int n = (n_sms + rb - 1) / rb;
     if (n > n_tiles) n = n_tiles;
     if (n > kMaxSplit) n = kMaxSplit;
     return n < 1 ? 1 : n;
@@ -808,18 +799,14 @@ cudaError_t launch_mla_absorb(const Tensor &w, int H, int Dn, int Dv, const floa
     p.tile0 = st0 / kTile;
     p.n_tiles = (T - 1) / kTile - p.tile0 + 1;
     p.n_split = n_split;
-    static bool attr[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
     const size_t smem = mla_smem_bytes(K, R);
     dim3 grid(n_split, (HS + kRows - 1) / kRows);
     if (K == 512 && R == 64) {      // the pages' model shape: widths fixed at compile time
-        e = allow_smem(mla_attn_kernel<512, 64>, smem, &attr[dev & 63]);
+        e = allow_smem(mla_attn_kernel<512, 64>, smem);
         if (e != cudaSuccess) return e;
         e = launch_pdl(mla_attn_kernel<512, 64>, grid, dim3(kAttnThreads), smem, st, p);
     } else {
-        static bool attr_g[64] = {};
-        e = allow_smem(mla_attn_kernel<0, 0>, smem, &attr_g[dev & 63]);
+        e = allow_smem(mla_attn_kernel<0, 0>, smem);
         if (e != cudaSuccess) return e;
         e = launch_pdl(mla_attn_kernel<0, 0>, grid, dim3(kAttnThreads), smem, st, p);
     }

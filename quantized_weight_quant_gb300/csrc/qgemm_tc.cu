@@ -702,7 +702,13 @@ __global__ void __launch_bounds__(kPieceThreads)
 
 cudaMemPool_t g_pool[64] = {};
 std::mutex g_pool_mu;
-int g_sms = 0;
+
+}  // namespace
+
+cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st);
+cudaError_t workspace_free(void *ptr, cudaStream_t st);
+
+namespace {
 
 cudaError_t get_pool(int dev, cudaMemPool_t *out) {
     std::lock_guard<std::mutex> lk(g_pool_mu);
@@ -713,6 +719,7 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out) {
         props.location.id = dev;
         cudaError_t e = cudaMemPoolCreate(&g_pool[dev], &props);
         if (e != cudaSuccess) return e;
+        count_workspace_alloc();
         uint64_t keep = ~0ull;   // keep freed workspace cached in the pool
         cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
     }
@@ -726,15 +733,9 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
                      cudaStream_t st, int ksplit = 1) {
     constexpr bool GS = GSM != 0;
     constexpr int code_bytes = FMT == B200Q_I4 ? 32 : 64;
-    CUtensorMap map_codes, map_x, map_sc;
-    memset(&map_sc, 0, sizeof map_sc);
-    if (GSM == 2 &&
-        !tmap_encode_2d(&map_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, t.scales, (uint64_t)t.G_ld, (uint64_t)t.o_pad,
-                        (uint64_t)t.G_ld * 4, kScaleBox, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    if (!tmap_encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
-                   (uint64_t)t.ld, code_bytes, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+    // the codes' and group scales' maps were encoded at upload; only x's
+    // (a per-call workspace) is encoded here
+    CUtensorMap map_x;
     if (!tmap_encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)xb, (uint64_t)t.k_pad, (uint64_t)b_rows,
                    (uint64_t)t.k_pad * 2, BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -761,20 +762,12 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
     constexpr int kStages = stages_for<FMT, BNT, GSM>();
     const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BNT * BK * 2 + C_BYTES + (GSM == 2 ? kScaleTile : 0)) +
                         (3 * kStages + 4) * 8 + 16;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = allow_dynamic_smem((const void *)qgemm_tc_kernel<FMT, BNT, PIECES, GSM>, (int)smem);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static bool attr[64] = {};
-    if (!attr[dev]) {
-        e = cudaFuncSetAttribute(qgemm_tc_kernel<FMT, BNT, PIECES, GSM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        attr[dev] = true;
-    }
+    const int n_sms = sm_count(t.device);
     const int tiles = p.m_tiles * p.n_tiles;
-    const int grid = ksplit > 1 ? tiles * ksplit : tiles < g_sms ? tiles : g_sms;
-    qgemm_tc_kernel<FMT, BNT, PIECES, GSM><<<grid, kThreads, smem, st>>>(map_codes, map_x, map_sc, p);
+    const int grid = ksplit > 1 ? tiles * ksplit : tiles < n_sms ? tiles : n_sms;
+    qgemm_tc_kernel<FMT, BNT, PIECES, GSM><<<grid, kThreads, smem, st>>>(t.gemm_map, map_x, t.gemm_sc_map, p);
     count_launch();
     return cudaGetLastError();
 }
@@ -795,19 +788,14 @@ cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x,
                               cudaStream_t st, bool *handled) {
     *handled = false;
     if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return cudaSuccess;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaMemPool_t pool;
-    cudaError_t e = get_pool(dev, &pool);
-    if (e != cudaSuccess) return e;
+    const int n_sms = sm_count(t.device);
     const size_t ws_bytes = (size_t)S * t.k_pad * 2;
     void *ws = nullptr;
-    e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, st);
+    cudaError_t e = workspace_alloc(&ws, ws_bytes, st);
     if (e != cudaSuccess) return e;
     const long long groups = (long long)S * t.k_pad / 8;
     long long blocks = (groups + 255) / 256;
-    if (blocks > (long long)g_sms * 16) blocks = (long long)g_sms * 16;
+    if (blocks > (long long)n_sms * 16) blocks = (long long)n_sms * 16;
     x_to_bf16_kernel<<<(int)blocks, 256, 0, st>>>(x, (__nv_bfloat16 *)ws, S, t.I, (int)t.k_pad,
                                                    t.fmt == B200Q_I4 ? 1 : 0);
     count_launch();
@@ -823,9 +811,6 @@ cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x,
     *handled = (e == cudaSuccess);
     return e;
 }
-
-cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st);
-cudaError_t workspace_free(void *ptr, cudaStream_t st);
 
 // f32-accurate tensor-core path (B200Q_PATH_TCX): x split into three exact
 // bf16 pieces, at most 15 tokens (45 piece columns) per GEMM launch.  With tu
@@ -854,7 +839,8 @@ cudaError_t run_tcx_chunk(const Tensor &t, const Tensor *tu, const __nv_bfloat16
         // several CTAs (each keeps at least 4 k-blocks); their partials go to
         // planes of a workspace and are added in plane order
         const int tiles = tt.o_pad / BM, nk = (int)(tt.k_pad / BK);
-        int ks = tiles * 2 <= g_sms ? g_sms / tiles : 1;
+        const int n_sms = sm_count(tt.device);
+        int ks = tiles * 2 <= n_sms ? n_sms / tiles : 1;
         if (ks > 4) ks = 4;
         if (ks > nk / 4) ks = nk / 4 > 1 ? nk / 4 : 1;
         float *dst = yy;
@@ -869,7 +855,7 @@ cudaError_t run_tcx_chunk(const Tensor &t, const Tensor *tu, const __nv_bfloat16
         if (ks > 1) {
             if (e == cudaSuccess) {
                 long long blocks = (n + 255) / 256;
-                if (blocks > (long long)g_sms * 4) blocks = (long long)g_sms * 4;
+                if (blocks > (long long)n_sms * 4) blocks = (long long)n_sms * 4;
                 sum_planes_kernel<<<(int)blocks, 256, 0, st>>>(dst, unscale, yy, n, tt.O, ks);
                 count_launch();
                 e = cudaGetLastError();
@@ -885,10 +871,7 @@ cudaError_t launch_tcx(const Tensor &t, const Tensor *tu, const float *x, float 
                        cudaStream_t st, bool *handled) {
     *handled = false;
     if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaSuccess;
     for (int s0 = 0; s0 < S && e == cudaSuccess;) {
         const int ns = S - s0 < 15 ? S - s0 : 15;
         const int bnt = 3 * ns <= 16 ? 16 : 3 * ns <= 32 ? 32 : 48;
@@ -923,7 +906,25 @@ cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st) {
     cudaMemPool_t pool;
     e = get_pool(dev, &pool);
     if (e != cudaSuccess) return e;
+    count_workspace_alloc();
     return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
+}
+
+// Tensor maps of the GEMM over an uploaded tensor: the codes as bytes
+// [o_pad, ld] with a box of 128 rows x one k-block's code bytes, and the
+// group scales [o_pad, G_ld] f32 with a box of 128 rows x 4.
+bool gemm_maps_encode(Tensor &t) {
+    memset(&t.gemm_map, 0, sizeof t.gemm_map);
+    memset(&t.gemm_sc_map, 0, sizeof t.gemm_sc_map);
+    if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return true;
+    const uint32_t code_bytes = t.fmt == B200Q_I4 ? 32 : 64;
+    if (!tmap_encode_2d(&t.gemm_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.codes, (uint64_t)t.ld, (uint64_t)t.o_pad,
+                        (uint64_t)t.ld, code_bytes, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    if (t.gs && !tmap_encode_2d(&t.gemm_sc_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, t.scales, (uint64_t)t.G_ld,
+                                (uint64_t)t.o_pad, (uint64_t)t.G_ld * 4, kScaleBox, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    return true;
 }
 
 cudaError_t workspace_free(void *ptr, cudaStream_t st) { return cudaFreeAsync(ptr, st); }
@@ -944,25 +945,19 @@ cudaError_t workspace_free(void *ptr, cudaStream_t st) { return cudaFreeAsync(pt
 constexpr size_t kNoAllocBytes = 24u << 20;   // 24 MiB: S * k_pad bf16 values
 static __device__ __align__(256) uint8_t g_noalloc_ws[kNoAllocBytes];
 
-namespace {
-void *g_noalloc_ptr[64] = {};
-std::mutex g_noalloc_mu;
-}  // namespace
-
 size_t noalloc_capacity() { return kNoAllocBytes; }
 
-// Device address of the array on the current device.  Resolved once per
-// device (with that device current) by the first call made on it.
-cudaError_t noalloc_workspace(int dev, void **out) {
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
-        if (e != cudaSuccess) return e;
-        g_noalloc_ptr[dev] = ptr;
-    }
-    *out = g_noalloc_ptr[dev];
+// Device address of the array in the current device's context, looked up
+// on every call (a host-side query, not a stream operation), so that a call
+// after the context was reset or recreated gets the new address rather than
+// a stale one.  The first lookup on a device may load the library's device
+// code into that context, which is why the first call should come before
+// any stream capture.
+cudaError_t noalloc_workspace(void **out) {
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+    if (e != cudaSuccess) return e;
+    *out = ptr;
     return cudaSuccess;
 }
 
@@ -970,16 +965,13 @@ cudaError_t noalloc_workspace(int dev, void **out) {
 // the tensor-core path.  The caller has checked fmt and that
 // S * k_pad * 2 <= kNoAllocBytes.
 cudaError_t launch_prefill_tc_noalloc(const Tensor &t, const float *x, float *y, int S, cudaStream_t st) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (!g_sms) cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     void *ws = nullptr;
-    e = noalloc_workspace(dev, &ws);
+    cudaError_t e = noalloc_workspace(&ws);
     if (e != cudaSuccess) return e;
+    const int n_sms = sm_count(t.device);
     const long long groups = (long long)S * t.k_pad / 8;
     long long blocks = (groups + 255) / 256;
-    if (blocks > (long long)g_sms * 16) blocks = (long long)g_sms * 16;
+    if (blocks > (long long)n_sms * 16) blocks = (long long)n_sms * 16;
     x_to_bf16_kernel<<<(int)blocks, 256, 0, st>>>(x, (__nv_bfloat16 *)ws, S, t.I, (int)t.k_pad,
                                                    t.fmt == B200Q_I4 ? 1 : 0);
     count_launch();

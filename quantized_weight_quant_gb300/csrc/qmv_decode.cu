@@ -926,8 +926,6 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     }
 }
 
-int g_sms = 0;
-
 // One group: n sets, each a tensor with its input(s) and output at token 0.
 struct Group {
     const Tensor *t[kMaxSets];
@@ -970,17 +968,8 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     // the kernel's row-group and unit arithmetic is 32-bit
     if ((long long)grid * p.n_rg >= (1ll << 31) || (long long)nw * rr * nseg >= (1ll << 31))
         return cudaErrorInvalidValue;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = allow_dynamic_smem((const void *)qmv_decode_kernel<FMT, NS, MS, GW>, (int)kSmemMax);
     if (e != cudaSuccess) return e;
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(qmv_decode_kernel<FMT, NS, MS, GW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemMax);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     DecParams<MS> q = p;
     q.depth = depth;
     q.round_rgs = rr;
@@ -1008,12 +997,8 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
 
 template <int FMT, int MS, int GW>
 cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
-    if (!g_sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    }
     const Tensor &t0 = *g.t[0];
+    const int n_sms = sm_count(t0.device);
     DecParams<MS> p;
     memset(&p, 0, sizeof p);
     p.nsets = g.n;
@@ -1039,7 +1024,7 @@ cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
     }
     p.rg_start[g.n] = n_rg;
     p.n_rg = n_rg;
-    const int grid = n_rg < g_sms ? n_rg : g_sms;
+    const int grid = n_rg < n_sms ? n_rg : n_sms;
     // most x slots a CTA spans (the same partition as the kernel's)
     int nx_max = 1;
     for (int b = 0, s = 0; b < grid; ++b) {

@@ -21,6 +21,8 @@ namespace qwq {
 struct Tensor {
     CUtensorMap dec_map;  // codes as uint32 [o_pad, ld / 4], box 8 rows x 512 bytes (decode stages)
     CUtensorMap sc_map;   // group scales as f32 [o_pad, G_ld], box 8 rows x sc_box (decode stages)
+    CUtensorMap gemm_map;     // int8 / int4 codes as bytes [o_pad, ld], box 128 rows x one k-block (tensor-core GEMM)
+    CUtensorMap gemm_sc_map;  // group scales as f32 [o_pad, G_ld], box 128 rows x 4 (tensor-core GEMM)
     int fmt;
     int O, I;
     int device;
@@ -67,11 +69,28 @@ bool tmap_encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, ui
 // Counts kernel launches made through the library (b200q_kernel_launches).
 void count_launch(int n = 1);
 
+// Counts device workspace allocations the library makes on a call's behalf
+// (stream-ordered pool allocations, the pool's creation, the host-call
+// staging buffer); b200q_workspace_allocations reports the total.
+void count_workspace_alloc();
+
+// Multiprocessor count of device dev, read once per device; safe when
+// several host threads make their first calls at the same time.
+int sm_count(int dev);
+
+// Raises kernel fn's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device, bytes); thread-safe.
+cudaError_t allow_dynamic_smem(const void *fn, int bytes);
+
 // ---- kernels (launchers return cudaGetLastError() after the launch) ----
 
 // Tail fix after the upload copy: forces the unused high bits of every row's
 // last host byte to the zero-point pattern.
 cudaError_t launch_fix_row_tails(const Tensor &t, long long rb, cudaStream_t st);
+
+// Encodes the tensor-core GEMM's tensor maps of an uploaded int8 / int4
+// tensor (codes, and group scales when gs > 0); other formats need none.
+bool gemm_maps_encode(Tensor &t);
 
 // f32-accurate SIMT path, any format, any S.  With tu != nullptr the launch
 // also computes yu = matmul(tu, x) (gate/up pair, same shape as t).

@@ -73,3 +73,10 @@ def test_committed_traffic_records_name_existing_sources(bench):
             for f in kv["sources"].split(","):
                 assert os.path.exists(os.path.join(ROOT, f)), f
             assert float(kv["bytes_per_launch"]) > 0
+
+
+def test_cpu_model_and_oracle_timer(bench):
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+    calls = []
+    n, dt = bench.time_oracle(lambda: calls.append(1), 0.01, min_calls=3)
+    assert n >= 3 and dt >= 0.01 and len(calls) == n + 1    # one untimed warm call

@@ -112,6 +112,23 @@ def test_prefill_12288x6144_s1571_sampled(q, fmt):
     assert np.all(np.isfinite(y))
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", [2, 1], ids=["i4", "i8"])
+def test_prefill_12288x6144_s1571_full(q, fmt):
+    """Every output of the W4A16 (and W8A16) prefill call O=12288, I=6144,
+    S=1571, in the launch configuration the benchmark times, against the
+    oracle (118.6 G double multiply-adds, about ten seconds on 16 host cores):
+    the persistent walk over all 96 x 9 output tiles, each over 96 k-blocks, is
+    compared in full, not only at sampled rows and tokens."""
+    O, I, S = 12288, 6144, 1571
+    codes, scales, x = inputs(fmt, O, I, S, seed=0)
+    with q.tensor_upload(fmt, O, I, codes, scales) as t:
+        assert q.matmul_path(t, S) == q.PATH_TC
+        y = gpu_matmul(q, t, x, S, O)
+    y_ref, bound = oracle.matmul(fmt, O, I, codes, scales, x)
+    assert_within(y, y_ref, bound, TOL_TC, "prefill full fmt%d" % fmt)
+
+
 def test_gate_up_tc(q):
     import torch
     fmt, O, I, S = 2, 2048, 6144, 40
