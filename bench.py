@@ -204,10 +204,11 @@ def job_throughput(bytes_per_rank_step, steps, world, ms_max):
 class Decode:
     """R distinct resident [O, I] tensors, S tokens: one step = R matmul calls."""
 
-    def __init__(self, q, fmt, O, I, S, R, seed=0, gs=0):
+    def __init__(self, q, fmt, O, I, S, R, seed=0, gs=0, path=None):
         import torch
         import synth
         self.q, self.fmt, self.O, self.I, self.S, self.R = q, fmt, O, I, S, R
+        self.path = path                # None: b200q_matmul (AUTO); else b200q_matmul_ex with this path
         self.tensors = []
         lo, hi = {0: (1e-3, 2e-2), 1: (1e-3, 1e-2), 2: (5e-3, 2e-2), 3: (1e-3, 2e-2)}[fmt]
         for r in range(R):
@@ -226,7 +227,10 @@ class Decode:
 
     def step(self, stream):
         for r in range(self.R):
-            self.q.matmul(self.tensors[r], self.x, self.y[r], self.S, stream)
+            if self.path is None:
+                self.q.matmul(self.tensors[r], self.x, self.y[r], self.S, stream)
+            else:
+                self.q.matmul_ex(self.tensors[r], self.x, self.y[r], self.S, self.path, stream)
 
     def close(self):
         for t in self.tensors:
@@ -634,12 +638,13 @@ def run_single(args):
     bits = {0: 32, 1: 8, 2: 4, 3: 2}[fmt]
     per = algorithmic_bytes(bits, args.O, args.I, args.S)
     R = args.copies or max(2, min(64, -(-3 * L2_BYTES // per)))
-    wl = Decode(q, fmt, args.O, args.I, args.S, R, gs=args.gs)
+    path = {"auto": None, "f32": q.PATH_F32, "tc": q.PATH_TC, "tcx": q.PATH_TCX, "tcs": q.PATH_TCS}[args.path]
+    wl = Decode(q, fmt, args.O, args.I, args.S, R, gs=args.gs, path=path)
     ms, launches = time_steps(wl, args.steps, args.warmup, stream)
     sec = ms * 1e-3
     print(json.dumps({"workload": "%s %s O=%d I=%d S=%d gs=%d" % (args.workload, args.fmt, args.O, args.I, args.S,
                                                                   args.gs),
-                      "path": q.matmul_path(wl.tensors[0], args.S),
+                      "path": q.matmul_path(wl.tensors[0], args.S) if path is None else path,
                       "GB/s": round(wl.bytes_per_step * args.steps / sec / 1e9, 1),
                       "frac_hbm": round(wl.bytes_per_step * args.steps / sec / 1e9 / pk["hbm_gbs"], 4),
                       "TFLOP/s": round(wl.flops_per_step * args.steps / sec / 1e12, 2),
@@ -950,6 +955,8 @@ def main():
     ap.add_argument("--gs", type=int, default=0, help="group size of the scales (0: one per row)")
     ap.add_argument("--T", type=int, default=0, help="cached positions of the mla workload (0: its default cases)")
     ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: enough for 3x L2)")
+    ap.add_argument("--path", default="auto", choices=["auto", "f32", "tc", "tcx", "tcs"],
+                    help="matmul path of the decode / prefill workload (auto: the library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

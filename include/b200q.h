@@ -79,7 +79,7 @@ enum {
 };
 
 /* Path selection for b200q_matmul_ex. */
-enum { B200Q_PATH_AUTO = 0, B200Q_PATH_F32 = 1, B200Q_PATH_TC = 2, B200Q_PATH_TCX = 3 };
+enum { B200Q_PATH_AUTO = 0, B200Q_PATH_F32 = 1, B200Q_PATH_TC = 2, B200Q_PATH_TCX = 3, B200Q_PATH_TCS = 4 };
 
 /*
  * Upload one weight tensor to the current device and keep it resident.
@@ -154,9 +154,26 @@ int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *s
  * As b200q_matmul with an explicit path: B200Q_PATH_AUTO (same as
  * b200q_matmul), B200Q_PATH_F32 (the f32-accurate SIMT kernels at any S, any
  * format), B200Q_PATH_TCX (the f32-accurate tensor-core path, x in three bf16
- * pieces, any S >= 1, at most 15 rows per launch) or B200Q_PATH_TC (the bf16
- * tensor-core path at any S >= 1).  The tensor-core paths take int8 and int4
- * tensors only (B200Q_EINVAL otherwise).
+ * pieces, any S >= 1, at most 15 rows per launch), B200Q_PATH_TCS (the
+ * f32-accurate tensor-core path with the weights in tensor memory, below) or
+ * B200Q_PATH_TC (the bf16 tensor-core path at any S >= 1).  TCX and TC take
+ * int8 and int4 tensors only, TCS int8, int4 and int2 tensors with per-row
+ * scales (B200Q_EINVAL otherwise).
+ *
+ * B200Q_PATH_TCS: each 128-row tile of codes is dequantized to exact fp16
+ * integers straight into tensor memory (tcgen05.st) and multiplied there
+ * (tcgen05.mma, A in tensor memory) against x split into two fp16 pieces per
+ * token: x * 2^k with a power of two that brings the largest |x| among the
+ * columns one CTA handles to [2^14, 2^15), p0 = fp16(x 2^k), p1 = fp16(x 2^k
+ * - p0), which carry x to 2^-22 relative; products are exact in f32 and
+ * accumulate in f32.  Bound: that of the f32 path, for tokens whose largest
+ * |x| is up to ~3e5 times their typical |x| (beyond that the pieces of the
+ * smallest elements fall below fp16's range, as the f32 path's outlier
+ * limit).  At most 16 tokens per launch; the work is split evenly over the
+ * SMs in (row tile, 128-byte k-block) items, and a tile shared by several
+ * CTAs is added up, in CTA order and in common units, by the CTA holding its
+ * last k-block.  Each call with shared tiles takes a workspace from the
+ * library's pool.
  */
 int b200q_matmul_ex(const b200q_tensor *t, const float *x, float *y, int S, int path,
                     void *stream);

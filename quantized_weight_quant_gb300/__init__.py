@@ -17,7 +17,7 @@ import numpy as np
 
 F32, I8, I4, I2 = 0, 1, 2, 3
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4
-PATH_AUTO, PATH_F32, PATH_TC, PATH_TCX = 0, 1, 2, 3
+PATH_AUTO, PATH_F32, PATH_TC, PATH_TCX, PATH_TCS = 0, 1, 2, 3, 4
 GROUP_MAX = 16
 FORMATS = {"f32": F32, "i8": I8, "i4": I4, "i2": I2}
 

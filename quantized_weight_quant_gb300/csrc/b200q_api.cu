@@ -25,6 +25,8 @@ cudaError_t launch_tcx(const Tensor &t, const Tensor *tu, const float *x, float 
 cudaError_t launch_prefill_tc(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu,
                               int S, cudaStream_t st, bool *handled);
 cudaError_t decode_take_error(unsigned int *code);
+cudaError_t launch_tcs(const Tensor &t, const float *x, float *y, int S, cudaStream_t st, bool *handled);
+cudaError_t tcs_take_error(unsigned int *code);
 size_t noalloc_capacity();
 cudaError_t launch_prefill_tc_noalloc(const Tensor &t, const float *x, float *y, int S, cudaStream_t st);
 cudaError_t prefill_take_error(unsigned int *code);
@@ -184,7 +186,24 @@ int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, floa
     path = select_path(t, S, path);
     cudaError_t e = cudaSuccess;
     bool handled = false;
-    if (path == B200Q_PATH_TC || path == B200Q_PATH_TCX) {
+    if (path == B200Q_PATH_TCS) {
+        if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8 && t.fmt != B200Q_I2)
+            return fail(B200Q_EINVAL, "%s: the f32-accurate tensor-core path takes int8, int4 and int2 tensors only",
+                        who);
+        if (t.gs || (tu && tu->gs))
+            return fail(B200Q_EINVAL, "%s: the f32-accurate tensor-core path takes per-row scales only", who);
+        // at most 16 rows per launch; the pair's second tensor runs after the first
+        for (int k = 0; k < (tu ? 2 : 1) && e == cudaSuccess; ++k) {
+            const Tensor &tt = k ? *tu : t;
+            float *yy = k ? yu : y;
+            for (int s0 = 0; s0 < S && e == cudaSuccess; s0 += 16) {
+                const int ns = S - s0 < 16 ? S - s0 : 16;
+                e = launch_tcs(tt, x + (long long)s0 * tt.I, yy + (long long)s0 * tt.O, ns, st, &handled);
+                if (e == cudaSuccess && !handled)
+                    return fail(B200Q_ECUDA, "%s: no f32-accurate tensor-core kernel for this shape", who);
+            }
+        }
+    } else if (path == B200Q_PATH_TC || path == B200Q_PATH_TCX) {
         if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8)
             return fail(B200Q_EINVAL, "%s: the tensor-core paths take int8 and int4 tensors only", who);
         if (path == B200Q_PATH_TCX && (t.gs || (tu && tu->gs)))
@@ -217,12 +236,13 @@ long long b200q_workspace_allocations(void) { return g_ws_allocs.load(std::memor
 int b200q_device_status(void) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "b200q_device_status");
-    unsigned int a = 0, b = 0, m = 0;
+    unsigned int a = 0, b = 0, m = 0, c = 0;
     e = decode_take_error(&a);
     if (e == cudaSuccess) e = prefill_take_error(&b);
     if (e == cudaSuccess) e = mla_take_error(&m);
+    if (e == cudaSuccess) e = tcs_take_error(&c);
     if (e != cudaSuccess) return cuda_fail(e, "b200q_device_status");
-    if (a || b || m == (unsigned)(-B200Q_ETIMEOUT))
+    if (a || b || c || m == (unsigned)(-B200Q_ETIMEOUT))
         return fail(B200Q_ETIMEOUT, "b200q_device_status: a kernel gave up on a bounded wait");
     if (m) return fail(B200Q_EINVAL, "b200q_device_status: an MLA call met a NULL or unaligned cache page");
     return B200Q_OK;
@@ -362,6 +382,7 @@ b200q_tensor *upload_impl(int fmt, int O, int I, int gs, const void *codes, cons
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         e = cudaErrorNotSupported;
     if (e == cudaSuccess && !gemm_maps_encode(*t)) e = cudaErrorNotSupported;
+    if (e == cudaSuccess && !tcs_map_encode(*t)) e = cudaErrorNotSupported;
     if (e != cudaSuccess) {
         cuda_fail(e, who);
         cudaGetLastError();
@@ -427,7 +448,8 @@ int b200q_matmul_ex(const b200q_tensor *h, const float *x, float *y, int S, int 
     if (rc) return rc;
     const Tensor &t = *reinterpret_cast<const Tensor *>(h);
     if (S < 0) return fail(B200Q_EINVAL, "b200q_matmul: S must be >= 0 (got %d)", S);
-    if (path != B200Q_PATH_AUTO && path != B200Q_PATH_F32 && path != B200Q_PATH_TC && path != B200Q_PATH_TCX)
+    if (path != B200Q_PATH_AUTO && path != B200Q_PATH_F32 && path != B200Q_PATH_TC && path != B200Q_PATH_TCX &&
+        path != B200Q_PATH_TCS)
         return fail(B200Q_EINVAL, "b200q_matmul: unknown path %d", path);
     if (S == 0) return B200Q_OK;
     rc = check_io(t, x, y, S, "b200q_matmul");

@@ -23,6 +23,8 @@ struct Tensor {
     CUtensorMap sc_map;   // group scales as f32 [o_pad, G_ld], box 8 rows x sc_box (decode stages)
     CUtensorMap gemm_map;     // int8 / int4 codes as bytes [o_pad, ld], box 128 rows x one k-block (tensor-core GEMM)
     CUtensorMap gemm_sc_map;  // group scales as f32 [o_pad, G_ld], box 128 rows x 4 (tensor-core GEMM)
+    CUtensorMap tcs_map;      // int8 / int4 / int2 codes as bytes [o_pad, ld], box 128 rows x 128 bytes,
+                              // 128-byte swizzle (f32-accurate tensor-core path for few tokens)
     int fmt;
     int O, I;
     int device;
@@ -74,6 +76,11 @@ void count_launch(int n = 1);
 // staging buffer); b200q_workspace_allocations reports the total.
 void count_workspace_alloc();
 
+// Stream-ordered device workspace from the library's per-device pool
+// (counted by count_workspace_alloc), and its release on the same stream.
+cudaError_t workspace_alloc(void **ptr, size_t bytes, cudaStream_t st);
+cudaError_t workspace_free(void *ptr, cudaStream_t st);
+
 // Multiprocessor count of device dev, read once per device; safe when
 // several host threads make their first calls at the same time.
 int sm_count(int dev);
@@ -91,6 +98,9 @@ cudaError_t launch_fix_row_tails(const Tensor &t, long long rb, cudaStream_t st)
 // Encodes the tensor-core GEMM's tensor maps of an uploaded int8 / int4
 // tensor (codes, and group scales when gs > 0); other formats need none.
 bool gemm_maps_encode(Tensor &t);
+
+// Encodes Tensor::tcs_map (int8 / int4 / int2 tensors; others need none).
+bool tcs_map_encode(Tensor &t);
 
 // f32-accurate SIMT path, any format, any S.  With tu != nullptr the launch
 // also computes yu = matmul(tu, x) (gate/up pair, same shape as t).
