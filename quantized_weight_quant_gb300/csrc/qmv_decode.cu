@@ -70,9 +70,14 @@ constexpr int kMaxWarps = 16;
 //   * two tokens: 15, or 11 with group-wise scales (a second set of sums,
 //     no spills); for int4 and int2 their larger staged x is paid for with a
 //     ring stage, for f32 and int8 with warps.
+//   * four tokens (per-row scales, f32 / int8 / int4): four sets of sums and
+//     the staged x of four tokens per word; 11 warps (f32, int8), 10 (int4).
+//     int2 keeps launches of two: its 16 codes per word spill at four.
 template <int FMT, int NS, int GW>
 constexpr int max_warps() {
-    return NS == 2 ? (GW ? 11 : 15) : (FMT == B200Q_F32 || FMT == B200Q_I8) ? 16 : 15;
+    return NS == 4   ? (FMT == B200Q_I4 ? 10 : 11)
+           : NS == 2 ? (GW ? 11 : 15)
+                     : (FMT == B200Q_F32 || FMT == B200Q_I8) ? 16 : 15;
 }
 // Whether a launch that does not fit gives up a ring stage before a warp:
 // one token for f32 / int8, two tokens for int4 / int2.
@@ -362,19 +367,20 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     const int stg = kStage + scb;                     // bytes per ring stage
 
     // shared memory: x' [nx_max][NS][k_alloc] | rings [nw][depth] | full and
-    // empty mbarriers [2][nw][depth] + x-staged | partials | per-row unscale
+    // empty mbarriers [2][nw][depth] + x-staged + x-issued | partials | per-row unscale
     // factors | max scratch | done counter | row scales
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * nxr * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stg);
     const int kR = p.round_rgs;
-    float *part = reinterpret_cast<float *>(bars + 2 * nw * depth + 1);  // [kR][nw][NS][8]
+    float *part = reinterpret_cast<float *>(bars + 2 * nw * depth + 2);  // [kR][nw][NS][8]
     float *unscale = part + (size_t)kR * nw * NS * 8;                  // [nxr][2]: 2^-T as two factors
     float *red = unscale + 2 * nxr;                                    // [nxr][kMaxWarps]
     int *done = reinterpret_cast<int *>(red + nxr * kMaxWarps);        // warps done with the last round
     float *row_scale = reinterpret_cast<float *>(done + 4);           // [rows of this CTA]
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nw * depth);
     const uint32_t x_ready = smem_u32(bars + 2 * nw * depth);   // completes once x is staged
+    const uint32_t x_issued = smem_u32(bars + 2 * nw * depth + 1);  // once every consumer warp's x loads are out
 
     // (32-bit products: the host keeps grid * n_rg and nw * round units below 2^31)
     const int rg0 = fdiv(blockIdx.x * p.n_rg, p.div_grid);
@@ -425,7 +431,10 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
             mbar_init(full0 + 8 * (lane * depth + b), 1);
             mbar_init(empty0 + 8 * (lane * depth + b), 1);
         }
-        if (lane == 0) mbar_init(x_ready, 1);
+        if (lane == 0) {
+            mbar_init(x_ready, 1);
+            mbar_init(x_issued, nw);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -471,7 +480,10 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
             issue();
             more = next();
         }
-        if (!mbar_wait(x_ready, 0, kWaitNs)) more = false;   // the consumers report the same timeout
+        // the rest of the rings go out once the consumers' loads of x have
+        // been issued, so that x does not return behind them; the weights
+        // then stream while x is staged
+        if (!mbar_wait(x_issued, 0, kWaitNs)) more = false;   // the consumers report the same timeout
         for (int k = 1; k < depth && more; ++k) {
             issue();
             more = next();
@@ -620,6 +632,9 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         return r;
     };
     auto tok_scale = [&](float mt) { return tok_scale_k(mt > 0.f ? -ilogb_bits(mt) : 0); };
+    // whether the single-slot path below signals x_issued as soon as its
+    // loads are out (the other paths signal it with x_ready)
+    const bool x_issued_early = FMT != B200Q_F32 && nx == 1 && n_slots <= (kXB / 4) * nthr;
     if constexpr (FMT == B200Q_F32) {
         for (int j = 0; j < nx; ++j)
             for (int base = 0; base < p.k_pad; base += kXB * nthr) {
@@ -661,6 +676,8 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
                     const int d = j * nthr + tid;
                     held[t][j] = d < n_slots ? gather(0, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x_issued);
 #pragma unroll
             for (int t = 0; t < NS; ++t) {
                 float mt = 0.f;
@@ -723,6 +740,7 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         }
     }
     if (tid == 0) mbar_arrive(x_ready);
+    if (!x_issued_early && lane == 0) mbar_arrive(x_issued);
 
     // ---- main loop
     const uint32_t my_full = full0 + 8 * warp * depth, my_empty = empty0 + 8 * warp * depth;
@@ -775,7 +793,7 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
                                   : FMT == B200Q_F32 ? a2[r][t].x + a2[r][t].y
                                                      : (a2[r][t].x - az[t].x) + (a2[r][t].y - az[t].y);
         const float sum = reduce_scatter<NV>(v, lane);
-        constexpr int sh = NS == 2 ? 1 : 2;         // this lane holds value index lane >> sh
+        constexpr int sh = NS == 4 ? 0 : NS == 2 ? 1 : 2;   // this lane holds value index lane >> sh
         const int idx = lane >> sh;
         if ((lane & ((1 << sh) - 1)) == 0) part[(((size_t)rgl * nw + warp) * NS + idx / 8) * 8 + (idx & 7)] = sum;
         clear_acc();
@@ -946,7 +964,7 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     const int rg_cta = (p.n_rg + grid - 1) / grid;
     const size_t nxr = (size_t)p.nx_max * NS;
     auto fixed_for = [&](int nw, int rr) {
-        return 4 * nxr * k_alloc + 8 + (size_t)rr * nw * NS * 8 * 4 + nxr * 8 + nxr * kMaxWarps * 4 + 16 +
+        return 4 * nxr * k_alloc + 16 + (size_t)rr * nw * NS * 8 * 4 + nxr * 8 + nxr * kMaxWarps * 4 + 16 +
                (size_t)rg_cta * 8 * 4;
     };
     // warps and depth first (round of kRound), then grow the round to all of
@@ -1037,13 +1055,21 @@ cudaError_t launch_group_ms(const Group &g, int S, cudaStream_t st) {
     }
     p.nx_max = nx_max;
     for (int s0 = 0; s0 < S;) {
-        const int ns = S - s0 >= 2 ? 2 : 1;
+        // tokens per launch: four while at least four remain (per-row scales),
+        // else two, else one
+        const int ns = !GW && FMT != B200Q_I2 && S - s0 >= 4 ? 4 : S - s0 >= 2 ? 2 : 1;
         for (int j = 0; j < g.n; ++j) {
             p.xa[p.xslot[j]] = g.xa[j] + (long long)s0 * t0.I;
             p.xb[p.xslot[j]] = g.xb[j] ? g.xb[j] + (long long)s0 * t0.I : nullptr;
             p.y[j] = g.y[j] + (long long)s0 * g.t[j]->O;
         }
-        cudaError_t e = ns == 2 ? launch_ns<FMT, 2, MS, GW>(p, grid, st) : launch_ns<FMT, 1, MS, GW>(p, grid, st);
+        cudaError_t e;
+        if constexpr (GW == 0 && FMT != B200Q_I2)
+            e = ns == 4   ? launch_ns<FMT, 4, MS, GW>(p, grid, st)
+                : ns == 2 ? launch_ns<FMT, 2, MS, GW>(p, grid, st)
+                          : launch_ns<FMT, 1, MS, GW>(p, grid, st);
+        else
+            e = ns == 2 ? launch_ns<FMT, 2, MS, GW>(p, grid, st) : launch_ns<FMT, 1, MS, GW>(p, grid, st);
         if (e != cudaSuccess) return e;
         s0 += ns;
     }
@@ -1090,7 +1116,8 @@ cudaError_t launch_group(const Group &g, int S, cudaStream_t st, bool *handled) 
 
 }  // namespace
 
-// Handles every format for 1 <= S < 16 (tokens in launches of two);
+// Handles every format for 1 <= S < 16 (tokens in launches of four, two or
+// one);
 // *handled = false sends the call to the general SIMT kernel (x too long for
 // shared memory).
 cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, float *y, float *yu, int S,
@@ -1108,7 +1135,8 @@ cudaError_t launch_decode(const Tensor &t, const Tensor *tu, const float *x, flo
     return launch_group(g, S, st, handled);
 }
 
-// n (<= 16) tensors of one format and I in one launch per token pair; input
+// n (<= 16) tensors of one format and I in one launch per four, two or one
+// tokens; input
 // j is xa[j], or silu(xa[j]) * xb[j] when silu is set.  *handled = false when
 // the staged inputs do not fit in shared memory (the caller then runs the
 // tensors one at a time).
