@@ -21,13 +21,16 @@
 //      warps 2-9  dequantizers, two threads per weight row (each half of
 //                 the row's k-block): codes -> exact bf16 (int4: OR the
 //                 nibble into the mantissa of 128.0 and subtract 136; int8:
-//                 exact via f32), written in the 128-byte-swizzled K-major
-//                 layout the MMA reads; two warps per scheduler hide each
-//                 other's load / convert / store latency;
+//                 exact via f32), stored with tcgen05.st into one of four
+//                 A buffers in tensor memory (lane = weight row, 32 columns
+//                 = the k-block's 64 bf16); a warp owns the rows of its
+//                 lane quarter (warp % 4).  With A out of shared memory a
+//                 stage holds only codes and x, so the ring is 8 deep;
 //      warp 1     MMA issuer (one thread): 4 x tcgen05.mma (kind::f16,
-//                 bf16 in, f32 accumulate, 128 x 176 x 16) per k-block into
-//                 one of two TMEM accumulators; tcgen05.commit releases the
-//                 stage and, after the last k-block, hands the tile to ...
+//                 bf16 in, f32 accumulate, 128 x 176 x 16, A from tensor
+//                 memory) per k-block into one of two TMEM accumulators;
+//                 tcgen05.commit releases the stage and the A buffer and,
+//                 after the last k-block, hands the tile to ...
 //      warps 10-13 epilogue: tcgen05.ld of its 32 TMEM lanes, times scale[o],
 //                 coalesced f32 stores of y (32 consecutive o per store).
 //    Integer codes are exact in bf16 and products are exact in f32, so the
@@ -47,9 +50,10 @@ namespace qwq {
 namespace {
 
 constexpr int BM = 128, BN = 176, BK = 64;
-// Pipeline stages (code tile + x tile + dequantized A tile; 42.5 KB for int4
-// at 176 tokens): as many as fit in 227 KB of shared memory, at most 8, since
-// the stage ring has to cover a TMA round trip plus dequantization.
+// Pipeline stages (code tile + x tile; 26.5 KB for int4 at 176 tokens): as
+// many as fit in 227 KB of shared memory, at most 10, since the stage ring has
+// to cover a TMA round trip plus dequantization.  The dequantized A tile of a
+// k-block (128 rows x 64 bf16) lives in tensor memory, in a ring of its own.
 // Group-scale tile of a stage when the producer copies the scales (GSM = 2):
 // 128 rows x 4 f32 from a 4-aligned first group.
 constexpr int kScaleBox = 4;
@@ -57,14 +61,19 @@ constexpr int kScaleTile = BM * kScaleBox * 4;      // 2 KB
 
 template <int FMT, int BNT, int GSM = 0>
 constexpr int stages_for() {
-    constexpr int per = BM * BK * 2 + BNT * BK * 2 + BM * (FMT == B200Q_I4 ? 32 : 64) + (GSM == 2 ? kScaleTile : 0);
+    constexpr int per = BNT * BK * 2 + BM * (FMT == B200Q_I4 ? 32 : 64) + (GSM == 2 ? kScaleTile : 0);
     constexpr int n = (232448 - 1024 - 512) / per;
-    return n > 8 ? 8 : n;
+    return n > 10 ? 10 : n;
 }
 constexpr int kThreads = 448;        // 14 warps
 constexpr int kDeqWarps = 8;
-constexpr int kTmemCols = 512;       // two accumulators of up to 256 columns
-constexpr int kAccStride = 256;
+// Tensor memory: kNumA A buffers of 32 columns (a k-block of 64 bf16 per
+// lane = weight row) at columns 0.., then two accumulators of up to 192
+// columns.
+constexpr int kTmemCols = 512;
+constexpr int kNumA = 4;
+constexpr int kAccBase = kNumA * 32;   // 128
+constexpr int kAccStride = 192;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 __device__ unsigned int g_prefill_err = 0;
@@ -146,6 +155,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D (tensor memory) += A (tensor memory, 128 lanes x 16 bf16) x B (shared memory)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
@@ -279,21 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool GS = GSM != 0;
     constexpr int kStages = stages_for<FMT, BNT, GSM>();
     constexpr uint32_t kIdesc = idesc_for(BNT);
-    static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 256 && (!PIECES || BNT <= 48), "token tile");
+    static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= kAccStride && (!PIECES || BNT <= 48), "token tile");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    constexpr int A_BYTES = BM * BK * 2;               // 16384
     constexpr int B_BYTES = BNT * BK * 2;
     constexpr int C_BYTES = BM * (FMT == B200Q_I4 ? 32 : 64);
-    uint8_t *a_s = smem;                                 // [kStages][A_BYTES]
-    uint8_t *b_s = a_s + kStages * A_BYTES;              // [kStages][B_BYTES]
+    uint8_t *b_s = smem;                                 // [kStages][B_BYTES]
     uint8_t *c_s = b_s + kStages * B_BYTES;              // [kStages][C_BYTES]
     constexpr int S_BYTES = GSM == 2 ? kScaleTile : 0;
     uint8_t *s_s = c_s + kStages * C_BYTES;              // [kStages][BM][kScaleBox] f32 (GSM = 2)
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_s + kStages * S_BYTES);
-    uint64_t *tma_full = bars, *a_full = bars + kStages, *empty = bars + 2 * kStages;
-    uint64_t *acc_full = bars + 3 * kStages, *acc_empty = acc_full + 2;
+    uint64_t *tma_full = bars, *empty = bars + kStages;
+    uint64_t *a_full = bars + 2 * kStages, *a_empty = a_full + kNumA;   // tensor-memory A ring
+    uint64_t *acc_full = a_empty + kNumA, *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -317,8 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&tma_full[s]), 1);
-            mbar_init(smem_u32(&a_full[s]), kDeqWarps);
             mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int s = 0; s < kNumA; ++s) {
+            mbar_init(smem_u32(&a_full[s]), kDeqWarps);
+            mbar_init(smem_u32(&a_empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
@@ -374,31 +404,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, abuf = 0;
+            uint32_t phase = 0, aphase = 0;
             bool ok = true;
             int t = 0;
             for (int tile = QWQ_TILE_FIRST; tile < n_tiles_total && ok; tile += QWQ_TILE_STEP, ++t) {
                 const int ab = t & 1;
                 if (!mbar_wait(smem_u32(&acc_empty[ab]), ((t >> 1) & 1) ^ 1)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + ab * kAccStride;
+                const uint32_t d_tmem = tmem_base + kAccBase + ab * kAccStride;
                 for (int kb = QWQ_KB_FIRST; kb < QWQ_KB_END; ++kb) {
-                    if (!mbar_wait(smem_u32(&a_full[stage]), phase)) {
+                    // the dequantizers arrive on a_full only after the stage's
+                    // copies (codes and the x tile B) have landed
+                    if (!mbar_wait(smem_u32(&a_full[abuf]), aphase)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(a_s + stage * A_BYTES);
+                    const uint32_t a_tmem = tmem_base + abuf * 32;
                     const uint32_t b_addr = smem_u32(b_s + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        mma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), kIdesc,
-                                 (kb > QWQ_KB_FIRST || k > 0) ? 1u : 0u);
+                        mma_bf16_ts(d_tmem, a_tmem + 8 * k, sw128_desc(b_addr + 32 * k), kIdesc,
+                                    (kb > QWQ_KB_FIRST || k > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty[stage]));
+                    mma_commit(smem_u32(&a_empty[abuf]));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
+                    }
+                    if (++abuf == kNumA) {
+                        abuf = 0;
+                        aphase ^= 1;
                     }
                 }
                 if (ok) mma_commit(smem_u32(&acc_full[ab]));
@@ -406,11 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 2 && warp < 2 + kDeqWarps) {
         // ---------------- dequantizers: thread (r, half) owns half of row r
-        // of every A tile (16-byte output chunks 4 half .. 4 half + 3)
-        const int r = ((warp - 2) & 3) * 32 + lane;
+        // of every A tile (tensor-memory columns 16 half .. 16 half + 15 of an
+        // A buffer); a warp reaches only its own lane quarter (warp % 4), so
+        // that quarter's 32 rows are its rows
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
         const int half = (warp - 2) >> 2;
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, abuf = 0;
+        uint32_t phase = 0, aphase = 0;
         bool ok = true;
         // group-wise scales of the thread's 4 code words (int4) or 2 chunks
         // (int8) of k-block kb, loaded one k-block ahead
@@ -463,16 +503,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const uint8_t *crow = c_s + stage * C_BYTES + r * (C_BYTES / BM);
-                uint8_t *arow = a_s + stage * A_BYTES + r * 128;
-                const int sw = r & 7;
+                // the thread's 32 bf16 of the k-block (16 columns) in MMA K order
+                uint32_t cols[16];
                 if (FMT == B200Q_I4) {
                     const uint4 cw = *reinterpret_cast<const uint4 *>(crow + 16 * half);
                     const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int c = 4 * half + i;
-                        const uint4 e = deq_i4_word(wv[i]);
-                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = GS ? scale_word4(e, gsc[i]) : e;
+                        uint4 e = deq_i4_word(wv[i]);
+                        if (GS) e = scale_word4(e, gsc[i]);
+                        cols[4 * i] = e.x;
+                        cols[4 * i + 1] = e.y;
+                        cols[4 * i + 2] = e.z;
+                        cols[4 * i + 3] = e.w;
                     }
                 } else {
 #pragma unroll
@@ -486,16 +529,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                             e0 = scale_word4(e0, gsc[hh]);
                             e1 = scale_word4(e1, gsc[hh]);
                         }
-                        *reinterpret_cast<uint4 *>(arow + (((2 * h) ^ sw) << 4)) = e0;
-                        *reinterpret_cast<uint4 *>(arow + (((2 * h + 1) ^ sw) << 4)) = e1;
+                        cols[8 * hh] = e0.x;
+                        cols[8 * hh + 1] = e0.y;
+                        cols[8 * hh + 2] = e0.z;
+                        cols[8 * hh + 3] = e0.w;
+                        cols[8 * hh + 4] = e1.x;
+                        cols[8 * hh + 5] = e1.y;
+                        cols[8 * hh + 6] = e1.z;
+                        cols[8 * hh + 7] = e1.w;
                     }
                 }
-                fence_async_smem();
+                // the A buffer comes free when the MMAs that read it complete
+                if (!mbar_wait(smem_u32(&a_empty[abuf]), aphase ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st16(tmem_base + ((uint32_t)(quarter * 32) << 16) + abuf * 32 + half * 16, cols);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&a_full[stage]));
+                if (lane == 0) mbar_arrive(smem_u32(&a_full[abuf]));
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1;
+                }
+                if (++abuf == kNumA) {
+                    abuf = 0;
+                    aphase ^= 1;
                 }
             }
         }
@@ -511,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m0 = (tile / p.n_tiles) * BM, n0 = (tile % p.n_tiles) * BNT;
             const int o = m0 + quarter * 32 + lane;
             const float sc = o < p.O ? (GS ? 1.f : p.scales[o]) : 0.f;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kAccStride;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + kAccBase + ab * kAccStride;
             if constexpr (PIECES) {
                 float v[BNT];
 #pragma unroll
@@ -760,8 +821,8 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
     }
     constexpr int C_BYTES = BM * code_bytes;
     constexpr int kStages = stages_for<FMT, BNT, GSM>();
-    const size_t smem = 1024 + (size_t)kStages * (BM * BK * 2 + BNT * BK * 2 + C_BYTES + (GSM == 2 ? kScaleTile : 0)) +
-                        (3 * kStages + 4) * 8 + 16;
+    const size_t smem = 1024 + (size_t)kStages * (BNT * BK * 2 + C_BYTES + (GSM == 2 ? kScaleTile : 0)) +
+                        (2 * kStages + 2 * kNumA + 4) * 8 + 16;
     cudaError_t e = allow_dynamic_smem((const void *)qgemm_tc_kernel<FMT, BNT, PIECES, GSM>, (int)smem);
     if (e != cudaSuccess) return e;
     const int n_sms = sm_count(t.device);
