@@ -160,20 +160,27 @@ int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *s
  * int8 and int4 tensors only, TCS int8, int4 and int2 tensors with per-row
  * scales (B200Q_EINVAL otherwise).
  *
- * B200Q_PATH_TCS: each 128-row tile of codes is dequantized to exact fp16
- * integers straight into tensor memory (tcgen05.st) and multiplied there
- * (tcgen05.mma, A in tensor memory) against x split into two fp16 pieces per
- * token: x * 2^k with a power of two that brings the largest |x| among the
- * columns one CTA handles to [2^14, 2^15), p0 = fp16(x 2^k), p1 = fp16(x 2^k
- * - p0), which carry x to 2^-22 relative; products are exact in f32 and
- * accumulate in f32.  Bound: that of the f32 path, for tokens whose largest
- * |x| is up to ~3e5 times their typical |x| (beyond that the pieces of the
- * smallest elements fall below fp16's range, as the f32 path's outlier
- * limit).  At most 16 tokens per launch; the work is split evenly over the
- * SMs in (row tile, 128-byte k-block) items, and a tile shared by several
- * CTAs is added up, in CTA order and in common units, by the CTA holding its
- * last k-block.  Each call with shared tiles takes a workspace from the
- * library's pool.
+ * B200Q_PATH_TCS: an exact integer dot product on the fp8 tensor cores.
+ * A 4-bit field in the low bits of an E4M3 byte is worth field * 2^-9 for
+ * every field value 0..15, so each 128-row tile of codes is masked straight
+ * into fp8 bytes in tensor memory (tcgen05.st): int4 and int2 codes as they
+ * are, int8 codes (sign bit flipped) as a low and a high nibble.  x is
+ * rounded per token to a fixed-point integer n = rint(x 2^T), 2^T a power of
+ * two that brings the largest |x| among the columns one CTA handles to
+ * [2^(4J-2), 2^(4J-1)), J = 7 or 8, offset to a non-negative value and cut
+ * into J 4-bit digits, which are fp8 bytes the same way.  tcgen05.mma
+ * (kind::f8f6f4, A in tensor memory) then sums products of small integers,
+ * exactly in its f32 accumulator; the digits are recombined in 64-bit
+ * integers (with one extra row of ones for the offset, and the zero point
+ * taken out), and each output is rounded once.  The only error is the
+ * rounding of x to 26 (S even) or 30 (S odd) bits below its token's largest
+ * magnitude in the CTA's columns: for every output, |y - y_exact| <=
+ * |scale| * 2^-27 * max|x| * sum|deq| at J = 7.  At most 8 tokens per launch
+ * (more are chunked); the work is split evenly over the SMs in (row tile,
+ * 128-byte k-block) items, and a tile shared by several CTAs is added up in
+ * a fixed order by the CTA that brings its arrival count to its number of
+ * pieces.  Each call with shared tiles takes a workspace from the library's
+ * pool.
  */
 int b200q_matmul_ex(const b200q_tensor *t, const float *x, float *y, int S, int path,
                     void *stream);

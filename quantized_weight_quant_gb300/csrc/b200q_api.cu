@@ -192,7 +192,7 @@ int run_matmul(const Tensor &t, const Tensor *tu, const float *x, float *y, floa
                         who);
         if (t.gs || (tu && tu->gs))
             return fail(B200Q_EINVAL, "%s: the f32-accurate tensor-core path takes per-row scales only", who);
-        // at most 16 rows per launch; the pair's second tensor runs after the first
+        // 16 rows per call here (launch_tcs splits them further); the pair's second tensor runs after the first
         for (int k = 0; k < (tu ? 2 : 1) && e == cudaSuccess; ++k) {
             const Tensor &tt = k ? *tu : t;
             float *yy = k ? yu : y;
