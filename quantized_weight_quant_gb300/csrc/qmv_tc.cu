@@ -66,13 +66,12 @@ constexpr int kRowsT = 128;                    // rows per tile (M)
 constexpr int kKbBytes = 128;                  // code bytes per row per item
 constexpr int kCodeTile = kRowsT * kKbBytes;   // 16 KB
 constexpr int kMaxS = 8;                       // tokens per launch
-constexpr int kDeqWarps = 8, kEpiWarps = 4;
-constexpr int kWDeq = 2, kWEpi = kWDeq + kDeqWarps;
-constexpr int kThreads = (kWEpi + kEpiWarps) * 32;      // 448
-constexpr int kStagers = (kDeqWarps + kEpiWarps) * 32;  // warps 2-13 build B
+constexpr int kEpiWarps = 4;
+constexpr int kWDeq = 2;                       // first dequantizing warp
 constexpr int kSmemLimit = 232448;             // 227 KB
 constexpr int kSmemFloor = 120 * 1024;         // keeps one CTA per SM (tensor memory is taken whole)
-constexpr int kMiscBytes = 2048;               // barriers, exponents, maxima (plus 64 bytes per B slot)
+constexpr int kMiscBytes = 3072;               // barriers, exponents, maxima, counters, plane list (plus 72 bytes per B slot)
+constexpr int kMaxPlanes = 256;                // pieces of one tile, at most (the count is 8 bits)
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 __device__ unsigned int g_tcs_err = 0;
@@ -98,6 +97,19 @@ template <>
 struct Fmt<B200Q_I2> {
     static constexpr int KPE = 512, POS = 512, COLS = 128, NA = 3, Z = 2, UMAX = 3;
     static constexpr bool PAIR = false;
+};
+
+// Warp roles per format: warp 0 producer, warp 1 MMA issuer, then NA groups
+// of four dequantizing warps (one per tensor-memory lane quarter; group g
+// takes items g, g + NA, ... of the run into A buffer g), then four
+// epilogue warps.  The dequantizing and epilogue warps build B first.
+template <int FMT>
+struct Roles {
+    static constexpr int kDeq = 4 * Fmt<FMT>::NA;
+    static constexpr int kWEpi = kWDeq + kDeq;
+    static constexpr int kThreads = (kWEpi + kEpiWarps) * 32;
+    static constexpr int kStageWarps = kDeq + kEpiWarps;
+    static constexpr int kStagers = kStageWarps * 32;
 };
 
 // ---- PTX helpers (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05)
@@ -133,15 +145,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // Bounded wait on a phase parity.  Gives up after kWaitNs, or at once when
 // another role has already given up (*abort set); a wait that gives up first
-// records the timeout and raises the abort flag.  Waiters other than the MMA
-// issuer pass a nonzero sleep_ns so that polling warps leave issue slots to
-// the issuing thread.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int sleep_ns = 256) {
+// records the timeout and raises the abort flag.  try_wait itself suspends
+// the thread for a while when the phase is not complete, so polling costs
+// few issue slots and no sleep is added (a sleep delays the wake-up).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_test(bar, parity)) return true;
-        if (sleep_ns) __nanosleep(sleep_ns);
-        if ((it & 63) == 63) {
+        if ((it & 15) == 15) {
             if (*abort) return false;
             if (t0 == 0) t0 = global_ns();
             else if (global_ns() - t0 > kWaitNs) {
@@ -241,6 +252,36 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
+// Counters in shared memory that hand work between roles of the CTA: an
+// mbarrier test costs a few hundred cycles on this part even when the phase
+// is complete, a shared load far less.  Release on the add, acquire on the
+// read (PTX memory model, CTA scope).
+__device__ __forceinline__ void cnt_add(uint32_t addr) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ uint32_t cnt_read(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait for a shared counter to reach want (see cnt_add).
+__device__ __forceinline__ bool cnt_wait(uint32_t addr, uint32_t want, volatile int *abort) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if ((int)(cnt_read(addr) - want) >= 0) return true;
+        if ((it & 255) == 255) {
+            if (*abort) return false;
+            if (t0 == 0) t0 = global_ns();
+            else if (global_ns() - t0 > kWaitNs) {
+                atomicExch(&g_tcs_err, (unsigned)(-B200Q_ETIMEOUT));
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Named barrier that also ORs a predicate over its threads (a uniform decision).
 __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
     uint32_t r;
@@ -309,6 +350,34 @@ __device__ __forceinline__ Item item_of(const TcsParams &p, int i) {
     it.seg = r * p.tiles + it.t;
     return it;
 }
+
+// Walks the items in order without divisions (item_of once, at the start).
+struct Walk {
+    int i, r, t, kb, rlo, rend;   // k-blocks of range r: [rlo, rend)
+    __device__ __forceinline__ void init(const TcsParams &p, int i_) {
+        const Item it = item_of(p, i_);
+        i = i_;
+        r = it.r;
+        t = it.t;
+        kb = it.kb;
+        rlo = r * p.R;
+        rend = rlo + range_size(p, r);
+    }
+    __device__ __forceinline__ void next(const TcsParams &p) {
+        ++i;
+        if (++kb == rend) {
+            kb = rlo;
+            if (++t == p.tiles) {
+                t = 0;
+                ++r;
+                rlo = r * p.R;
+                rend = rlo + range_size(p, r);
+                kb = rlo;
+            }
+        }
+    }
+    __device__ __forceinline__ int seg(const TcsParams &p) const { return r * p.tiles + t; }
+};
 
 // First item of segment (r, t), and the CTA whose run holds item i (runs are
 // [b n / G, (b + 1) n / G)).
@@ -390,12 +459,14 @@ __device__ __forceinline__ uint32_t digit_word(const uint32_t (&t)[4], int j) {
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
     qmv_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const TcsParams p) {
     using F = Fmt<FMT>;
+    using RL = Roles<FMT>;
     constexpr int kMma = F::POS / 32;          // MMAs per item
     constexpr int kDStride = F::PAIR ? 128 : 64;
     constexpr int kDCol = F::NA * F::COLS;     // first accumulator column
+    constexpr int kWEpi = RL::kWEpi, kStageWarps = RL::kStageWarps, kStagers = RL::kStagers;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int DC = p.dc, N = p.N, S = p.S, J = p.J;
@@ -404,40 +475,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *b_s = code_s + (size_t)DC * kCodeTile;             // [nb][bslot]
     uint64_t *bars = reinterpret_cast<uint64_t *>(b_s + (size_t)p.nb * bslot);
     uint64_t *code_full = bars, *code_empty = bars + DC;
-    uint64_t *a_full = bars + 2 * DC, *a_empty = a_full + F::NA;
+    uint64_t *a_empty = bars + 2 * DC;                         // [NA] MMAs done with A buffer g
     uint64_t *d_full = a_empty + F::NA, *d_empty = d_full + 2;
-    uint64_t *b_ready = d_empty + 2, *mma_done = b_ready + 1;
+    uint64_t *mma_done = d_empty + 2;
     long long *nsum = reinterpret_cast<long long *>(mma_done + 1);   // [nb][kMaxS] sum of n per slot and token
     long long *npiece = nsum + (size_t)p.nb * kMaxS;                // [2][kMaxS] the same over a piece
     int *texp = reinterpret_cast<int *>(npiece + 2 * kMaxS);         // [kMaxS] shift T per token
-    float *red = reinterpret_cast<float *>(texp + kMaxS);             // [12][kMaxS] per-warp maxima
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red + 12 * kMaxS);
+    float *red = reinterpret_cast<float *>(texp + kMaxS);             // [kStageWarps][kMaxS] per-warp maxima
+    uint32_t *a_cnt = reinterpret_cast<uint32_t *>(red + kStageWarps * kMaxS);  // [NA] warps done filling buffer g
+    uint32_t *slot_cnt = a_cnt + F::NA;                               // [nb] units of slot k built
+    uint32_t *tmem_slot = slot_cnt + p.nb;
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort + 1;
+    int *plist = const_cast<int *>(last_flag + 1);                    // [kMaxPlanes + 1] planes of a tile to add
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i0 = run_first(p, blockIdx.x), i1 = run_first(p, blockIdx.x + 1);
+    const int n_items = i1 - i0;
     const Slots sl = slots_of(p, i0, i1);
     const int n_slots = sl.cnt0 + sl.cnt1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < DC; ++s) {
             mbar_init(smem_u32(&code_full[s]), 1);
-            mbar_init(smem_u32(&code_empty[s]), kDeqWarps);
+            mbar_init(smem_u32(&code_empty[s]), 4);
         }
         for (int s = 0; s < F::NA; ++s) {
-            mbar_init(smem_u32(&a_full[s]), kDeqWarps);
             mbar_init(smem_u32(&a_empty[s]), 1);
+            a_cnt[s] = 0;
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&d_full[s]), 1);
             mbar_init(smem_u32(&d_empty[s]), kEpiWarps);
         }
-        mbar_init(smem_u32(b_ready), 1);
         mbar_init(smem_u32(mma_done), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int k = threadIdx.x; k < p.nb; k += blockDim.x) slot_cnt[k] = 0;
     if (warp == 0)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_codes)) : "memory");
     if (warp == 1) {
@@ -458,12 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int st = 0;
             uint32_t ph = 0;
             long long issued = 0;
-            for (int i = i0; i < i1; ++i) {
+            Walk w;
+            w.init(p, i0);
+            for (int i = i0; i < i1; ++i, w.next(p)) {
                 if (!mbar_wait(smem_u32(&code_empty[st]), ph ^ 1, abort)) break;
-                const Item it = item_of(p, i);
                 const uint32_t bar = smem_u32(&code_full[st]);
                 mbar_expect_tx(bar, kCodeTile);
-                tma_load_2d(smem_u32(code_s + (size_t)st * kCodeTile), &map_codes, it.kb * kKbBytes, it.t * kRowsT,
+                tma_load_2d(smem_u32(code_s + (size_t)st * kCodeTile), &map_codes, w.kb * kKbBytes, w.t * kRowsT,
                             bar, policy);
                 ++issued;
                 if (++st == DC) {
@@ -479,27 +555,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_e4m3(N);
-            int ab = 0, db = 0;
-            uint32_t aph = 0, dph = 0;
-            bool ok = mbar_wait(smem_u32(b_ready), 0, abort, 0);
+            int g = 0, db = 0;
+            uint32_t fill = 0, dph = 0;          // fills of buffer g so far (per round of groups)
+            unsigned long long ready = 0;        // B slots known to be built
             const uint64_t bdesc0 = sw128_desc(smem_u32(b_s));
             bool issued_any = false;
-            Item it = item_of(p, i0);
-            int prev_seg = -1;
-            for (int i = i0; i < i1 && ok; ++i) {
-                const Item nx = i + 1 < i1 ? item_of(p, i + 1) : it;
-                const bool first = it.seg != prev_seg;
-                const bool last = i == i1 - 1 || nx.seg != it.seg;
-                prev_seg = it.seg;
+            Walk w;
+            w.init(p, i0);
+            for (int i = i0; i < i1; ++i, w.next(p)) {
+                const bool first = i == i0 || w.kb == w.rlo;
+                const bool last = i == i1 - 1 || w.kb + 1 == w.rend;
                 if (first) {
-                    if (!mbar_wait(smem_u32(&d_empty[db]), dph ^ 1, abort, 0)) break;
-                    tc_fence_after();
+                    if (!mbar_wait(smem_u32(&d_empty[db]), dph ^ 1, abort)) break;
                 }
-                if (!mbar_wait(smem_u32(&a_full[ab]), aph, abort, 0)) break;
+                const int slot = slot_of(p, sl, w.kb);
+                if (!((ready >> slot) & 1)) {
+                    if (!cnt_wait(smem_u32(&slot_cnt[slot]), (uint32_t)S, abort)) break;
+                    ready |= 1ull << slot;
+                }
+                if (!cnt_wait(smem_u32(&a_cnt[g]), 4u * (fill + 1), abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + kDCol + db * kDStride;
-                const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)slot_of(p, sl, it.kb) * bslot) >> 4);
-                const uint32_t at = tmem_base + ab * F::COLS;
+                const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)slot * bslot) >> 4);
+                const uint32_t at = tmem_base + g * F::COLS;
 #pragma unroll
                 for (int m = 0; m < kMma; ++m) {
                     const bool hi = F::PAIR && m >= kMma / 2;
@@ -508,10 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            bd + (uint64_t)((uint32_t)((m >> 2) * N * 128 + (m & 3) * 32) >> 4), idesc, acc);
                 }
                 issued_any = true;
-                mma_commit(smem_u32(&a_empty[ab]));
-                if (++ab == F::NA) {
-                    ab = 0;
-                    aph ^= 1;
+                mma_commit(smem_u32(&a_empty[g]));
+                if (++g == F::NA) {
+                    g = 0;
+                    ++fill;
                 }
                 if (last) {
                     mma_commit(smem_u32(&d_full[db]));
@@ -520,7 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dph ^= 1;
                     }
                 }
-                it = nx;
             }
             // every MMA issued has completed before tensor memory is freed
             if (issued_any) {
@@ -529,126 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- warps 2-13: build B, then dequantize / drain
-        const int sw = warp - kWDeq;                 // 0..11
-        const int stid = sw * 32 + lane;             // 0..383
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        const bool vec = (p.I & 3) == 0 && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0;
-        auto ld4 = [&](const float *r, int k0) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (vec) {
-                if (k0 < p.I) v = *reinterpret_cast<const float4 *>(r + k0);
-            } else {
-                v.x = k0 < p.I ? r[k0] : 0.f;
-                v.y = k0 + 1 < p.I ? r[k0 + 1] : 0.f;
-                v.z = k0 + 2 < p.I ? r[k0 + 2] : 0.f;
-                v.w = k0 + 3 < p.I ? r[k0 + 3] : 0.f;
-            }
-            return v;
-        };
-        // (1) largest |x| per token over the staged k-blocks
+        // ---------------- dequantizing and epilogue warps: build B, then their loops
+        const int sw = warp - kWDeq;                  // 0 .. kStageWarps - 1
+        const int stid = sw * 32 + lane;
+        // the row of ones (each byte 0x01: 2^-9) and the unused rows (zero)
+        // do not depend on x: written before the dependency wait
         {
-            const int n4 = n_slots * (F::KPE / 4);   // float4 groups per token
-            for (int s = 0; s < S; ++s) {
-                const float *xr = p.x + (long long)s * p.I;
-                float m = 0.f;
-                for (int g = stid; g < n4; g += kStagers) {
-                    const int slot = g / (F::KPE / 4);
-                    const int k0 = kb_of_slot(p, sl, slot) * F::KPE + (g - slot * (F::KPE / 4)) * 4;
-                    const float4 v = ld4(xr, k0);
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                if (lane == 0) red[sw * kMaxS + s] = m;
-            }
-            named_sync(1, kStagers);
-            if (stid < S) {
-                float m = 0.f;
-                for (int w = 0; w < 12; ++w) m = fmaxf(m, red[w * kMaxS + stid]);
-                // T brings the largest |x| to [2^(4J-2), 2^(4J-1)); zero tokens keep T = 0
-                texp[stid] = m > 0.f ? 4 * J - 2 - ilog2_bits(m) : 0;
-            }
-            named_sync(1, kStagers);
-        }
-        // (2) digits: one warp per (slot, token); lane q takes 8 (int4),
-        // 4 (int8) or 16 (int2) consecutive x and writes their J digit rows
-        {
-            const uint32_t off_n = 1u << (4 * J - 1);
-            for (int u = sw; u < n_slots * S; u += 12) {
-                const int slot = u / S, s = u - slot * S;
-                const int kb = kb_of_slot(p, sl, slot);
-                const float2 f = pow2_pair(texp[s]);
-                const float *xr = p.x + (long long)s * p.I + (long long)kb * F::KPE;
-                const int kleft = p.I - kb * F::KPE;          // x beyond I reads as zero
-                uint8_t *bs = b_s + (size_t)slot * bslot;
-                long long nsm = 0;
-                auto conv = [&](float v) {
-                    const int n = __float2int_rn((v * f.x) * f.y);
-                    nsm += n;
-                    return (uint32_t)n + off_n;
-                };
-                auto ldk = [&](int k0) {   // x[k0..k0+3] of this k-block, zero past I
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (vec) {
-                        if (k0 < kleft) v = *reinterpret_cast<const float4 *>(xr + k0);
-                    } else {
-                        v.x = k0 < kleft ? xr[k0] : 0.f;
-                        v.y = k0 + 1 < kleft ? xr[k0 + 1] : 0.f;
-                        v.z = k0 + 2 < kleft ? xr[k0 + 2] : 0.f;
-                        v.w = k0 + 3 < kleft ? xr[k0 + 3] : 0.f;
-                    }
-                    return v;
-                };
-                if (FMT == B200Q_I4) {
-                    // positions 8q + i <- k = 8q + 2i, positions 8q + 4 + i <- k = 8q + 2i + 1
-                    const float4 a = ldk(8 * lane), b = ldk(8 * lane + 4);
-                    uint32_t te[4], to[4];
-                    bytes_t4(conv(a.x), conv(a.z), conv(b.x), conv(b.z), te);
-                    bytes_t4(conv(a.y), conv(a.w), conv(b.y), conv(b.w), to);
-                    #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j >= J) break;
-                        const int row = s * J + j;
-                        *reinterpret_cast<uint2 *>(bs + b_off(row, 8 * lane, N)) =
-                            make_uint2(digit_word(te, j), digit_word(to, j));
-                    }
-                } else if (FMT == B200Q_I8) {
-                    // positions 4q + i (low nibbles) and 128 + 4q + i (high) <- k = 4q + i
-                    const float4 a = ldk(4 * lane);
-                    uint32_t t4[4];
-                    bytes_t4(conv(a.x), conv(a.y), conv(a.z), conv(a.w), t4);
-                    #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j >= J) break;
-                        const int row = s * J + j;
-                        const uint32_t w = digit_word(t4, j);
-                        *reinterpret_cast<uint32_t *>(bs + b_off(row, 4 * lane, N)) = w;
-                        *reinterpret_cast<uint32_t *>(bs + b_off(row, 128 + 4 * lane, N)) = w;
-                    }
-                } else {
-                    // positions 16q + 4i + e <- k = 16q + 4e + i
-                    const float4 a = ldk(16 * lane), b = ldk(16 * lane + 4), c = ldk(16 * lane + 8),
-                                 d = ldk(16 * lane + 12);
-                    uint32_t t0[4], t1[4], t2[4], t3[4];
-                    bytes_t4(conv(a.x), conv(b.x), conv(c.x), conv(d.x), t0);
-                    bytes_t4(conv(a.y), conv(b.y), conv(c.y), conv(d.y), t1);
-                    bytes_t4(conv(a.z), conv(b.z), conv(c.z), conv(d.z), t2);
-                    bytes_t4(conv(a.w), conv(b.w), conv(c.w), conv(d.w), t3);
-                    #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j >= J) break;
-                        const int row = s * J + j;
-                        *reinterpret_cast<uint4 *>(bs + b_off(row, 16 * lane, N)) =
-                            make_uint4(digit_word(t0, j), digit_word(t1, j), digit_word(t2, j), digit_word(t3, j));
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) nsm += __shfl_xor_sync(0xffffffffu, nsm, o);
-                if (lane == 0) nsum[slot * kMaxS + s] = nsm;
-            }
-            // the row of ones (each byte 0x01: 2^-9) and the unused rows (zero)
             const int ones = S * J;
             const int rows_left = N - ones;
             const int chunks = n_slots * rows_left * (F::POS / 16);
@@ -660,78 +623,220 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(b_s + (size_t)slot * bslot + b_off(row, ch * 16, N)) = make_uint4(v, v, v, v);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            named_sync(1, kStagers);
-            if (stid == 0) mbar_arrive(smem_u32(b_ready));
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        const bool vec = (p.I & 3) == 0 && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0;
+        // Units of B work: (slot, token) pairs, unit u = slot * S + s, warp
+        // sw takes units sw, sw + kStageWarps, ...; lane q of a unit holds V
+        // float4 of x: 8 (int4), 4 (int8) or 16 (int2) consecutive elements of
+        // its k-block.  When every warp has at most kHold units, x is loaded
+        // once and kept in registers across the exponent barrier; otherwise a
+        // max-only pass runs first and the digit pass loads again.  Loads of
+        // a batch all go out before any is used.  Units go in slot order, and
+        // each unit's slot counter is raised as soon as its rows are written,
+        // so the MMAs can start on the first slot while the rest are built.
+        constexpr int V = F::KPE / 128;
+        constexpr int kHold = 2;
+        const int units = n_slots * S;
+        const bool hold = (units + kStageWarps - 1) / kStageWarps <= kHold;
+        auto load_unit = [&](int u, float4 (&v)[V]) {
+            const int slot = u / S, s = u - slot * S;
+            const int kb = kb_of_slot(p, sl, slot);
+            const float *xr = p.x + (long long)s * p.I + (long long)kb * F::KPE;
+            const int kleft = p.I - kb * F::KPE;      // x beyond I reads as zero
+#pragma unroll
+            for (int h = 0; h < V; ++h) {
+                const int k0 = (lane * V + h) * 4;
+                float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (vec) {
+                    if (k0 < kleft) t = *reinterpret_cast<const float4 *>(xr + k0);
+                } else {
+                    t.x = k0 < kleft ? xr[k0] : 0.f;
+                    t.y = k0 + 1 < kleft ? xr[k0 + 1] : 0.f;
+                    t.z = k0 + 2 < kleft ? xr[k0 + 2] : 0.f;
+                    t.w = k0 + 3 < kleft ? xr[k0 + 3] : 0.f;
+                }
+                v[h] = t;
+            }
+        };
+        float4 xv[kHold][V];
+        float m[kMaxS];
+#pragma unroll
+        for (int t = 0; t < kMaxS; ++t) m[t] = 0.f;
+        auto note = [&](int u, const float4 (&v)[V]) {
+            const int s = u % S;
+            float a = 0.f;
+#pragma unroll
+            for (int h = 0; h < V; ++h) a = fmaxf(a, fmaxf(fmaxf(fabsf(v[h].x), fabsf(v[h].y)), fmaxf(fabsf(v[h].z), fabsf(v[h].w))));
+#pragma unroll
+            for (int t = 0; t < kMaxS; ++t)
+                if (t == s) m[t] = fmaxf(m[t], a);
+        };
+        // (1) largest |x| per token over the staged k-blocks
+        for (int u0 = sw; u0 < units; u0 += kStageWarps * kHold) {
+#pragma unroll
+            for (int k = 0; k < kHold; ++k)
+                if (u0 + kStageWarps * k < units) load_unit(u0 + kStageWarps * k, xv[k]);
+#pragma unroll
+            for (int k = 0; k < kHold; ++k)
+                if (u0 + kStageWarps * k < units) note(u0 + kStageWarps * k, xv[k]);
+            if (hold) break;
+        }
+#pragma unroll
+        for (int t = 0; t < kMaxS; ++t) {
+            if (t >= S) break;
+            float a = m[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            if (lane == 0) red[sw * kMaxS + t] = a;
+        }
+        named_sync(1, kStagers);
+        if (stid < S) {
+            float a = 0.f;
+            for (int w = 0; w < kStageWarps; ++w) a = fmaxf(a, red[w * kMaxS + stid]);
+            // T brings the largest |x| to [2^(4J-2), 2^(4J-1)); zero tokens keep T = 0
+            texp[stid] = a > 0.f ? 4 * J - 2 - ilog2_bits(a) : 0;
+        }
+        named_sync(1, kStagers);
+        // (2) digits of each unit's x into its B rows
+        {
+            const uint32_t off_n = 1u << (4 * J - 1);
+            auto convert = [&](int u, const float4 (&v)[V]) {
+                const int slot = u / S, s = u - slot * S;
+                const float2 f = pow2_pair(texp[s]);
+                uint8_t *bs = b_s + (size_t)slot * bslot;
+                long long nsm = 0;
+                auto conv = [&](float x) {
+                    const int n = __float2int_rn((x * f.x) * f.y);
+                    nsm += n;
+                    return (uint32_t)n + off_n;
+                };
+                if (FMT == B200Q_I4) {
+                    // positions 8q + i <- k = 8q + 2i, positions 8q + 4 + i <- k = 8q + 2i + 1
+                    uint32_t te[4], to[4];
+                    bytes_t4(conv(v[0].x), conv(v[0].z), conv(v[1].x), conv(v[1].z), te);
+                    bytes_t4(conv(v[0].y), conv(v[0].w), conv(v[1].y), conv(v[1].w), to);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j >= J) break;
+                        *reinterpret_cast<uint2 *>(bs + b_off(s * J + j, 8 * lane, N)) =
+                            make_uint2(digit_word(te, j), digit_word(to, j));
+                    }
+                } else if (FMT == B200Q_I8) {
+                    // positions 4q + i (low nibbles) and 128 + 4q + i (high) <- k = 4q + i
+                    uint32_t t4[4];
+                    bytes_t4(conv(v[0].x), conv(v[0].y), conv(v[0].z), conv(v[0].w), t4);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j >= J) break;
+                        const uint32_t w = digit_word(t4, j);
+                        *reinterpret_cast<uint32_t *>(bs + b_off(s * J + j, 4 * lane, N)) = w;
+                        *reinterpret_cast<uint32_t *>(bs + b_off(s * J + j, 128 + 4 * lane, N)) = w;
+                    }
+                } else {
+                    // positions 16q + 4i + e <- k = 16q + 4e + i
+                    uint32_t t0[4], t1[4], t2[4], t3[4];
+                    bytes_t4(conv(v[0].x), conv(v[1].x), conv(v[2].x), conv(v[3].x), t0);
+                    bytes_t4(conv(v[0].y), conv(v[1].y), conv(v[2].y), conv(v[3].y), t1);
+                    bytes_t4(conv(v[0].z), conv(v[1].z), conv(v[2].z), conv(v[3].z), t2);
+                    bytes_t4(conv(v[0].w), conv(v[1].w), conv(v[2].w), conv(v[3].w), t3);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j >= J) break;
+                        *reinterpret_cast<uint4 *>(bs + b_off(s * J + j, 16 * lane, N)) =
+                            make_uint4(digit_word(t0, j), digit_word(t1, j), digit_word(t2, j), digit_word(t3, j));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) nsm += __shfl_xor_sync(0xffffffffu, nsm, o);
+                // every lane's rows visible to the tensor cores before the count
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    nsum[slot * kMaxS + s] = nsm;
+                    cnt_add(smem_u32(&slot_cnt[slot]));
+                }
+            };
+            for (int u0 = sw; u0 < units; u0 += kStageWarps * kHold) {
+                if (!hold) {
+#pragma unroll
+                    for (int k = 0; k < kHold; ++k)
+                        if (u0 + kStageWarps * k < units) load_unit(u0 + kStageWarps * k, xv[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < kHold; ++k)
+                    if (u0 + kStageWarps * k < units) convert(u0 + kStageWarps * k, xv[k]);
+            }
         }
 
         if (warp < kWEpi) {
-            // ---------------- dequantizers: row r of the tile, half a k-block each
-            const int quarter = warp & 3, half = (warp - kWDeq) >> 2;
+            // ---------------- dequantizers: group grp fills A buffer grp with
+            // items grp, grp + NA, ... of the run; lane = row of the tile
+            const int grp = (warp - kWDeq) >> 2, quarter = warp & 3;
             const int r = quarter * 32 + lane;
-            const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
-            int st = 0, ab = 0;
-            uint32_t ph = 0, aph = 0;
-            for (int i = i0; i < i1; ++i) {
-                if (!mbar_wait(smem_u32(&code_full[st]), ph, abort)) break;
-                // this half's 64 code bytes of row r: four 16-byte chunks, swizzled
+            const uint32_t abase = tmem_base + ((uint32_t)(quarter * 32) << 16) + grp * F::COLS;
+            uint32_t fill = 0;
+            for (int k = grp; k < n_items; k += F::NA, ++fill) {
+                const int st = k % DC;
+                if (!mbar_wait(smem_u32(&code_full[st]), (uint32_t)((k / DC) & 1), abort)) break;
+                // row r's 128 code bytes: eight 16-byte chunks, swizzled; read
+                // in two halves of 16 words, the stage released after the second
                 const uint8_t *row = code_s + (size_t)st * kCodeTile + r * 128;
-                uint4 c[4];
+                uint32_t w[16], v[32];
+                auto load_half = [&](int h) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    c[k] = *reinterpret_cast<const uint4 *>(row + (((half * 4 + k) ^ (r & 7)) << 4));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&code_empty[st]));
-                if (++st == DC) {
-                    st = 0;
-                    ph ^= 1;
-                }
-                const uint32_t w[16] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w,
-                                        c[2].x, c[2].y, c[2].z, c[2].w, c[3].x, c[3].y, c[3].z, c[3].w};
-                if (!mbar_wait(smem_u32(&a_empty[ab]), aph ^ 1, abort)) break;
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 t = *reinterpret_cast<const uint4 *>(row + (((4 * h + c) ^ (r & 7)) << 4));
+                        w[4 * c] = t.x;
+                        w[4 * c + 1] = t.y;
+                        w[4 * c + 2] = t.z;
+                        w[4 * c + 3] = t.w;
+                    }
+                };
+                load_half(0);
+                if (!mbar_wait(smem_u32(&a_empty[grp]), (fill & 1) ^ 1, abort)) break;
                 tc_fence_after();
-                const uint32_t abase = lane_base + ab * F::COLS;
-                if (FMT == B200Q_I4) {
-                    // word q -> columns 2q (even codes) and 2q + 1 (odd codes)
-                    uint32_t v[32];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        v[2 * q] = w[q] & 0x0F0F0F0Fu;
-                        v[2 * q + 1] = (w[q] >> 4) & 0x0F0F0F0Fu;
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1) {
+                        load_half(1);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&code_empty[st]));
                     }
-                    tmem_st32(abase + half * 32, v);
-                } else if (FMT == B200Q_I8) {
-                    // code + 128 = 16 hi + lo: low nibbles to columns q, high to 32 + q
-                    uint32_t lo[16], hi[16];
+                    if (FMT == B200Q_I4) {
+                        // word q -> columns 2q (even codes) and 2q + 1 (odd codes)
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const uint32_t u = w[q] ^ 0x80808080u;
-                        lo[q] = u & 0x0F0F0F0Fu;
-                        hi[q] = (u >> 4) & 0x0F0F0F0Fu;
+                        for (int q = 0; q < 16; ++q) {
+                            v[2 * q] = w[q] & 0x0F0F0F0Fu;
+                            v[2 * q + 1] = (w[q] >> 4) & 0x0F0F0F0Fu;
+                        }
+                        tmem_st32(abase + h * 32, v);
+                    } else if (FMT == B200Q_I8) {
+                        // code + 128 = 16 hi + lo: low nibbles to columns q, high to 32 + q
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            v[q] = (w[q] ^ 0x80808080u) & 0x0F0F0F0Fu;
+                            v[16 + q] = ((w[q] ^ 0x80808080u) >> 4) & 0x0F0F0F0Fu;
+                        }
+                        tmem_st16(abase + h * 16, v);
+                        tmem_st16(abase + 32 + h * 16, v + 16);
+                    } else {
+                        // word q -> columns 4q + i: fields i, i + 4, i + 8, i + 12
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) v[4 * q + i] = (w[8 * e + q] >> (2 * i)) & 0x03030303u;
+                            tmem_st32(abase + h * 64 + e * 32, v);
+                        }
                     }
-                    tmem_st16(abase + half * 16, lo);
-                    tmem_st16(abase + 32 + half * 16, hi);
-                } else {
-                    // word q -> columns 4q + i: fields i, i + 4, i + 8, i + 12
-                    uint32_t v[32];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) v[4 * q + i] = (w[q] >> (2 * i)) & 0x03030303u;
-                    tmem_st32(abase + half * 64, v);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) v[4 * q + i] = (w[8 + q] >> (2 * i)) & 0x03030303u;
-                    tmem_st32(abase + half * 64 + 32, v);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&a_full[ab]));
-                if (++ab == F::NA) {
-                    ab = 0;
-                    aph ^= 1;
-                }
+                if (lane == 0) cnt_add(smem_u32(&a_cnt[grp]));
             }
         } else {
             // ---------------- epilogue: one row per thread, one piece at a time
@@ -742,21 +847,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long off_n = 1ll << (4 * J - 1);
             int db = 0, pc = 0;
             uint32_t dph = 0;
-            int i = i0;
-            const int seg_base = item_of(p, i0).seg;
-            while (i < i1) {
-                const Item it = item_of(p, i);
-                int iend = i + 1;
-                while (iend < i1 && item_of(p, iend).seg == it.seg) ++iend;
-                const Item il = item_of(p, iend - 1);     // the piece covers k-blocks [it.kb, il.kb]
+            Walk w;
+            w.init(p, i0);
+            const int seg_base = w.seg(p);
+            while (w.i < i1) {
+                // the piece: k-blocks [kb0, kb0 + len) of segment (w.r, w.t)
+                const int kb0 = w.kb, pr = w.r, t = w.t, seg = w.seg(p);
+                const int len = w.rend - w.kb < i1 - w.i ? w.rend - w.kb : i1 - w.i;
                 // sum of n over the piece's k-blocks, per token
                 long long *np = npiece + (pc & 1) * kMaxS;
+                bool ok = true;
                 if (etid < S) {
                     long long a = 0;
-                    for (int kb = it.kb; kb <= il.kb; ++kb) a += nsum[slot_of(p, sl, kb) * kMaxS + etid];
+                    for (int kb = kb0; kb < kb0 + len && ok; ++kb) {
+                        const int slot = slot_of(p, sl, kb);
+                        ok = cnt_wait(smem_u32(&slot_cnt[slot]), (uint32_t)S, abort);   // its nsum is written
+                        a += nsum[slot * kMaxS + etid];
+                    }
                     np[etid] = a;
                 }
-                const bool ok = mbar_wait(smem_u32(&d_full[db]), dph, abort);
+                ok = mbar_wait(smem_u32(&d_full[db]), dph, abort) && ok;
                 if (named_sync_or(2, kEpiWarps * 32, !ok)) break;     // np is visible too
                 tc_fence_after();
                 const uint32_t dt = lane_base + kDCol + db * kDStride;
@@ -801,26 +911,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     db = 0;
                     dph ^= 1;
                 }
-                const int t = it.t;
                 const int o = t * kRowsT + r;
                 const double sc = (double)p.scales[o];
                 // whole tile in this piece: one range, and no other CTA in the segment
-                const int sf = seg_first(p, it.r, t);
-                const bool whole = p.nr == 1 && cta_of(p, sf) == cta_of(p, sf + range_size(p, it.r) - 1);
+                const int sf = seg_first(p, pr, t);
+                const bool whole = p.nr == 1 && cta_of(p, sf) == cta_of(p, sf + range_size(p, pr) - 1);
                 if (whole) {
                     if (o < p.O)
                         #pragma unroll
                         for (int s = 0; s < kMaxS; ++s)
                             if (s < S) p.y[(long long)s * p.O + o] = (float)(sc * val[s]);
                 } else {
-                    const int lp = it.seg - seg_base;
+                    const int lp = seg - seg_base;
                     double *pl = p.plane + ((size_t)blockIdx.x * p.pmax + lp) * S * kRowsT;
                     #pragma unroll
                     for (int s = 0; s < kMaxS; ++s)
                         if (s < S) pl[s * kRowsT + r] = val[s];
-                    __threadfence();
+                    // the barrier orders every thread's plane before thread 0's
+                    // fence (cumulative), which orders them before the count
                     named_sync(2, kEpiWarps * 32);
                     if (etid == 0) {
+                        __threadfence();
                         // pieces of tile t: its segments' CTAs, range by range
                         int expect = 0;
                         for (int rr = 0; rr < p.nr; ++rr) {
@@ -836,25 +947,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                             old = prev;
                             nv = 0;
                         }
-                        *last_flag = nv != 0 && (int)(nv & 0xFF) == expect;
-                        __threadfence();
+                        const bool last = nv != 0 && (int)(nv & 0xFF) == expect;
+                        if (last) {
+                            __threadfence();
+                            // the tile's planes in (range, CTA) order
+                            int n = 0;
+                            for (int rr = 0; rr < p.nr; ++rr) {
+                                const int f0 = seg_first(p, rr, t);
+                                const int c0 = cta_of(p, f0), c1 = cta_of(p, f0 + range_size(p, rr) - 1);
+                                for (int c = c0; c <= c1 && n < kMaxPlanes; ++c)
+                                    plist[1 + n++] = c * p.pmax + rr * p.tiles + t - item_of(p, run_first(p, c)).seg;
+                            }
+                            plist[0] = n;
+                        }
+                        *last_flag = last;
                     }
                     named_sync(2, kEpiWarps * 32);
                     if (*last_flag) {
-                        __threadfence();
+                        // loads of two planes go out together
                         double sum[kMaxS];
 #pragma unroll
                         for (int s = 0; s < kMaxS; ++s) sum[s] = 0.0;
-                        for (int rr = 0; rr < p.nr; ++rr) {
-                            const int f0 = seg_first(p, rr, t);
-                            const int c0 = cta_of(p, f0), c1 = cta_of(p, f0 + range_size(p, rr) - 1);
-                            for (int c = c0; c <= c1; ++c) {
-                                const int lpc = rr * p.tiles + t - item_of(p, run_first(p, c)).seg;
-                                const double *q = p.plane + ((size_t)c * p.pmax + lpc) * S * kRowsT;
-                                #pragma unroll
-                                for (int s = 0; s < kMaxS; ++s)
-                                    if (s < S) sum[s] += __ldcg(q + s * kRowsT + r);
+                        const int npl = plist[0];
+                        for (int k0 = 0; k0 < npl; k0 += 2) {
+                            double v[2][kMaxS];
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const double *q = p.plane + (size_t)plist[1 + (k0 + k < npl ? k0 + k : 0)] * S * kRowsT + r;
+#pragma unroll
+                                for (int s = 0; s < kMaxS; ++s) v[k][s] = k0 + k < npl && s < S ? __ldcg(q + s * kRowsT) : 0.0;
                             }
+#pragma unroll
+                            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                                for (int s = 0; s < kMaxS; ++s) sum[s] += v[k][s];
                         }
                         if (o < p.O)
                             #pragma unroll
@@ -864,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_sync(2, kEpiWarps * 32);
                 }
                 ++pc;
-                i = iend;
+                for (int k = 0; k < len; ++k) w.next(p);
             }
         }
     }
@@ -931,7 +1057,7 @@ bool make_plan(const Tensor &t, int S, int n_sms, Plan &pl) {
             const long long pc = seg_of(i1 - 1) - seg_of(i0) + 1;
             if (pc > pmax) pmax = (int)pc;
         }
-        if (!ok || (long long)need * (bslot + 64) + 4ll * kCodeTile > budget) continue;
+        if (!ok || need > 64 || (long long)need * (bslot + 72) + 4ll * kCodeTile > budget) continue;
         // arrival counts fit 8 bits
         int maxc = 0;
         for (int tt = 0; tt < tiles && nr > 1; ++tt) {
@@ -948,12 +1074,12 @@ bool make_plan(const Tensor &t, int S, int n_sms, Plan &pl) {
         pl.nr = nr;
         pl.nb = need;
         pl.pmax = pmax;
-        int dc = (int)((budget - (long long)need * (bslot + 64)) / kCodeTile);
+        int dc = (int)((budget - (long long)need * (bslot + 72)) / kCodeTile);
         pl.dc = dc > 16 ? 16 : dc;
         bool shared = nr > 1;
         for (int b = 1; b < G && !shared; ++b) shared = ((long long)b * n / G) % nkb != 0;
         pl.shared = shared;
-        size_t smem = 1024 + (size_t)pl.dc * kCodeTile + (size_t)need * (bslot + 64) + kMiscBytes;
+        size_t smem = 1024 + (size_t)pl.dc * kCodeTile + (size_t)need * (bslot + 72) + kMiscBytes;
         pl.smem = smem < (size_t)kSmemFloor ? (size_t)kSmemFloor : smem;
         return true;
     }
@@ -998,7 +1124,7 @@ cudaError_t launch_fmt(const Tensor &t, const float *x, float *y, int S, cudaStr
     if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(pl.G);
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(Roles<FMT>::kThreads);
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
