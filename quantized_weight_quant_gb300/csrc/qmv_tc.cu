@@ -36,20 +36,26 @@
 // k-blocks (whose B tiles it builds once, in shared memory) fit; it is the
 // whole row when they do.  A CTA accumulates each (range, tile) run of its
 // items in one tensor-memory accumulator.  A tile that one CTA covers whole
-// goes straight to y; otherwise each piece is written as an f64 plane and
-// the CTA that brings a tile's arrival count (an atomic per tile, tagged with
-// the call's token) to its number of pieces adds the planes in a fixed order
-// and writes y.  Nothing waits on another CTA.
-// Warp roles (14 warps): warp 0 issues the TMA copies of the code tiles (128
-// rows x 128 bytes, 128-byte swizzle) into a ring, from the start, since the
+// goes straight to y.  Otherwise, with one range, the CTA holding the tile's
+// first item (the tile is the last piece of its run) adds the other CTAs'
+// f64 planes, in CTA order, once their flags (tagged with the call's token)
+// are set; with several ranges, the CTA that brings the tile's arrival count
+// (an atomic tagged with the token) to its number of pieces adds them.
+// Warp roles: warp 0 issues the TMA copies of the code tiles (128 rows x
+// 128 bytes, 128-byte swizzle) into a ring, from the start, since the
 // weights are read-only; warp 1 allocates tensor memory and issues the MMAs;
-// warps 2-9 dequantize (two per tensor-memory lane quarter, half a row's
-// k-block each) into tensor memory; warps 10-13 drain the accumulators.
-// Before their loops warps 2-13 build the B tiles (after the dependency
-// wait).  Every mbarrier wait is bounded; a CTA that gives up records
-// B200Q_ETIMEOUT (b200q_device_status) and winds down: an abort flag in
-// shared memory releases the other roles' waits, the producer's copies in
-// flight land, the MMAs issued complete, and tensor memory is freed.
+// NA groups of four warps dequantize (group g takes every NA-th item into A
+// buffer g, one tensor-memory lane quarter per warp); four warps drain the
+// accumulators.  The dequantizing and draining warps first build the B
+// tiles (after the dependency wait), slot by slot, and the MMAs start as
+// soon as the slot they need is built.  Hand-offs inside the CTA that no
+// tensor-core commit is involved in go through shared-memory counters
+// (release add, acquire load): an mbarrier test costs a few hundred cycles
+// on this part even when its phase is complete.  Every wait is bounded; a
+// CTA that gives up records B200Q_ETIMEOUT (b200q_device_status) and winds
+// down: an abort flag in shared memory releases the other roles' waits, the
+// producer's copies in flight land, the MMAs issued complete, and tensor
+// memory is freed.
 #include <cuda.h>
 
 #include <atomic>
@@ -152,6 +158,59 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_test(bar, parity)) return true;
+        if ((it & 15) == 15) {
+            if (*abort) return false;
+            if (t0 == 0) t0 = global_ns();
+            else if (global_ns() - t0 > kWaitNs) {
+                atomicExch(&g_tcs_err, (unsigned)(-B200Q_ETIMEOUT));
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Two adjacent counters read at once (8-byte aligned pair): waits for the
+// first to reach want and reports whether the second has too.
+__device__ __forceinline__ bool cnt_wait2(uint32_t addr, uint32_t want, volatile int *abort, bool &second) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        unsigned long long v;
+        asm volatile("ld.acquire.cta.shared::cta.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+        if ((int)((uint32_t)v - want) >= 0) {
+            second = (int)((uint32_t)(v >> 32) - want) >= 0;
+            return true;
+        }
+        if ((it & 255) == 255) {
+            if (*abort) return false;
+            if (t0 == 0) t0 = global_ns();
+            else if (global_ns() - t0 > kWaitNs) {
+                atomicExch(&g_tcs_err, (unsigned)(-B200Q_ETIMEOUT));
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Flags between CTAs (PTX memory model: release / acquire at GPU scope).
+__device__ __forceinline__ void flag_release(unsigned long long *f, unsigned long long v) {
+    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long flag_acquire(const unsigned long long *f) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Bounded wait for another CTA's flag to read v.  The CTAs of a launch are
+// all resident once the SMs they wait for are free, and a CTA that publishes
+// never waits on the one reading, so the wait ends; past kWaitNs it records
+// B200Q_ETIMEOUT instead.
+__device__ __forceinline__ bool flag_wait(const unsigned long long *f, unsigned long long v, volatile int *abort) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (flag_acquire(f) == v) return true;
         if ((it & 15) == 15) {
             if (*abort) return false;
             if (t0 == 0) t0 = global_ns();
@@ -315,7 +374,8 @@ struct TcsParams {
     const float *scales;       // [o_pad]
     float *y;                  // [S, O]
     double *plane;             // [grid * pmax][S][128] pieces of shared tiles (f64, unscaled by 2^-T)
-    unsigned long long *cnt;   // [tiles] (token << 8) | arrivals
+    unsigned long long *cnt;   // [tiles] (token << 8) | arrivals (several ranges)
+    unsigned long long *flag;  // [grid * pmax] the token once a plane is written (one range)
     unsigned long long token;  // this call's tag (56 bits)
     int O, I, S;
     int J, N;                  // digits per token; MMA N (rows of B)
@@ -558,6 +618,7 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
             int g = 0, db = 0;
             uint32_t fill = 0, dph = 0;          // fills of buffer g so far (per round of groups)
             unsigned long long ready = 0;        // B slots known to be built
+            uint32_t known = 0;                  // A buffers known to be filled for the current round
             const uint64_t bdesc0 = sw128_desc(smem_u32(b_s));
             bool issued_any = false;
             Walk w;
@@ -573,7 +634,17 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
                     if (!cnt_wait(smem_u32(&slot_cnt[slot]), (uint32_t)S, abort)) break;
                     ready |= 1ull << slot;
                 }
-                if (!cnt_wait(smem_u32(&a_cnt[g]), 4u * (fill + 1), abort)) break;
+                // buffer g filled for this round; an even g also tells about g + 1
+                if (!((known >> g) & 1)) {
+                    if (F::NA % 2 == 0 && (g & 1) == 0) {
+                        bool next = false;
+                        if (!cnt_wait2(smem_u32(&a_cnt[g]), 4u * (fill + 1), abort, next)) break;
+                        if (next) known |= 2u << g;
+                    } else if (!cnt_wait(smem_u32(&a_cnt[g]), 4u * (fill + 1), abort)) {
+                        break;
+                    }
+                }
+                known &= ~(1u << g);
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + kDCol + db * kDStride;
                 const uint64_t bd = bdesc0 + (uint64_t)(((uint32_t)slot * bslot) >> 4);
@@ -609,6 +680,74 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
         // ---------------- dequantizing and epilogue warps: build B, then their loops
         const int sw = warp - kWDeq;                  // 0 .. kStageWarps - 1
         const int stid = sw * 32 + lane;
+        // Dequantizing warps: group grp fills A buffer grp with items grp,
+        // grp + NA, ... of the run (lane = row of the tile).  Item k, the
+        // fill-th use of the buffer:
+        const int grp = (warp - kWDeq) >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t abase = tmem_base + ((uint32_t)(quarter * 32) << 16) + grp * F::COLS;
+        auto deq_item = [&](int k, uint32_t fill) -> bool {
+            const int st = k % DC;
+            if (!mbar_wait(smem_u32(&code_full[st]), (uint32_t)((k / DC) & 1), abort)) return false;
+            // row r's 128 code bytes: eight 16-byte chunks, swizzled; read
+            // in two halves of 16 words, the stage released after the second
+            const uint8_t *row = code_s + (size_t)st * kCodeTile + r * 128;
+            uint32_t w[16], v[32];
+            auto load_half = [&](int h) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 t = *reinterpret_cast<const uint4 *>(row + (((4 * h + c) ^ (r & 7)) << 4));
+                    w[4 * c] = t.x;
+                    w[4 * c + 1] = t.y;
+                    w[4 * c + 2] = t.z;
+                    w[4 * c + 3] = t.w;
+                }
+            };
+            load_half(0);
+            if (!mbar_wait(smem_u32(&a_empty[grp]), (fill & 1) ^ 1, abort)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1) {
+                    load_half(1);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&code_empty[st]));
+                }
+                if (FMT == B200Q_I4) {
+                    // word q -> columns 2q (even codes) and 2q + 1 (odd codes)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        v[2 * q] = w[q] & 0x0F0F0F0Fu;
+                        v[2 * q + 1] = (w[q] >> 4) & 0x0F0F0F0Fu;
+                    }
+                    tmem_st32(abase + h * 32, v);
+                } else if (FMT == B200Q_I8) {
+                    // code + 128 = 16 hi + lo: low nibbles to columns q, high to 32 + q
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        v[q] = (w[q] ^ 0x80808080u) & 0x0F0F0F0Fu;
+                        v[16 + q] = ((w[q] ^ 0x80808080u) >> 4) & 0x0F0F0F0Fu;
+                    }
+                    tmem_st16(abase + h * 16, v);
+                    tmem_st16(abase + 32 + h * 16, v + 16);
+                } else {
+                    // word q -> columns 4q + i: fields i, i + 4, i + 8, i + 12
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) v[4 * q + i] = (w[8 * e + q] >> (2 * i)) & 0x03030303u;
+                        tmem_st32(abase + h * 64 + e * 32, v);
+                    }
+                }
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) cnt_add(smem_u32(&a_cnt[grp]));
+            return true;
+        };
         // the row of ones (each byte 0x01: 2^-9) and the unused rows (zero)
         // do not depend on x: written before the dependency wait
         {
@@ -771,73 +910,9 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
         }
 
         if (warp < kWEpi) {
-            // ---------------- dequantizers: group grp fills A buffer grp with
-            // items grp, grp + NA, ... of the run; lane = row of the tile
-            const int grp = (warp - kWDeq) >> 2, quarter = warp & 3;
-            const int r = quarter * 32 + lane;
-            const uint32_t abase = tmem_base + ((uint32_t)(quarter * 32) << 16) + grp * F::COLS;
-            uint32_t fill = 0;
-            for (int k = grp; k < n_items; k += F::NA, ++fill) {
-                const int st = k % DC;
-                if (!mbar_wait(smem_u32(&code_full[st]), (uint32_t)((k / DC) & 1), abort)) break;
-                // row r's 128 code bytes: eight 16-byte chunks, swizzled; read
-                // in two halves of 16 words, the stage released after the second
-                const uint8_t *row = code_s + (size_t)st * kCodeTile + r * 128;
-                uint32_t w[16], v[32];
-                auto load_half = [&](int h) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 t = *reinterpret_cast<const uint4 *>(row + (((4 * h + c) ^ (r & 7)) << 4));
-                        w[4 * c] = t.x;
-                        w[4 * c + 1] = t.y;
-                        w[4 * c + 2] = t.z;
-                        w[4 * c + 3] = t.w;
-                    }
-                };
-                load_half(0);
-                if (!mbar_wait(smem_u32(&a_empty[grp]), (fill & 1) ^ 1, abort)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1) {
-                        load_half(1);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&code_empty[st]));
-                    }
-                    if (FMT == B200Q_I4) {
-                        // word q -> columns 2q (even codes) and 2q + 1 (odd codes)
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            v[2 * q] = w[q] & 0x0F0F0F0Fu;
-                            v[2 * q + 1] = (w[q] >> 4) & 0x0F0F0F0Fu;
-                        }
-                        tmem_st32(abase + h * 32, v);
-                    } else if (FMT == B200Q_I8) {
-                        // code + 128 = 16 hi + lo: low nibbles to columns q, high to 32 + q
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            v[q] = (w[q] ^ 0x80808080u) & 0x0F0F0F0Fu;
-                            v[16 + q] = ((w[q] ^ 0x80808080u) >> 4) & 0x0F0F0F0Fu;
-                        }
-                        tmem_st16(abase + h * 16, v);
-                        tmem_st16(abase + 32 + h * 16, v + 16);
-                    } else {
-                        // word q -> columns 4q + i: fields i, i + 4, i + 8, i + 12
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) v[4 * q + i] = (w[8 * e + q] >> (2 * i)) & 0x03030303u;
-                            tmem_st32(abase + h * 64 + e * 32, v);
-                        }
-                    }
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) cnt_add(smem_u32(&a_cnt[grp]));
-            }
+            // ---------------- dequantizers
+            for (int k = grp, fill = 0; k < n_items; k += F::NA, ++fill)
+                if (!deq_item(k, (uint32_t)fill)) break;
         } else {
             // ---------------- epilogue: one row per thread, one piece at a time
             const int quarter = warp & 3;
@@ -921,6 +996,55 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
                         #pragma unroll
                         for (int s = 0; s < kMaxS; ++s)
                             if (s < S) p.y[(long long)s * p.O + o] = (float)(sc * val[s]);
+                } else if (p.nr == 1) {
+                    // One range: the CTA holding the tile's first item covers the
+                    // tile's start as the last piece of its run, so it finishes
+                    // last (with any CTA whose whole run lies in the tile); it adds
+                    // the other CTAs' planes, in CTA order, after their flags.
+                    const int c0 = cta_of(p, sf), c1 = cta_of(p, sf + range_size(p, pr) - 1);
+                    if ((int)blockIdx.x != c0) {
+                        const int lp = seg - seg_base;
+                        double *pl = p.plane + ((size_t)blockIdx.x * p.pmax + lp) * S * kRowsT;
+#pragma unroll
+                        for (int s = 0; s < kMaxS; ++s)
+                            if (s < S) pl[s * kRowsT + r] = val[s];
+                        // the barrier orders every thread's plane before thread 0's
+                        // fence (cumulative), which orders them before the flag
+                        named_sync(2, kEpiWarps * 32);
+                        if (etid == 0) {
+                            __threadfence();
+                            flag_release(p.flag + (size_t)blockIdx.x * p.pmax + lp, p.token);
+                        }
+                    } else {
+                        bool okw = true;
+                        if (etid == 0)
+                            for (int c = c0 + 1; c <= c1 && okw; ++c)
+                                okw = flag_wait(p.flag + (size_t)c * p.pmax + (seg - item_of(p, run_first(p, c)).seg),
+                                                p.token, abort);
+                        if (named_sync_or(2, kEpiWarps * 32, !okw)) break;
+                        double sum[kMaxS];
+#pragma unroll
+                        for (int s = 0; s < kMaxS; ++s) sum[s] = val[s];
+                        for (int c = c0 + 1; c <= c1; c += 2) {
+                            double v[2][kMaxS];
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const int cc = c + k <= c1 ? c + k : c;
+                                const double *q = p.plane +
+                                                  ((size_t)cc * p.pmax + (seg - item_of(p, run_first(p, cc)).seg)) * S * kRowsT + r;
+#pragma unroll
+                                for (int s = 0; s < kMaxS; ++s) v[k][s] = c + k <= c1 && s < S ? __ldcg(q + s * kRowsT) : 0.0;
+                            }
+#pragma unroll
+                            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                                for (int s = 0; s < kMaxS; ++s) sum[s] += v[k][s];
+                        }
+                        if (o < p.O)
+#pragma unroll
+                            for (int s = 0; s < kMaxS; ++s)
+                                if (s < S) p.y[(long long)s * p.O + o] = (float)(sc * sum[s]);
+                    }
                 } else {
                     const int lp = seg - seg_base;
                     double *pl = p.plane + ((size_t)blockIdx.x * p.pmax + lp) * S * kRowsT;
@@ -1095,7 +1219,7 @@ cudaError_t launch_fmt(const Tensor &t, const float *x, float *y, int S, cudaStr
     cudaError_t e = cudaSuccess;
     const size_t plane_bytes = (size_t)pl.G * pl.pmax * S * kRowsT * sizeof(double);
     if (pl.shared) {
-        e = workspace_alloc((void **)&plane, plane_bytes + (size_t)tiles * 8 + 256, st);
+        e = workspace_alloc((void **)&plane, plane_bytes + (size_t)tiles * 8 + (size_t)pl.G * pl.pmax * 8 + 256, st);
         if (e != cudaSuccess) return e;
     }
     e = allow_dynamic_smem((const void *)qmv_tc_kernel<FMT>, (int)pl.smem);
@@ -1107,6 +1231,7 @@ cudaError_t launch_fmt(const Tensor &t, const float *x, float *y, int S, cudaStr
     prm.cnt = plane ? reinterpret_cast<unsigned long long *>(
                           (reinterpret_cast<uintptr_t>(plane) + plane_bytes + 15) & ~(uintptr_t)15)
                     : nullptr;
+    prm.flag = prm.cnt ? prm.cnt + tiles : nullptr;
     prm.token = next_token();
     prm.O = t.O;
     prm.I = t.I;
