@@ -65,8 +65,12 @@ constexpr int stages_for() {
     constexpr int n = (232448 - 1024 - 512) / per;
     return n > 10 ? 10 : n;
 }
-constexpr int kThreads = 448;        // 14 warps
-constexpr int kDeqWarps = 8;
+constexpr int kDeqWarps = 8;         // per group of dequantizing warps
+// Groups of dequantizing warps (on alternate k-blocks): two where the
+// dequantization carries group scales (measured +8 % at gs = 128), one with
+// per-row scales (measured 2 % slower with two).
+constexpr int deq_groups(int gsm) { return gsm ? 2 : 1; }
+constexpr int threads_for(int gsm) { return (2 + deq_groups(gsm) * kDeqWarps + 4) * 32; }
 // Tensor memory: kNumA A buffers of 32 columns (a k-block of 64 bf16 per
 // lane = weight row) at columns 0.., then two accumulators of up to 192
 // columns.
@@ -301,10 +305,11 @@ struct GemmParams {
 // code word (8 columns) or an int8 16-byte chunk (16 columns) always lies in
 // one group (gs is a multiple of 16 for int8, of 16 or 32 for int4).
 template <int FMT, int BNT, bool PIECES, int GSM = 0>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(GSM), 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const __grid_constant__ CUtensorMap map_sc, const GemmParams p) {
     constexpr bool GS = GSM != 0;
+    constexpr int kDeqGroups = deq_groups(GSM);
     constexpr int kStages = stages_for<FMT, BNT, GSM>();
     constexpr uint32_t kIdesc = idesc_for(BNT);
     static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= kAccStride && (!PIECES || BNT <= 48), "token tile");
@@ -441,16 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) mma_commit(smem_u32(&acc_full[ab]));
             }
         }
-    } else if (warp >= 2 && warp < 2 + kDeqWarps) {
+    } else if (warp >= 2 && warp < 2 + kDeqGroups * kDeqWarps) {
         // ---------------- dequantizers: thread (r, half) owns half of row r
         // of every A tile (tensor-memory columns 16 half .. 16 half + 15 of an
         // A buffer); a warp reaches only its own lane quarter (warp % 4), so
         // that quarter's 32 rows are its rows
+        // With two groups of eight warps, they take alternate k-blocks of
+        // the CTA's sequence (the k-th of all its (tile, k-block) steps goes
+        // to group k % 2), so two k-blocks are dequantized at once: each step
+        // waits on the stage's copy and on the A buffer.
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        const int half = (warp - 2) >> 2;
-        int stage = 0, abuf = 0;
-        uint32_t phase = 0, aphase = 0;
+        const int grp = (warp - 2) / kDeqWarps;
+        const int half = ((warp - 2) % kDeqWarps) >> 2;
         bool ok = true;
         // group-wise scales of the thread's 4 code words (int4) or 2 chunks
         // (int8) of k-block kb, loaded one k-block ahead
@@ -470,9 +478,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dst[i] = __ldg(p.scales + o * p.g_ld + g);
             }
         };
-        if (GSM == 1 && t_first < n_tiles_total) load_gs(t_first, kb0, gsn);
+        // the step after (tile, kb) in the CTA's sequence
+        auto step = [&](int &tl, int &k) {
+            if (++k == kb1) {
+                k = kb0;
+                tl += t_step;
+            }
+        };
+        if (GSM == 1) {   // this group's first step
+            int tl = t_first, k = kb0;
+            for (int g = 0; g < grp; ++g) step(tl, k);
+            if (tl < n_tiles_total) load_gs(tl, k, gsn);
+        }
+        unsigned seq = 0;                                // step index in the CTA's sequence
         for (int tile = QWQ_TILE_FIRST; tile < n_tiles_total && ok; tile += QWQ_TILE_STEP) {
-            for (int kb = QWQ_KB_FIRST; kb < QWQ_KB_END; ++kb) {
+            for (int kb = QWQ_KB_FIRST; kb < QWQ_KB_END; ++kb, ++seq) {
+                if ((int)(seq % kDeqGroups) != grp) continue;
+                const int stage = (int)(seq % kStages), abuf = (int)(seq % kNumA);
+                const uint32_t phase = (seq / kStages) & 1, aphase = (seq / kNumA) & 1;
                 if constexpr (GSM == 1) {
                     if (p.g_one) {
                         const ScalePair sp = split_scale(gsn[0]);
@@ -482,8 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kGW; ++i) gsc[i] = split_scale(gsn[i]);
                     }
-                    if (kb + 1 < kb1) load_gs(tile, kb + 1, gsn);
-                    else if (tile + t_step < n_tiles_total) load_gs(tile + t_step, kb0, gsn);
+                    int tl = tile, k = kb;                   // this group's next step
+                    for (int g = 0; g < kDeqGroups; ++g) step(tl, k);
+                    if (tl < n_tiles_total) load_gs(tl, k, gsn);
                 }
                 if (!mbar_wait(smem_u32(&tma_full[stage]), phase)) {
                     ok = false;
@@ -550,14 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&a_full[abuf]));
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-                if (++abuf == kNumA) {
-                    abuf = 0;
-                    aphase ^= 1;
-                }
             }
         }
     } else {
@@ -828,7 +844,7 @@ cudaError_t run_gemm(const Tensor &t, const __nv_bfloat16 *xb, int b_rows, const
     const int n_sms = sm_count(t.device);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = ksplit > 1 ? tiles * ksplit : tiles < n_sms ? tiles : n_sms;
-    qgemm_tc_kernel<FMT, BNT, PIECES, GSM><<<grid, kThreads, smem, st>>>(t.gemm_map, map_x, t.gemm_sc_map, p);
+    qgemm_tc_kernel<FMT, BNT, PIECES, GSM><<<grid, threads_for(GSM), smem, st>>>(t.gemm_map, map_x, t.gemm_sc_map, p);
     count_launch();
     return cudaGetLastError();
 }
