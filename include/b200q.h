@@ -177,10 +177,16 @@ int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *s
  * magnitude in the CTA's columns: for every output, |y - y_exact| <=
  * |scale| * 2^-27 * max|x| * sum|deq| at J = 7.  At most 8 tokens per launch
  * (more are chunked); the work is split evenly over the SMs in (row tile,
- * 128-byte k-block) items, and a tile shared by several CTAs is added up in
- * a fixed order by the CTA that brings its arrival count to its number of
- * pieces.  Each call with shared tiles takes a workspace from the library's
- * pool.
+ * 128-byte k-block) items.  A tile shared by several CTAs is added up in a
+ * fixed order: with one k-range, by the CTA holding its first k-block, once
+ * the others have published their parts (a bounded wait on their flags);
+ * with several k-ranges, by the CTA that brings its arrival count to its
+ * number of parts.  Each call with shared tiles takes a workspace from the
+ * library's pool.  The flag wait assumes the launch's CTAs (one per SM) can
+ * all become resident: calls of this path on concurrent streams that keep
+ * each other's CTAs off the SMs end in B200Q_ETIMEOUT
+ * (b200q_device_status) after 2 s, not in a hang.  AUTO never takes this
+ * path.
  */
 int b200q_matmul_ex(const b200q_tensor *t, const float *x, float *y, int S, int path,
                     void *stream);
