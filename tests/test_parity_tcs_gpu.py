@@ -56,6 +56,31 @@ def test_tcs_partitions(q, fmt, O, I):
         _check(q, fmt, O, I, S, seed=O + I + S)
 
 
+@pytest.mark.parametrize("fmt", [f for f, _ in FMTS], ids=[n for _, n in FMTS])
+@pytest.mark.parametrize("O,I,S", [(4000, 16384, 5), (4000, 16384, 8), (3000, 20000, 8)])
+def test_tcs_several_ranges(q, fmt, O, I, S):
+    """Long rows at 5-8 tokens: every CTA's k-blocks no longer fit its B
+    slots at once, so K is cut into ranges (8 to 53 of them here), each tile
+    is shared by the CTAs of all its ranges, and the CTA that brings the
+    tile's arrival count to its number of pieces adds them."""
+    _check(q, fmt, O, I, S, seed=O + S)
+
+
+def test_tcs_several_ranges_extreme_x(q):
+    """The same shared-tile path with tokens of very different magnitudes:
+    every CTA's pieces carry their own power of two."""
+    fmt, O, I, S = 2, 4000, 16384, 8
+    codes, scales, x = inputs(fmt, O, I, S, seed=31)
+    x = x.astype(np.float64)
+    x[0] *= 2.0 ** -135
+    x[1] *= 1e30
+    x[2, : I // 2] = 0.0
+    x[3] = 0.0
+    x[4, 5] = 1e4
+    y = _check(q, fmt, O, I, S, x=x.astype(np.float32))
+    assert np.all(y[3] == 0)
+
+
 @pytest.mark.parametrize("S", [1, 4])
 def test_tcs_int4_12288x6144(q, S):
     """The headline decode shape, every output."""
