@@ -30,8 +30,11 @@
  *                   the tensor cores (B200Q_PATH_TCX): each row of x is scaled
  *                   by an exact power of two and split exactly into three
  *                   bf16 pieces, so every product is exact and only the f32
- *                   accumulation rounds; S = 1 and the other formats run
- *                   SIMT kernels (B200Q_PATH_F32)
+ *                   accumulation rounds; int2 tensors with per-row scales
+ *                   at 3 to 15 rows run it on the fp8 tensor cores
+ *                   (B200Q_PATH_TCS: exact products, x rounded to 26-30
+ *                   bits); S = 1 and the other cases run SIMT kernels
+ *                   (B200Q_PATH_F32)
  *   tensor-core path (int8 / int4 tensors at S >= b200q_tc_min_s()): x is
  *                   rounded to bf16 (nearest, ties to even) inside the call,
  *                   products and sums are f32 on the tensor cores:
@@ -178,15 +181,10 @@ int b200q_matmul(const b200q_tensor *t, const float *x, float *y, int S, void *s
  * |scale| * 2^-27 * max|x| * sum|deq| at J = 7.  At most 8 tokens per launch
  * (more are chunked); the work is split evenly over the SMs in (row tile,
  * 128-byte k-block) items.  A tile shared by several CTAs is added up in a
- * fixed order: with one k-range, by the CTA holding its first k-block, once
- * the others have published their parts (a bounded wait on their flags);
- * with several k-ranges, by the CTA that brings its arrival count to its
- * number of parts.  Each call with shared tiles takes a workspace from the
- * library's pool.  The flag wait assumes the launch's CTAs (one per SM) can
- * all become resident: calls of this path on concurrent streams that keep
- * each other's CTAs off the SMs end in B200Q_ETIMEOUT
- * (b200q_device_status) after 2 s, not in a hang.  AUTO never takes this
- * path.
+ * fixed order by the CTA that brings its arrival count to its number of
+ * parts; no CTA waits on another.  Each call with shared tiles takes a
+ * workspace from the library's pool.  AUTO takes this path for int2 tensors
+ * with per-row scales at 3 to 15 rows.
  */
 int b200q_matmul_ex(const b200q_tensor *t, const float *x, float *y, int S, int path,
                     void *stream);

@@ -170,10 +170,14 @@ int tcx_min_s() {
 
 // AUTO: int8 / int4 take the bf16 tensor-core path from tc_min_s() rows, the
 // f32-accurate tensor-core path (x in three bf16 pieces; per-row scales only)
-// from tcx_min_s() rows, the SIMT f32 path below; f32 and int2 tensors always
-// the SIMT path.
+// from tcx_min_s() rows, the SIMT f32 path below.  int2 with per-row scales
+// takes the exact fp8 tensor-core path from 3 to 15 rows (where the SIMT
+// kernel needs two or more passes over the weights: 8192^2 at 3 / 4 / 8
+// rows, 29.0 / 32.5 / 64.4 us against 23.5 / 24.1 / 42.8 us), the SIMT path
+// otherwise; f32 tensors always the SIMT path.
 int select_path(const Tensor &t, int S, int path) {
     if (path != B200Q_PATH_AUTO) return path;
+    if (t.fmt == B200Q_I2) return !t.gs && S >= 3 && S < 16 ? B200Q_PATH_TCS : B200Q_PATH_F32;
     if (t.fmt != B200Q_I4 && t.fmt != B200Q_I8) return B200Q_PATH_F32;
     if (S >= tc_min_s()) return B200Q_PATH_TC;
     if (!t.gs && S >= tcx_min_s()) return B200Q_PATH_TCX;

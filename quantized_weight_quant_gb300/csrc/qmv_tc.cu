@@ -36,11 +36,14 @@
 // k-blocks (whose B tiles it builds once, in shared memory) fit; it is the
 // whole row when they do.  A CTA accumulates each (range, tile) run of its
 // items in one tensor-memory accumulator.  A tile that one CTA covers whole
-// goes straight to y.  Otherwise, with one range, the CTA holding the tile's
-// first item (the tile is the last piece of its run) adds the other CTAs'
-// f64 planes, in CTA order, once their flags (tagged with the call's token)
-// are set; with several ranges, the CTA that brings the tile's arrival count
-// (an atomic tagged with the token) to its number of pieces adds them.
+// goes straight to y.  Otherwise every piece is written as an f64 plane and
+// the CTA that brings the tile's arrival count (an atomic tagged with the
+// call's token) to its number of pieces adds the planes in a fixed order and
+// writes y.  No CTA waits on another, so calls on concurrent streams cannot
+// hold each other up.  (A variant in which the CTA holding the tile's first
+// item waited for the others' flags measured ~1 us faster per call; its
+// wait needs every CTA of the launch resident, which concurrent launches
+// can prevent.)
 // Warp roles: warp 0 issues the TMA copies of the code tiles (128 rows x
 // 128 bytes, 128-byte swizzle) into a ring, from the start, since the
 // weights are read-only; warp 1 allocates tensor memory and issues the MMAs;
@@ -182,36 +185,6 @@ __device__ __forceinline__ bool cnt_wait2(uint32_t addr, uint32_t want, volatile
             return true;
         }
         if ((it & 255) == 255) {
-            if (*abort) return false;
-            if (t0 == 0) t0 = global_ns();
-            else if (global_ns() - t0 > kWaitNs) {
-                atomicExch(&g_tcs_err, (unsigned)(-B200Q_ETIMEOUT));
-                *abort = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// Flags between CTAs (PTX memory model: release / acquire at GPU scope).
-__device__ __forceinline__ void flag_release(unsigned long long *f, unsigned long long v) {
-    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long flag_acquire(const unsigned long long *f) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
-    return v;
-}
-
-// Bounded wait for another CTA's flag to read v.  The CTAs of a launch are
-// all resident once the SMs they wait for are free, and a CTA that publishes
-// never waits on the one reading, so the wait ends; past kWaitNs it records
-// B200Q_ETIMEOUT instead.
-__device__ __forceinline__ bool flag_wait(const unsigned long long *f, unsigned long long v, volatile int *abort) {
-    unsigned long long t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (flag_acquire(f) == v) return true;
-        if ((it & 15) == 15) {
             if (*abort) return false;
             if (t0 == 0) t0 = global_ns();
             else if (global_ns() - t0 > kWaitNs) {
@@ -374,8 +347,7 @@ struct TcsParams {
     const float *scales;       // [o_pad]
     float *y;                  // [S, O]
     double *plane;             // [grid * pmax][S][128] pieces of shared tiles (f64, unscaled by 2^-T)
-    unsigned long long *cnt;   // [tiles] (token << 8) | arrivals (several ranges)
-    unsigned long long *flag;  // [grid * pmax] the token once a plane is written (one range)
+    unsigned long long *cnt;   // [tiles] (token << 8) | arrivals
     unsigned long long token;  // this call's tag (56 bits)
     int O, I, S;
     int J, N;                  // digits per token; MMA N (rows of B)
@@ -996,55 +968,6 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
                         #pragma unroll
                         for (int s = 0; s < kMaxS; ++s)
                             if (s < S) p.y[(long long)s * p.O + o] = (float)(sc * val[s]);
-                } else if (p.nr == 1) {
-                    // One range: the CTA holding the tile's first item covers the
-                    // tile's start as the last piece of its run, so it finishes
-                    // last (with any CTA whose whole run lies in the tile); it adds
-                    // the other CTAs' planes, in CTA order, after their flags.
-                    const int c0 = cta_of(p, sf), c1 = cta_of(p, sf + range_size(p, pr) - 1);
-                    if ((int)blockIdx.x != c0) {
-                        const int lp = seg - seg_base;
-                        double *pl = p.plane + ((size_t)blockIdx.x * p.pmax + lp) * S * kRowsT;
-#pragma unroll
-                        for (int s = 0; s < kMaxS; ++s)
-                            if (s < S) pl[s * kRowsT + r] = val[s];
-                        // the barrier orders every thread's plane before thread 0's
-                        // fence (cumulative), which orders them before the flag
-                        named_sync(2, kEpiWarps * 32);
-                        if (etid == 0) {
-                            __threadfence();
-                            flag_release(p.flag + (size_t)blockIdx.x * p.pmax + lp, p.token);
-                        }
-                    } else {
-                        bool okw = true;
-                        if (etid == 0)
-                            for (int c = c0 + 1; c <= c1 && okw; ++c)
-                                okw = flag_wait(p.flag + (size_t)c * p.pmax + (seg - item_of(p, run_first(p, c)).seg),
-                                                p.token, abort);
-                        if (named_sync_or(2, kEpiWarps * 32, !okw)) break;
-                        double sum[kMaxS];
-#pragma unroll
-                        for (int s = 0; s < kMaxS; ++s) sum[s] = val[s];
-                        for (int c = c0 + 1; c <= c1; c += 2) {
-                            double v[2][kMaxS];
-#pragma unroll
-                            for (int k = 0; k < 2; ++k) {
-                                const int cc = c + k <= c1 ? c + k : c;
-                                const double *q = p.plane +
-                                                  ((size_t)cc * p.pmax + (seg - item_of(p, run_first(p, cc)).seg)) * S * kRowsT + r;
-#pragma unroll
-                                for (int s = 0; s < kMaxS; ++s) v[k][s] = c + k <= c1 && s < S ? __ldcg(q + s * kRowsT) : 0.0;
-                            }
-#pragma unroll
-                            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                                for (int s = 0; s < kMaxS; ++s) sum[s] += v[k][s];
-                        }
-                        if (o < p.O)
-#pragma unroll
-                            for (int s = 0; s < kMaxS; ++s)
-                                if (s < S) p.y[(long long)s * p.O + o] = (float)(sc * sum[s]);
-                    }
                 } else {
                     const int lp = seg - seg_base;
                     double *pl = p.plane + ((size_t)blockIdx.x * p.pmax + lp) * S * kRowsT;
@@ -1219,7 +1142,7 @@ cudaError_t launch_fmt(const Tensor &t, const float *x, float *y, int S, cudaStr
     cudaError_t e = cudaSuccess;
     const size_t plane_bytes = (size_t)pl.G * pl.pmax * S * kRowsT * sizeof(double);
     if (pl.shared) {
-        e = workspace_alloc((void **)&plane, plane_bytes + (size_t)tiles * 8 + (size_t)pl.G * pl.pmax * 8 + 256, st);
+        e = workspace_alloc((void **)&plane, plane_bytes + (size_t)tiles * 8 + 256, st);
         if (e != cudaSuccess) return e;
     }
     e = allow_dynamic_smem((const void *)qmv_tc_kernel<FMT>, (int)pl.smem);
@@ -1231,7 +1154,6 @@ cudaError_t launch_fmt(const Tensor &t, const float *x, float *y, int S, cudaStr
     prm.cnt = plane ? reinterpret_cast<unsigned long long *>(
                           (reinterpret_cast<uintptr_t>(plane) + plane_bytes + 15) & ~(uintptr_t)15)
                     : nullptr;
-    prm.flag = prm.cnt ? prm.cnt + tiles : nullptr;
     prm.token = next_token();
     prm.O = t.O;
     prm.I = t.I;

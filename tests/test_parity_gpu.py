@@ -148,7 +148,7 @@ def test_bad_pointers_rejected(q):
 
 def test_path_selection(q):
     thr, thx = q.tc_min_s(), q.tcx_min_s()
-    for fmt in (0, 1, 2, 3):
+    for fmt in (0, 1, 2):
         codes, scales, _ = inputs(fmt, 8, 32, 1)
         with q.tensor_upload(fmt, 8, 32, codes, scales) as t:
             tcx = fmt in (1, 2) and thx < thr
@@ -156,6 +156,15 @@ def test_path_selection(q):
             assert q.matmul_path(t, 1) == (q.PATH_TCX if tcx and thx <= 1 else q.PATH_F32)
             want = q.PATH_TC if fmt in (1, 2) else q.PATH_F32
             assert q.matmul_path(t, thr) == want
+    # int2 with per-row scales: the exact fp8 tensor-core path from 3 to 15
+    # rows, the SIMT kernels otherwise; with group scales always SIMT
+    codes, scales, _ = inputs(3, 8, 64, 1)
+    with q.tensor_upload(3, 8, 64, codes, scales) as t:
+        assert [q.matmul_path(t, S) for S in (1, 2, 3, 8, 15, 16, 100)] == \
+            [q.PATH_F32, q.PATH_F32, q.PATH_TCS, q.PATH_TCS, q.PATH_TCS, q.PATH_F32, q.PATH_F32]
+    gsc = synth.uniform_f32((8, 1), 1e-3, 2e-2, 0, 2)
+    with q.tensor_upload(3, 8, 64, codes, gsc, gs=64) as t:
+        assert q.matmul_path(t, 8) == q.PATH_F32
 
 
 def test_tensor_info(q):
