@@ -800,7 +800,9 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     };
     clear_acc();
 
-    for (int base = rg0; base < rg1 && ok; base += kR) {
+    // A warp whose wait gave up keeps walking the rounds without work, so
+    // that every consumer still reaches each round's barriers.
+    for (int base = rg0; base < rg1; base += kR) {
         const int rend = base + kR < rg1 ? base + kR : rg1;
         const bool last_round = rend >= rg1;
         if (base != rg0) {
@@ -810,7 +812,7 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         }
         run_of(cc, base, warp);
         int cur_rgl = -1;
-        for (; cc.u < cc.u_end; advance(cc)) {
+        for (; ok && cc.u < cc.u_end; advance(cc)) {
             if (!mbar_wait(my_full + 8 * c_stage, c_phase, kWaitNs)) {
                 ok = false;
                 break;
