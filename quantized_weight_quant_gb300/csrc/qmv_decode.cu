@@ -368,7 +368,7 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
 
     // shared memory: x' [nx_max][NS][k_alloc] | rings [nw][depth] | full and
     // empty mbarriers [2][nw][depth] + x-staged + x-issued | partials | per-row unscale
-    // factors | max scratch | done counter | row scales
+    // factors | max scratch | 16 spare bytes | row scales
     float *xs = reinterpret_cast<float *>(smem);
     uint8_t *ring = smem + (size_t)4 * nxr * k_alloc;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + (size_t)nw * depth * stg);
@@ -376,8 +376,7 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     float *part = reinterpret_cast<float *>(bars + 2 * nw * depth + 2);  // [kR][nw][NS][8]
     float *unscale = part + (size_t)kR * nw * NS * 8;                  // [nxr][2]: 2^-T as two factors
     float *red = unscale + 2 * nxr;                                    // [nxr][kMaxWarps]
-    int *done = reinterpret_cast<int *>(red + nxr * kMaxWarps);        // warps done with the last round
-    float *row_scale = reinterpret_cast<float *>(done + 4);           // [rows of this CTA]
+    float *row_scale = red + nxr * kMaxWarps + 4;                     // [rows of this CTA]
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nw * depth);
     const uint32_t x_ready = smem_u32(bars + 2 * nw * depth);   // completes once x is staged
     const uint32_t x_issued = smem_u32(bars + 2 * nw * depth + 1);  // once every consumer warp's x loads are out
@@ -541,9 +540,8 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     }
 
     // round-0 partials start at zero (warps that touch no unit of a row group
-    // leave 0); the counter picks the warp that combines the last round
+    // leave 0)
     for (int i = tid; i < kR * nw * NS * 8; i += nct) part[i] = 0.f;
-    if (tid == 0) *done = 0;
 
     // Everything above touched only the weights, which no kernel writes; x
     // (and y) may be written (read) by the kernel before this one in the
@@ -882,22 +880,11 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
             }
         }
         if (cur_rgl >= 0) flush(cur_rgl);
-        // combine this round: warps in order, unscale, apply the row scale.
-        // The last round is combined by whichever warp finishes last (no
-        // block barrier); earlier rounds by all consumers between barriers.
-        int c_first = tid, c_step = nct;
-        if (last_round) {
-            __threadfence_block();
-            int prev = 0;
-            if (lane == 0) prev = atomicAdd(done, 1);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev != nw - 1) break;               // not the last warp: done
-            __threadfence_block();
-            c_first = lane;
-            c_step = 32;
-        } else {
-            consumers_sync(nct);
-        }
+        // combine this round, all consumers after a barrier (a row per thread;
+        // measured 0.4 us faster per call than the last warp alone): warps in
+        // order, unscale, apply the row scale
+        const int c_first = tid, c_step = nct;
+        consumers_sync(nct);
         // partials added in warp order (warps that ran no unit of a row group
         // hold +0 there); the set's fields stay in registers until the row
         // groups move into the next set
