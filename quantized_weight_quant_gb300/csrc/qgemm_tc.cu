@@ -912,14 +912,23 @@ cudaError_t run_tcx_chunk(const Tensor &t, const Tensor *tu, const __nv_bfloat16
     for (int k = 0; k < (tu ? 2 : 1) && e == cudaSuccess; ++k) {
         const Tensor &tt = k ? *tu : t;
         float *yy = k ? yu : y;
-        // fewer row tiles than half the SMs: split each tile's k-blocks over
-        // several CTAs (each keeps at least 4 k-blocks); their partials go to
-        // planes of a workspace and are added in plane order
+        // Split each tile's k-blocks over ks CTAs (one CTA per SM, each
+        // keeping at least 4 k-blocks) when that shortens the call: the time
+        // goes as (waves of CTAs) x (k-blocks per CTA), since each k-block
+        // costs a fixed copy/barrier round trip.  The partials go to planes
+        // of a workspace and are added in plane order.  (O = 8192: 64 tiles,
+        // ks = 2; O = 12288: 96 tiles, ks = 3 in two waves.)
         const int tiles = tt.o_pad / BM, nk = (int)(tt.k_pad / BK);
         const int n_sms = sm_count(tt.device);
-        int ks = tiles * 2 <= n_sms ? n_sms / tiles : 1;
-        if (ks > 4) ks = 4;
-        if (ks > nk / 4) ks = nk / 4 > 1 ? nk / 4 : 1;
+        int ks = 1;
+        long long best = (long long)((tiles + n_sms - 1) / n_sms) * nk;
+        for (int k = 2; k <= 6 && nk / k >= 4; ++k) {
+            const long long cost = (long long)((tiles * k + n_sms - 1) / n_sms) * ((nk + k - 1) / k);
+            if (cost < best) {
+                best = cost;
+                ks = k;
+            }
+        }
         float *dst = yy;
         const long long n = (long long)ns * tt.O;
         if (ks > 1) {
