@@ -156,6 +156,32 @@ def test_tcs_zero_column_ranges(q, fmt):
     _check(q, fmt, O, I, S, x=x.astype(np.float32))
 
 
+def _digits(S):
+    """Digits per token of a launch of S (<= 8) tokens: N = 16 ceil((7S+1)/16)
+    columns, 8 digits where 8S + 1 of them fit, else 7."""
+    n = 16 * -(-(7 * S + 1) // 16)
+    return 8 if 8 * S + 1 <= n else 7
+
+
+@pytest.mark.parametrize("fmt", [f for f, _ in FMTS], ids=[n for _, n in FMTS])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
+def test_tcs_error_bound(q, fmt, S):
+    """The path's own bound, far inside the f32 bar: x is the only thing
+    rounded (to 4J-2 bits below its token's largest magnitude), so
+    |y - y_exact| <= 2^(1-4J) max|x_s| sum_i |scale deq| plus y's rounding."""
+    O, I = 1024, 4096
+    codes, scales, x = inputs(fmt, O, I, S, seed=7 + S)
+    _, _, ydbl = oracle.matmul(fmt, O, I, codes, scales, x, want_dbl=True)
+    _, absrow = oracle.matmul(fmt, O, I, codes, scales, np.ones((1, I), np.float32))   # sum_i |scale deq|
+    with q.tensor_upload(fmt, O, I, codes, scales) as t:
+        y = gpu_matmul(q, t, x, S, O, q.PATH_TCS).astype(np.float64)
+    J = _digits(S)
+    xmax = np.abs(x.astype(np.float64)).max(axis=1, keepdims=True)
+    tol = 2.0 ** (1 - 4 * J) * xmax * absrow[0][None, :] + 2.0 ** -24 * np.abs(ydbl) + 1e-300
+    err = np.abs(y - ydbl)
+    assert np.all(err <= tol), float((err / tol).max())
+
+
 def test_tcs_repeatable(q):
     codes, scales, x = inputs(2, 1024, 4096, 5, seed=3)
     with q.tensor_upload(2, 1024, 4096, codes, scales) as t:
