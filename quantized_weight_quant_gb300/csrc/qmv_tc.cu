@@ -196,6 +196,17 @@ __device__ __forceinline__ bool cnt_wait2(uint32_t addr, uint32_t want, volatile
     }
 }
 
+// Compare-and-swap at GPU scope with acquire-release semantics: the release
+// orders this thread's earlier writes (and, through a preceding barrier, its
+// CTA's) before the swap; the acquire orders its later reads after it.
+__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long *a, unsigned long long cmp,
+                                                          unsigned long long val) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(old) : "l"(a), "l"(cmp), "l"(val)
+                 : "memory");
+    return old;
+}
+
 // A wait that ignores the abort flag (winding down: copies or MMAs already
 // issued must complete before the CTA leaves), bounded by a quarter of kWaitNs.
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
@@ -975,10 +986,9 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
                     for (int s = 0; s < kMaxS; ++s)
                         if (s < S) pl[s * kRowsT + r] = val[s];
                     // the barrier orders every thread's plane before thread 0's
-                    // fence (cumulative), which orders them before the count
+                    // release (cumulative), part of the count's update
                     named_sync(2, kEpiWarps * 32);
                     if (etid == 0) {
-                        __threadfence();
                         // pieces of tile t: its segments' CTAs, range by range
                         int expect = 0;
                         for (int rr = 0; rr < p.nr; ++rr) {
@@ -986,17 +996,19 @@ __global__ void __launch_bounds__(Roles<FMT>::kThreads, 1)
                             expect += cta_of(p, f0 + range_size(p, rr) - 1) - cta_of(p, f0) + 1;
                         }
                         const unsigned long long tag = p.token << 8;
+                        // a word left by an earlier call (or any earlier use of the
+                        // memory) does not carry this call's tag: the first
+                        // arrival replaces it
                         unsigned long long old = *(volatile unsigned long long *)&p.cnt[t], nv = 0;
                         for (int k = 0; k < 4096; ++k) {
                             nv = (old & ~0xFFull) == tag ? old + 1 : tag | 1ull;
-                            const unsigned long long prev = atomicCAS(&p.cnt[t], old, nv);
+                            const unsigned long long prev = cas_acq_rel(&p.cnt[t], old, nv);
                             if (prev == old) break;
                             old = prev;
                             nv = 0;
                         }
                         const bool last = nv != 0 && (int)(nv & 0xFF) == expect;
                         if (last) {
-                            __threadfence();
                             // the tile's planes in (range, CTA) order
                             int n = 0;
                             for (int rr = 0; rr < p.nr; ++rr) {
