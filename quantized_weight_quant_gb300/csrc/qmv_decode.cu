@@ -331,7 +331,7 @@ struct DecParams {
     int round_rgs;            // row groups combined per round (partials buffer rows)
     int nx_max;               // most x slots any CTA stages (shared-memory layout)
     int gbox;                 // group scales per row in a stage (group-wise scales)
-    FastDiv div_grid, div_nw, div_nseg;   // by gridDim.x, the consumer warps, the segments per row
+    FastDiv div_grid, div_nseg;   // by gridDim.x, the segments per row
     FastDiv div_gs;           // by the group size (group-wise scales)
 };
 
@@ -350,6 +350,10 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     constexpr int SEGE = (kSeg / 16) * E;            // elements of a row in one stage
     constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
     constexpr int EW = 32 / bits;                    // elements per 32-bit word
+    // several tokens with per-row scales: the unrolled body of a stage
+    // outgrows the instruction cache (no_instruction stalls led at four
+    // tokens), so its four words run as a loop
+    constexpr bool kRollQ = FMT != B200Q_F32 && NS >= 2 && GW == 0;
     constexpr int NV = 8 * NS;                       // partial sums per lane and row group
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -402,12 +406,30 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         int u, u_end;                // unit index within the round's run
         int rgl, sg;                 // u = rgl * nseg + sg
     };
+    // A round's units are shared out by the warps' schedulers (warp % 4):
+    // measured per-scheduler finish times fit a throughput of n / (n + 1) for
+    // n consumer warps on a scheduler (3 warps: 0.94 and 2 warps: 0.87 of a
+    // full scheduler's rate), so each warp's weight is 60 / (n + 1).  Even
+    // shares per warp left the 3-warp schedulers of a 10-warp launch (3, 3,
+    // 2, 2) with 30% more work than the rest.  wcum(w): the weights of the
+    // warps below w.
+    auto wcum = [&](int w) {
+        int c = 0;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const int n_on = (nw - s + 3) >> 2;
+            const int below = w > s ? (w - s + 3) >> 2 : 0;
+            c += below * (n_on >= 4 ? 12 : n_on == 3 ? 15 : n_on == 2 ? 20 : 30);
+        }
+        return c;
+    };
+    const int wtot = wcum(nw);
     auto run_of = [&](Cursor &c, int base, int w) {
         c.round_base = base;
         c.round_end = base + kR < rg1 ? base + kR : rg1;
         const int U = (c.round_end - c.round_base) * nseg;
-        c.u = fdiv(w * U, p.div_nw);
-        c.u_end = fdiv((w + 1) * U, p.div_nw);
+        c.u = U * wcum(w) / wtot;
+        c.u_end = U * wcum(w + 1) / wtot;
         c.rgl = fdiv(c.u, p.div_nseg);
         c.sg = c.u - c.rgl * nseg;
     };
@@ -630,9 +652,11 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         return r;
     };
     auto tok_scale = [&](float mt) { return tok_scale_k(mt > 0.f ? -ilogb_bits(mt) : 0); };
-    // whether the single-slot path below signals x_issued as soon as its
-    // loads are out (the other paths signal it with x_ready)
-    const bool x_issued_early = FMT != B200Q_F32 && nx == 1 && n_slots <= (kXB / 4) * nthr;
+    // x slots per thread per round trip (quantized formats), and whether one
+    // round trip stages all of x, so that x_issued is signalled as soon as its
+    // loads are out (otherwise together with x_ready)
+    constexpr int kG = 5;
+    const bool x_issued_early = FMT != B200Q_F32 && nx == 1 && n_slots <= kG * nthr;
     if constexpr (FMT == B200Q_F32) {
         for (int j = 0; j < nx; ++j)
             for (int base = 0; base < p.k_pad; base += kXB * nthr) {
@@ -663,44 +687,37 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
             for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
             if (lane == 0) atomicMax(tokmax + row, __float_as_uint(mt));
         };
-        constexpr int kG = kXB / 4;                   // slots per thread held in registers
-        if (nx == 1 && n_slots <= kG * nthr) {
-            // one x slot, one round trip: every load of the thread in flight at once
-            float4 held[NS][kG];
+        // Batches of kG slots per thread and token, every load of a batch in
+        // flight at once: one round trip to L2 per batch (one in all for
+        // x_issued_early).
+        for (int j = 0; j < nx; ++j) {
+            float mt[NS];
 #pragma unroll
-            for (int t = 0; t < NS; ++t)
+            for (int t = 0; t < NS; ++t) mt[t] = 0.f;
+            for (int b0 = 0; b0 < n_slots; b0 += kG * nthr) {
+                float4 held[NS][kG];
 #pragma unroll
-                for (int j = 0; j < kG; ++j) {
-                    const int d = j * nthr + tid;
-                    held[t][j] = d < n_slots ? gather(0, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(x_issued);
+                for (int t = 0; t < NS; ++t)
 #pragma unroll
-            for (int t = 0; t < NS; ++t) {
-                float mt = 0.f;
-#pragma unroll
-                for (int j = 0; j < kG; ++j) {
-                    const int d = j * nthr + tid;
-                    mt = fmaxf(mt, absmax4(held[t][j]));
-                    if (d < n_slots) put(xs + (size_t)t * k_alloc, d, held[t][j], ts_fix);
-                }
-                note_max(t, mt);
-            }
-        } else {
-            for (int j = 0; j < nx; ++j)
-#pragma unroll
-                for (int t = 0; t < NS; ++t) {
-                    float *dst = xs + (size_t)(j * NS + t) * k_alloc;
-                    float mt = 0.f;
-#pragma unroll 4
-                    for (int d = tid; d < n_slots; d += nthr) {
-                        const float4 v = gather(j, t, slot_src(d));
-                        mt = fmaxf(mt, absmax4(v));
-                        put(dst, d, v, ts_fix);
+                    for (int g = 0; g < kG; ++g) {
+                        const int d = b0 + g * nthr + tid;
+                        held[t][g] = d < n_slots ? gather(j, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    note_max(j * NS + t, mt);
+                if (x_issued_early) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(x_issued);
                 }
+#pragma unroll
+                for (int t = 0; t < NS; ++t)
+#pragma unroll
+                    for (int g = 0; g < kG; ++g) {
+                        const int d = b0 + g * nthr + tid;
+                        mt[t] = fmaxf(mt[t], absmax4(held[t][g]));
+                        if (d < n_slots) put(xs + (size_t)(j * NS + t) * k_alloc, d, held[t][g], ts_fix);
+                    }
+            }
+#pragma unroll
+            for (int t = 0; t < NS; ++t) note_max(j * NS + t, mt[t]);
         }
         if (tid < nxr) {
             unscale[2 * tid] = ts_fix.u1;
@@ -831,8 +848,10 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
                     ssc = reinterpret_cast<const float *>(my_ring + (size_t)c_stage * stg + kStage) +
                           (fdiv(sg * SEGE + lane * E, p.div_gs) - (fdiv(sg * SEGE, p.div_gs) & ~3));
                 uint4 cw[8];
+                if constexpr (!kRollQ) {
 #pragma unroll
-                for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rb);
+                    for (int r = 0; r < 8; ++r) cw[r] = *reinterpret_cast<const uint4 *>(st + r * rb);
+                }
                 if constexpr (FMT == B200Q_F32) {
                     const int k0 = (sg * (kSeg / 16) + lane) * E;
 #pragma unroll
@@ -847,6 +866,29 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
                         }
                     }
                     if (GW) fold_group(ssc);     // a chunk lies in one group
+                } else if constexpr (kRollQ) {
+                    // the chunk's 4 words in a loop (a body the instruction
+                    // cache holds); lane group lane / 8 starts at its own word,
+                    // so the warp's 4-byte code loads fall in 32 distinct banks
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        const int qq = (q + (lane >> 3)) & 3;
+                        float2 xv[NS * EW / 2];
+#pragma unroll
+                        for (int t = 0; t < NS; ++t)
+#pragma unroll
+                            for (int e4 = 0; e4 < EW; e4 += 4) {
+                                const float4 v4 = *reinterpret_cast<const float4 *>(
+                                    xsb + (size_t)t * k_alloc +
+                                    ((((size_t)sg * 4 + qq) * (EW / 4) + (e4 >> 2)) * 32 + lane) * 4);
+                                xv[t * (EW / 2) + e4 / 2] = make_float2(v4.x, v4.y);
+                                xv[t * (EW / 2) + e4 / 2 + 1] = make_float2(v4.z, v4.w);
+                            }
+#pragma unroll
+                        for (int r = 0; r < 8; ++r)
+                            word_fma2<FMT, NS, EW>(*reinterpret_cast<const uint32_t *>(st + r * rb + 4 * qq), xv, a2[r]);
+                        word_fma2<FMT, NS, EW>(F<FMT>::ZW, xv, az);
+                    }
                 } else {
                     // one 16-byte chunk = 4 words; x' for one word at a time
 #pragma unroll
@@ -981,7 +1023,6 @@ cudaError_t launch_ns(const DecParams<MS> &p, int grid, cudaStream_t st) {
     q.depth = depth;
     q.round_rgs = rr;
     q.div_grid = make_fastdiv((uint32_t)grid);
-    q.div_nw = make_fastdiv((uint32_t)nw);
     q.div_nseg = make_fastdiv((uint32_t)nseg);
     // programmatic dependent launch: this grid may start while the previous
     // kernel in the stream drains; it waits (griddepcontrol.wait) before it
