@@ -49,6 +49,44 @@ def test_f32_path_at_large_s(q, fmt):
     _check(q, fmt, 97, 200, 37, path=q.PATH_F32)
 
 
+@pytest.mark.parametrize("fmt", list(FMTS.values()), ids=list(FMTS))
+@pytest.mark.parametrize("S", [1, 2, 3, 4])
+def test_decode_staging_batches(q, fmt, S):
+    """The decode kernel (forced) with x too long for one staging round trip:
+    I = 20000 is 5000 x slots, two to four batches of five slots per thread
+    at one, two and four tokens per launch, and a ragged last segment."""
+    _check(q, fmt, 300, 20000, S, seed=S, path=q.PATH_F32)
+
+
+@pytest.mark.parametrize("fmt", [1, 2, 3], ids=["i8", "i4", "i2"])
+def test_decode_staging_batches_extreme_x(q, fmt):
+    """Several staging batches with tokens far from unit scale: the largest
+    |x| of a token is gathered across batches before the range check, and
+    out-of-range tokens are staged again with their own exponent."""
+    O, I, S = 64, 20000, 4
+    codes, scales, x = inputs(fmt, O, I, S, seed=23)
+    g = synth.rng(23, 5)
+    x = x.astype(np.float64)
+    x[0] = np.sign(x[0]) * g.uniform(1.0, 3.0, I) * 2.0 ** -140     # all subnormal in f32
+    x[1] = x[1] * 1e33
+    x[2, I - 5] = 1e3                                                # an outlier in the last batch
+    x[3] = 0.0
+    x = x.astype(np.float32)
+    y_ref, bound = oracle.matmul(fmt, O, I, codes, scales, x)
+    with q.tensor_upload(fmt, O, I, codes, scales) as t:
+        y = gpu_matmul(q, t, x, S, O, q.PATH_F32)
+    assert_within(y, y_ref, bound, TOL_F32, "staging batches, extreme x, fmt%d" % fmt)
+    assert np.all(y[3] == 0)
+
+
+@pytest.mark.parametrize("fmt", list(FMTS.values()), ids=list(FMTS))
+@pytest.mark.parametrize("O,I", [(7, 3), (129, 31), (130, 257), (64, 1000), (1000, 4096)])
+def test_decode_four_tokens_ragged(q, fmt, O, I):
+    """Four-token decode launches (the word loop of several-token launches)
+    on ragged shapes, every output."""
+    _check(q, fmt, O, I, 4, seed=O + I, path=q.PATH_F32)
+
+
 @pytest.mark.parametrize("fmt", [1, 2, 3], ids=["i8", "i4", "i2"])
 def test_onehot_dequant_bit_exact(q, fmt):
     """x = one-hot rows e_i: y[s,o] = RN_f32(scale[o] * deq(W[o,i])), a single
