@@ -350,10 +350,10 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     constexpr int SEGE = (kSeg / 16) * E;            // elements of a row in one stage
     constexpr int bits = FMT == B200Q_F32 ? 32 : FMT == B200Q_I8 ? 8 : FMT == B200Q_I4 ? 4 : 2;
     constexpr int EW = 32 / bits;                    // elements per 32-bit word
-    // several tokens with per-row scales: the unrolled body of a stage
-    // outgrows the instruction cache (no_instruction stalls led at four
-    // tokens), so its four words run as a loop
-    constexpr bool kRollQ = FMT != B200Q_F32 && NS >= 2 && GW == 0;
+    // four tokens with per-row scales: the unrolled body of a stage outgrows
+    // the instruction cache (no_instruction stalls led), so its four words
+    // run as a loop (measured slower at one and two tokens)
+    constexpr bool kRollQ = FMT != B200Q_F32 && NS >= 4 && GW == 0;
     constexpr int NV = 8 * NS;                       // partial sums per lane and row group
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -406,13 +406,13 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         int u, u_end;                // unit index within the round's run
         int rgl, sg;                 // u = rgl * nseg + sg
     };
-    // A round's units are shared out by the warps' schedulers (warp % 4):
-    // measured per-scheduler finish times fit a throughput of n / (n + 1) for
-    // n consumer warps on a scheduler (3 warps: 0.94 and 2 warps: 0.87 of a
-    // full scheduler's rate), so each warp's weight is 60 / (n + 1).  Even
-    // shares per warp left the 3-warp schedulers of a 10-warp launch (3, 3,
-    // 2, 2) with 30% more work than the rest.  wcum(w): the weights of the
-    // warps below w.
+    // Four-token launches share a round's units out by the warps' schedulers
+    // (warp % 4). Measured per-scheduler finish times fit a throughput of
+    // n / (n + 1) for n consumer warps on a scheduler (3 warps: 0.94 and
+    // 2 warps: 0.87 of a full scheduler's rate), so each warp's weight is
+    // 60 / (n + 1). Even shares per warp left the 3-warp schedulers of a
+    // 10-warp launch (3, 3, 2, 2) with 30% more work than the rest.
+    // wcum(w): the weights of the warps below w.
     auto wcum = [&](int w) {
         int c = 0;
 #pragma unroll
@@ -423,13 +423,17 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         }
         return c;
     };
-    const int wtot = wcum(nw);
     auto run_of = [&](Cursor &c, int base, int w) {
         c.round_base = base;
         c.round_end = base + kR < rg1 ? base + kR : rg1;
         const int U = (c.round_end - c.round_base) * nseg;
-        c.u = U * wcum(w) / wtot;
-        c.u_end = U * wcum(w + 1) / wtot;
+        // only the four-token launches (10 or 11 warps) take the scheduler
+        // weights; at 15 or 16 warps even shares per warp measured 1-2%
+        // faster, and the two-token group-scale builds (at the register
+        // limit) would spill for them
+        const int wtot = wcum(nw);   // recomputed here rather than held across the main loop
+        c.u = GW || NS < 4 ? w * U / nw : U * wcum(w) / wtot;
+        c.u_end = GW || NS < 4 ? (w + 1) * U / nw : U * wcum(w + 1) / wtot;
         c.rgl = fdiv(c.u, p.div_nseg);
         c.sg = c.u - c.rgl * nseg;
     };
@@ -652,11 +656,13 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         return r;
     };
     auto tok_scale = [&](float mt) { return tok_scale_k(mt > 0.f ? -ilogb_bits(mt) : 0); };
-    // x slots per thread per round trip (quantized formats), and whether one
-    // round trip stages all of x, so that x_issued is signalled as soon as its
-    // loads are out (otherwise together with x_ready)
+    // x slots per thread per round trip of the batched staging below, and
+    // whether x_issued is signalled as soon as x's loads are out: only on the
+    // one-slot path of kXB / 4 slots per thread.  Elsewhere it comes with
+    // x_ready: the rest of the weight rings then go out after x is staged,
+    // which measured faster (int4 8192^2: 11.7 against 13.0 us).
     constexpr int kG = 5;
-    const bool x_issued_early = FMT != B200Q_F32 && nx == 1 && n_slots <= kG * nthr;
+    const bool x_issued_early = FMT != B200Q_F32 && nx == 1 && n_slots <= (kXB / 4) * nthr;
     if constexpr (FMT == B200Q_F32) {
         for (int j = 0; j < nx; ++j)
             for (int base = 0; base < p.k_pad; base += kXB * nthr) {
@@ -687,9 +693,51 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
             for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
             if (lane == 0) atomicMax(tokmax + row, __float_as_uint(mt));
         };
+        constexpr int kG1 = kXB / 4;
+        if (nx == 1 && n_slots <= kG1 * nthr) {
+            // one x slot in one round trip of kG1 slots per thread: every load
+            // of the thread in flight at once (measured 1% faster at one token
+            // than the batched form below)
+            float4 held[NS][kG1];
+#pragma unroll
+            for (int t = 0; t < NS; ++t)
+#pragma unroll
+                for (int g = 0; g < kG1; ++g) {
+                    const int d = g * nthr + tid;
+                    held[t][g] = d < n_slots ? gather(0, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x_issued);
+#pragma unroll
+            for (int t = 0; t < NS; ++t) {
+                float mt = 0.f;
+#pragma unroll
+                for (int g = 0; g < kG1; ++g) {
+                    const int d = g * nthr + tid;
+                    mt = fmaxf(mt, absmax4(held[t][g]));
+                    if (d < n_slots) put(xs + (size_t)t * k_alloc, d, held[t][g], ts_fix);
+                }
+                note_max(t, mt);
+            }
+        } else if constexpr (NS >= 2 && GW != 0) {
+            // two tokens with group scales (no registers to spare): a loop
+            // over each token's slots, four loads in flight
+            for (int j = 0; j < nx; ++j)
+#pragma unroll
+                for (int t = 0; t < NS; ++t) {
+                    float *dst = xs + (size_t)(j * NS + t) * k_alloc;
+                    float mt = 0.f;
+#pragma unroll 4
+                    for (int d = tid; d < n_slots; d += nthr) {
+                        const float4 v = gather(j, t, slot_src(d));
+                        mt = fmaxf(mt, absmax4(v));
+                        put(dst, d, v, ts_fix);
+                    }
+                    note_max(j * NS + t, mt);
+                }
+        } else
         // Batches of kG slots per thread and token, every load of a batch in
-        // flight at once: one round trip to L2 per batch (one in all for
-        // x_issued_early).
+        // flight at once: one round trip to L2 per batch.
         for (int j = 0; j < nx; ++j) {
             float mt[NS];
 #pragma unroll
@@ -703,10 +751,6 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
                         const int d = b0 + g * nthr + tid;
                         held[t][g] = d < n_slots ? gather(j, t, slot_src(d)) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                if (x_issued_early) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(x_issued);
-                }
 #pragma unroll
                 for (int t = 0; t < NS; ++t)
 #pragma unroll
