@@ -406,8 +406,8 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         int u, u_end;                // unit index within the round's run
         int rgl, sg;                 // u = rgl * nseg + sg
     };
-    // Four-token launches share a round's units out by the warps' schedulers
-    // (warp % 4). Measured per-scheduler finish times fit a throughput of
+    // Quantized four-token launches share a round's units out by the warps'
+    // schedulers (warp % 4). Measured per-scheduler finish times fit a throughput of
     // n / (n + 1) for n consumer warps on a scheduler (3 warps: 0.94 and
     // 2 warps: 0.87 of a full scheduler's rate), so each warp's weight is
     // 60 / (n + 1). Even shares per warp left the 3-warp schedulers of a
@@ -427,13 +427,16 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
         c.round_base = base;
         c.round_end = base + kR < rg1 ? base + kR : rg1;
         const int U = (c.round_end - c.round_base) * nseg;
-        // only the four-token launches (10 or 11 warps) take the scheduler
-        // weights; at 15 or 16 warps even shares per warp measured 1-2%
-        // faster, and the two-token group-scale builds (at the register
-        // limit) would spill for them
+        // only the quantized four-token launches (10 or 11 warps, bound by
+        // the FMA pipe) take the scheduler weights; at 15 or 16 warps even
+        // shares per warp measured 1-2% faster, f32 streams at a rate set by
+        // each warp's ring (f32 8192^2 S = 8: 100 against 112 us weighted),
+        // and the two-token group-scale builds (at the register limit) would
+        // spill for them
+        constexpr bool kEven = GW || NS < 4 || FMT == B200Q_F32;
         const int wtot = wcum(nw);   // recomputed here rather than held across the main loop
-        c.u = GW || NS < 4 ? w * U / nw : U * wcum(w) / wtot;
-        c.u_end = GW || NS < 4 ? (w + 1) * U / nw : U * wcum(w + 1) / wtot;
+        c.u = kEven ? w * U / nw : U * wcum(w) / wtot;
+        c.u_end = kEven ? (w + 1) * U / nw : U * wcum(w + 1) / wtot;
         c.rgl = fdiv(c.u, p.div_nseg);
         c.sg = c.u - c.rgl * nseg;
     };
