@@ -37,8 +37,10 @@
 // reads one row's 512 contiguous bytes), so the x values it loads from shared
 // memory serve 8 rows; x is staged lane-interleaved so those loads are
 // conflict-free.  The units of a CTA are split into contiguous runs, one per
-// warp, in row-group-major order; a warp keeps its sums in registers across
-// the segments of a row group and combines its lanes (butterfly
+// warp, in row-group-major order (even shares per warp, or shares weighted by
+// the warps on each scheduler for quantized four-token launches, whose 10 or
+// 11 warps sit unevenly on the four schedulers); a warp keeps its sums in
+// registers across the segments of a row group and combines its lanes (butterfly
 // reduce-scatter) only when its row group changes.  The per-warp partial
 // sums of each row group are added in warp order after the run, in rounds of
 // at most 16 row groups.  Persistent CTAs own contiguous runs of row groups.
@@ -95,12 +97,11 @@ __device__ unsigned int g_decode_err = 0;
 
 template <int FMT>
 struct F;
-// E: elements per 16-byte chunk; ZW: a code word whose every code is the
-// zero point (int8: the byte 0, i.e. 128 after the sign flip)
+// E: elements per 16-byte chunk; ZW (quantized formats): a code word whose
+// every code is the zero point (int8: the byte 0, i.e. 128 after the sign flip)
 template <>
 struct F<B200Q_F32> {
     static constexpr int E = 4;
-    static constexpr uint32_t ZW = 0u;
 };
 template <>
 struct F<B200Q_I8> {
@@ -398,9 +399,10 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
     const int slot_lo = p.xslot[s_lo];
     const int nx = p.xslot[s_hi] - slot_lo + 1;       // x slots this CTA stages
 
-    // Consumer warp c's units: in round r (row groups [rg0 + kR r, ...)), the
-    // run [c U / nw, (c + 1) U / nw) of its U = rows * nseg units,
-    // row-group-major.  A cursor walks them in order across rounds.
+    // Consumer warp c's units: in round r (row groups [rg0 + kR r, ...)), a
+    // contiguous run of the round's U = rows * nseg units, row-group-major
+    // ([c U / nw, (c + 1) U / nw), or by scheduler weights, run_of below).
+    // A cursor walks them in order across rounds.
     struct Cursor {
         int round_base, round_end;   // row groups of the current round
         int u, u_end;                // unit index within the round's run
@@ -957,7 +959,9 @@ __global__ void __launch_bounds__((max_warps<FMT, NS, GW>() + 1) * 32, 1)
                             word_fma2<FMT, NS, EW>(w, xv, a2[r]);
                         }
                         word_fma2<FMT, NS, EW>(F<FMT>::ZW, xv, az);
-                        if (GW && (q + 1) % GW == 0) fold_group(ssc + q / GW);
+                        if constexpr (GW != 0) {
+                            if ((q + 1) % GW == 0) fold_group(ssc + q / GW);
+                        }
                     }
                 }
             }
